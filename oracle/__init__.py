@@ -1,0 +1,175 @@
+"""CPU oracle for the SparseLoCo pseudo-gradient codec.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline
+leg of ``bench.py`` may import this package.  The product path (the CUDA library and its
+binding in ``compressed_pseudo_gradient_gb300``) never imports, links or calls it, and this
+package never imports the product: the two share nothing but the seeded input generators.
+
+The arithmetic lives in ``spl_oracle.c`` (plain single-threaded C, built with
+``-O2 -ffp-contract=off``); this module only compiles it with gcc, loads it with ctypes and
+marshals numpy arrays.  Each wrapper names the page section the C function restates; see the
+header of ``spl_oracle.c`` for the readings taken where the pages leave a step open.
+
+bf16 arrays are passed as their uint16 bit patterns (numpy has no bfloat16).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "spl_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libspl_oracle.so")
+_CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+           "-Wall", "-Wextra"]
+
+_lock = threading.Lock()
+_lib = None
+
+CHUNK = 4096
+TOPK = 64
+RECORD_BYTES = 112
+FLAG_NONFINITE = 1
+FLAG_BAD_RECORD = 2
+
+
+def build(force: bool = False) -> str:
+    """Compile spl_oracle.c into a shared library next to it (if stale) and return its path."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", *_CFLAGS, "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        vp, i64, f32, u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_uint32
+        lib.orc_num_chunks.argtypes, lib.orc_num_chunks.restype = [i64], i64
+        lib.orc_topk_select.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp]
+        lib.orc_topk_select.restype = ctypes.c_int
+        lib.orc_scale.argtypes, lib.orc_scale.restype = [f32], f32
+        lib.orc_code.argtypes, lib.orc_code.restype = [f32, f32], ctypes.c_int
+        lib.orc_level.argtypes, lib.orc_level.restype = [ctypes.c_int, f32], f32
+        lib.orc_pack.argtypes, lib.orc_pack.restype = [vp, vp, i64, vp], None
+        lib.orc_unpack.argtypes, lib.orc_unpack.restype = [vp, i64, vp, vp], None
+        lib.orc_ef_compress.argtypes = [vp, ctypes.c_int, vp, i64, f32, vp, vp]
+        lib.orc_ef_compress.restype = u32
+        lib.orc_decode_aggregate.argtypes = [vp, vp, ctypes.c_int, i64, vp, vp, f32]
+        lib.orc_decode_aggregate.restype = u32
+        for name in ("orc_chunk", "orc_topk", "orc_record_bytes"):
+            getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data
+
+
+def constants() -> dict:
+    """Chunk length, k and record size as the C oracle states them."""
+    lib = _load()
+    return {"chunk": lib.orc_chunk(), "topk": lib.orc_topk(),
+            "record_bytes": lib.orc_record_bytes()}
+
+
+def num_chunks(n: int) -> int:
+    return int(_load().orc_num_chunks(n))
+
+
+def topk_select(a: np.ndarray, k: int) -> tuple[np.ndarray, int]:
+    """Chunk top-k by |a| (ties to the lower index), ascending; also the first-ranked index.
+
+    The Sparse Frontier, "SparseLoCo: Three Compression Levers in One Pass", item 1.
+    """
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    out = np.zeros(k, dtype=np.int32)
+    top = _load().orc_topk_select(_ptr(a), a.size, k, _ptr(out))
+    return out, int(top)
+
+
+def scale(m: float) -> np.float32:
+    return np.float32(_load().orc_scale(m))
+
+
+def code(v: float, s: float) -> int:
+    return int(_load().orc_code(v, s))
+
+
+def level(c: int, s: float) -> np.float32:
+    return np.float32(_load().orc_level(c, s))
+
+
+def pack(idx: np.ndarray, codes: np.ndarray) -> np.ndarray:
+    """(idx[C,64] u16, codes[C,64] u8) -> payload[C,112] u8 (bit-at-a-time writer)."""
+    idx = np.ascontiguousarray(idx, dtype=np.uint16).reshape(-1, TOPK)
+    codes = np.ascontiguousarray(codes, dtype=np.uint8).reshape(-1, TOPK)
+    C = idx.shape[0]
+    out = np.zeros((C, RECORD_BYTES), dtype=np.uint8)
+    _load().orc_pack(_ptr(idx), _ptr(codes), C, _ptr(out))
+    return out
+
+
+def unpack(payload: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    payload = np.ascontiguousarray(payload, dtype=np.uint8).reshape(-1, RECORD_BYTES)
+    C = payload.shape[0]
+    idx = np.zeros((C, TOPK), dtype=np.uint16)
+    codes = np.zeros((C, TOPK), dtype=np.uint8)
+    _load().orc_unpack(_ptr(payload), C, _ptr(idx), _ptr(codes))
+    return idx, codes
+
+
+def ef_compress(delta: np.ndarray, ef: np.ndarray, beta: float, *, bf16: bool = False):
+    """One sender round; ``ef`` (fp32) is updated in place.
+
+    ``delta`` is fp32, or with ``bf16=True`` a uint16 array of bf16 bit patterns.
+    Returns (payload[C,112] u8, scales[C] f32, flags).
+    """
+    if bf16:
+        delta = np.ascontiguousarray(delta, dtype=np.uint16)
+    else:
+        delta = np.ascontiguousarray(delta, dtype=np.float32)
+    assert ef.dtype == np.float32 and ef.flags["C_CONTIGUOUS"] and ef.size == delta.size
+    n = delta.size
+    C = num_chunks(n)
+    payload = np.zeros((C, RECORD_BYTES), dtype=np.uint8)
+    scales = np.zeros(C, dtype=np.float32)
+    flags = _load().orc_ef_compress(_ptr(delta), 1 if bf16 else 0, _ptr(ef), n,
+                                    np.float32(beta), _ptr(payload), _ptr(scales))
+    return payload, scales, int(flags)
+
+
+def decode_aggregate(payloads, scales, n: int, theta: np.ndarray | None = None,
+                     lr: float = 0.0):
+    """Mean of P peers' decoded records; with ``theta`` also theta -= lr * mean (in place).
+
+    Returns (mean[n] f32, flags).
+    """
+    P = len(payloads)
+    assert P == len(scales) and P >= 1
+    C = num_chunks(n)
+    pl = [np.ascontiguousarray(p, dtype=np.uint8).reshape(C, RECORD_BYTES) for p in payloads]
+    sc = [np.ascontiguousarray(s, dtype=np.float32).reshape(C) for s in scales]
+    parr = (ctypes.c_void_p * P)(*[_ptr(p) for p in pl])
+    sarr = (ctypes.c_void_p * P)(*[_ptr(s) for s in sc])
+    mean = np.zeros(n, dtype=np.float32)
+    tptr = None
+    if theta is not None:
+        assert theta.dtype == np.float32 and theta.flags["C_CONTIGUOUS"] and theta.size == n
+        tptr = _ptr(theta)
+    flags = _load().orc_decode_aggregate(parr, sarr, P, n, _ptr(mean), tptr, np.float32(lr))
+    return mean, int(flags)
