@@ -1,0 +1,31 @@
+"""SparseLoCo pseudo-gradient codec on one GB300 (sm_103a).
+
+A thin binding over the C ABI of ``libspl.so`` (declared in ``include/spl.h``): each function
+checks the torch tensors it is given, passes their device pointers and the current CUDA
+stream to the library, and raises on a non-OK status.  Every step of the codec runs in the
+library's CUDA kernels; there is no CPU path.  The library is loaded on first use, and a
+missing or unloadable library raises instead of falling back.
+
+The codec: "The Sparse Frontier: SparseLoCo and the Compression Math Behind Permissionless
+Pre-Training", "SparseLoCo: Three Compression Levers in One Pass" and "Why Extreme Sparsity
+Doesn't Break Convergence".
+"""
+from __future__ import annotations
+
+from ._binding import (  # noqa: F401
+    CHUNK,
+    FLAG_BAD_RECORD,
+    FLAG_NONFINITE,
+    MAX_PEERS,
+    RECORD_BYTES,
+    TOPK,
+    SplError,
+    decode_aggregate,
+    ef_compress,
+    ef_compress_multi,
+    library,
+    library_path,
+    num_chunks,
+    pack,
+    unpack,
+)

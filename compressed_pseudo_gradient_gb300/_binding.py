@@ -1,0 +1,256 @@
+"""ctypes binding of libspl.so: argument marshalling only (torch tensors -> device pointers).
+
+Function names follow the C ABI in include/spl.h without the ``spl_`` prefix.  Outputs that
+the caller does not pass are allocated with torch on the input's device; the library itself
+allocates nothing.  All work is enqueued on ``torch.cuda.current_stream()`` of the inputs'
+device and is not waited for.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+CHUNK = 4096
+TOPK = 64
+RECORD_BYTES = 112
+MAX_PEERS = 256
+FLAG_NONFINITE = 1
+FLAG_BAD_RECORD = 2
+
+_F32, _BF16 = 0, 1
+_lock = threading.Lock()
+_lib = None
+
+
+class SplError(RuntimeError):
+    """A non-OK status from libspl (argument error, alignment error or CUDA failure)."""
+
+    def __init__(self, fn: str, status: int, cuda_error: int = 0):
+        lib = _lib
+        text = lib.spl_status_string(status).decode() if lib is not None else str(status)
+        msg = f"{fn}: {text} (status {status})"
+        if status == 3:
+            msg += f", cudaError {cuda_error}"
+        super().__init__(msg)
+        self.status = status
+        self.cuda_error = cuda_error
+
+
+class _Tensor(ctypes.Structure):
+    _fields_ = [("delta", ctypes.c_void_p), ("ef", ctypes.c_void_p), ("n", ctypes.c_size_t)]
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def library():
+    """The loaded libspl.so (built first if missing or older than its sources)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if _build.is_stale():
+            _build.build()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libspl.so is missing at {path}; the CUDA library must be built")
+        lib = ctypes.CDLL(path)
+        vp, sz, ci, cf = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_float
+        lib.spl_num_chunks.argtypes, lib.spl_num_chunks.restype = [sz], sz
+        lib.spl_status_string.argtypes, lib.spl_status_string.restype = [ci], ctypes.c_char_p
+        lib.spl_last_cuda_error.argtypes, lib.spl_last_cuda_error.restype = [], ci
+        lib.spl_ef_compress.argtypes = [vp, ci, vp, sz, cf, vp, vp, vp, vp]
+        lib.spl_ef_compress.restype = ci
+        lib.spl_ef_compress_multi.argtypes = [ctypes.POINTER(_Tensor), ci, ci, cf, vp, vp, vp, vp]
+        lib.spl_ef_compress_multi.restype = ci
+        lib.spl_decode_aggregate.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), ci, sz, vp,
+                                             vp, cf, vp, vp]
+        lib.spl_decode_aggregate.restype = ci
+        lib.spl_pack.argtypes, lib.spl_pack.restype = [vp, vp, sz, vp, vp], ci
+        lib.spl_unpack.argtypes, lib.spl_unpack.restype = [vp, sz, vp, vp, vp], ci
+        _lib = lib
+        return lib
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        lib = library()
+        raise SplError(fn, status, lib.spl_last_cuda_error() if status == 3 else 0)
+
+
+def _cuda(t: torch.Tensor, name: str, dtypes) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}; expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _stream(dev: torch.device) -> int:
+    return torch.cuda.current_stream(dev).cuda_stream
+
+
+def _flags_ptr(flags, dev):
+    if flags is None:
+        return None
+    _cuda(flags, "flags", (torch.int32,))
+    if flags.numel() < 1 or flags.device != dev:
+        raise ValueError("flags must be a 1-element int32 tensor on the inputs' device")
+    return flags.data_ptr()
+
+
+def num_chunks(n: int) -> int:
+    return (int(n) + CHUNK - 1) // CHUNK
+
+
+def ef_compress(delta: torch.Tensor, ef: torch.Tensor, beta: float, *, payload=None,
+                scales=None, flags=None):
+    """One sender round (spl_ef_compress); ``ef`` is updated in place.
+
+    delta: fp32 or bf16 CUDA tensor of n values; ef: fp32 CUDA tensor of n values.
+    Returns (payload uint8 [C, 112], scales fp32 [C]).
+    """
+    lib = library()
+    _cuda(delta, "delta", (torch.float32, torch.bfloat16))
+    _cuda(ef, "ef", (torch.float32,))
+    if ef.numel() != delta.numel() or ef.device != delta.device:
+        raise ValueError("delta and ef must have the same size and device")
+    dev = delta.device
+    n = delta.numel()
+    C = num_chunks(n)
+    if payload is None:
+        payload = torch.empty((C, RECORD_BYTES), dtype=torch.uint8, device=dev)
+    if scales is None:
+        scales = torch.empty(C, dtype=torch.float32, device=dev)
+    _cuda(payload, "payload", (torch.uint8,))
+    _cuda(scales, "scales", (torch.float32,))
+    if payload.numel() < C * RECORD_BYTES or scales.numel() < C:
+        raise ValueError("payload/scales too small")
+    with torch.cuda.device(dev):
+        st = lib.spl_ef_compress(delta.data_ptr(), _BF16 if delta.dtype == torch.bfloat16 else _F32,
+                                 ef.data_ptr(), n, float(beta), payload.data_ptr(),
+                                 scales.data_ptr(), _flags_ptr(flags, dev), _stream(dev))
+    _check("spl_ef_compress", st)
+    return payload, scales
+
+
+def ef_compress_multi(deltas, efs, beta: float, *, payload=None, scales=None, flags=None):
+    """One sender round over a list of tensors, each chunked on its own (spl_ef_compress_multi).
+
+    Returns (payload uint8 [sum C_i, 112], scales fp32 [sum C_i]) in tensor order.
+    """
+    lib = library()
+    if len(deltas) != len(efs) or not deltas:
+        raise ValueError("deltas and efs must be non-empty lists of equal length")
+    dtype = deltas[0].dtype
+    dev = deltas[0].device
+    table = (_Tensor * len(deltas))()
+    C = 0
+    for i, (d, e) in enumerate(zip(deltas, efs)):
+        _cuda(d, f"deltas[{i}]", (torch.float32, torch.bfloat16))
+        _cuda(e, f"efs[{i}]", (torch.float32,))
+        if d.dtype != dtype or d.device != dev or e.device != dev or e.numel() != d.numel():
+            raise ValueError(f"tensor {i}: dtype/device/size mismatch")
+        table[i].delta = d.data_ptr() if d.numel() else None
+        table[i].ef = e.data_ptr() if e.numel() else None
+        table[i].n = d.numel()
+        C += num_chunks(d.numel())
+    if payload is None:
+        payload = torch.empty((C, RECORD_BYTES), dtype=torch.uint8, device=dev)
+    if scales is None:
+        scales = torch.empty(C, dtype=torch.float32, device=dev)
+    _cuda(payload, "payload", (torch.uint8,))
+    _cuda(scales, "scales", (torch.float32,))
+    if payload.numel() < C * RECORD_BYTES or scales.numel() < C:
+        raise ValueError("payload/scales too small")
+    with torch.cuda.device(dev):
+        st = lib.spl_ef_compress_multi(table, len(deltas),
+                                       _BF16 if dtype == torch.bfloat16 else _F32, float(beta),
+                                       payload.data_ptr() if C else None,
+                                       scales.data_ptr() if C else None,
+                                       _flags_ptr(flags, dev), _stream(dev))
+    _check("spl_ef_compress_multi", st)
+    return payload, scales
+
+
+def decode_aggregate(payloads, scales, n: int, *, mean=None, theta=None, lr: float = 0.0,
+                     flags=None):
+    """Mean of P peers' decoded records, optionally fused with theta -= lr * mean in place
+    (spl_decode_aggregate).  Returns mean (fp32 [n])."""
+    lib = library()
+    P = len(payloads)
+    if P != len(scales) or P < 1:
+        raise ValueError("payloads and scales must be non-empty lists of equal length")
+    dev = payloads[0].device
+    C = num_chunks(n)
+    for i, (p, s) in enumerate(zip(payloads, scales)):
+        _cuda(p, f"payloads[{i}]", (torch.uint8,))
+        _cuda(s, f"scales[{i}]", (torch.float32,))
+        if p.device != dev or s.device != dev or p.numel() < C * RECORD_BYTES or s.numel() < C:
+            raise ValueError(f"peer {i}: device mismatch or arrays too small")
+    if mean is None:
+        mean = torch.empty(n, dtype=torch.float32, device=dev)
+    _cuda(mean, "mean", (torch.float32,))
+    if mean.numel() < n or mean.device != dev:
+        raise ValueError("mean too small or on another device")
+    tptr = None
+    if theta is not None:
+        _cuda(theta, "theta", (torch.float32,))
+        if theta.numel() < n or theta.device != dev:
+            raise ValueError("theta too small or on another device")
+        tptr = theta.data_ptr()
+    parr = (ctypes.c_void_p * P)(*[p.data_ptr() for p in payloads])
+    sarr = (ctypes.c_void_p * P)(*[s.data_ptr() for s in scales])
+    with torch.cuda.device(dev):
+        st = lib.spl_decode_aggregate(parr, sarr, P, int(n), mean.data_ptr(), tptr, float(lr),
+                                      _flags_ptr(flags, dev), _stream(dev))
+    _check("spl_decode_aggregate", st)
+    return mean
+
+
+def pack(idx: torch.Tensor, codes: torch.Tensor, *, payload=None):
+    """(idx int16/uint16-as-int16 [C, 64], codes uint8 [C, 64]) -> payload uint8 [C, 112]."""
+    lib = library()
+    _cuda(idx, "idx", (torch.int16,))
+    _cuda(codes, "codes", (torch.uint8,))
+    C = idx.numel() // TOPK
+    if idx.numel() != C * TOPK or codes.numel() != C * TOPK:
+        raise ValueError("idx and codes must hold C x 64 entries")
+    dev = idx.device
+    if payload is None:
+        payload = torch.empty((C, RECORD_BYTES), dtype=torch.uint8, device=dev)
+    _cuda(payload, "payload", (torch.uint8,))
+    with torch.cuda.device(dev):
+        st = lib.spl_pack(idx.data_ptr(), codes.data_ptr(), C, payload.data_ptr(), _stream(dev))
+    _check("spl_pack", st)
+    return payload
+
+
+def unpack(payload: torch.Tensor, *, idx=None, codes=None):
+    """payload uint8 [C, 112] -> (idx int16 [C, 64] holding 0..4095, codes uint8 [C, 64])."""
+    lib = library()
+    _cuda(payload, "payload", (torch.uint8,))
+    C = payload.numel() // RECORD_BYTES
+    if payload.numel() != C * RECORD_BYTES:
+        raise ValueError("payload must hold C x 112 bytes")
+    dev = payload.device
+    if idx is None:
+        idx = torch.empty((C, TOPK), dtype=torch.int16, device=dev)
+    if codes is None:
+        codes = torch.empty((C, TOPK), dtype=torch.uint8, device=dev)
+    _cuda(idx, "idx", (torch.int16,))
+    _cuda(codes, "codes", (torch.uint8,))
+    with torch.cuda.device(dev):
+        st = lib.spl_unpack(payload.data_ptr(), C, idx.data_ptr(), codes.data_ptr(), _stream(dev))
+    _check("spl_unpack", st)
+    return idx, codes

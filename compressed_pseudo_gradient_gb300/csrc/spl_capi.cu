@@ -1,0 +1,223 @@
+// C ABI of the codec (declared in include/spl.h): argument checks on the host, then
+// stream-ordered kernel launches.  Nothing here allocates device memory or synchronises.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "spl.h"
+#include "spl_kernels.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+spl_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return SPL_OK;
+    g_last_cuda_error = static_cast<int>(e);
+    return SPL_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Byte ranges [p, p + n) and [q, q + m) share a byte.
+bool overlap(const void* p, size_t n, const void* q, size_t m) {
+    if (p == nullptr || q == nullptr || n == 0 || m == 0) return false;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
+    return a < b + m && b < a + n;
+}
+
+constexpr size_t kMaxChunks = 0x7fffffff;   // chunk indices stay below 2^31
+
+}  // namespace
+
+namespace spl {
+
+// Resident CTAs of a kernel on the current device (SMs x blocks per SM).  The device's SM
+// count is read once per device; the occupancy query is a host-side computation.
+int persistent_grid(const void* kernel, int threads, size_t dyn_smem) {
+    static std::mutex mu;
+    static int sm_count[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+    int sms;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (sm_count[dev] == 0 &&
+            cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev) !=
+                cudaSuccess)
+            return -1;
+        sms = sm_count[dev];
+    }
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, dyn_smem) !=
+        cudaSuccess)
+        return -1;
+    return sms * (per_sm > 0 ? per_sm : 1);
+}
+
+}  // namespace spl
+
+extern "C" {
+
+size_t spl_num_chunks(size_t n) { return n / SPL_CHUNK + (n % SPL_CHUNK != 0); }
+
+const char* spl_status_string(int status) {
+    switch (status) {
+        case SPL_OK: return "ok";
+        case SPL_ERR_INVALID_ARG: return "invalid argument";
+        case SPL_ERR_ALIGNMENT: return "misaligned pointer";
+        case SPL_ERR_CUDA: return "CUDA error";
+        default: return "unknown status";
+    }
+}
+
+int spl_last_cuda_error(void) { return g_last_cuda_error; }
+
+static spl_status check_tensor(const void* delta, spl_dtype dt, const float* ef, size_t n) {
+    if (n == 0) return SPL_OK;
+    if (delta == nullptr || ef == nullptr) return SPL_ERR_INVALID_ARG;
+    if (dt != SPL_F32 && dt != SPL_BF16) return SPL_ERR_INVALID_ARG;
+    if (spl_num_chunks(n) > kMaxChunks) return SPL_ERR_INVALID_ARG;
+    if (!aligned(delta, 16) || !aligned(ef, 16)) return SPL_ERR_ALIGNMENT;
+    const size_t esz = dt == SPL_F32 ? 4 : 2;
+    if (overlap(delta, n * esz, ef, n * 4)) return SPL_ERR_INVALID_ARG;
+    return SPL_OK;
+}
+
+static spl_status check_outputs(const spl_tensor* t, int num, spl_dtype dt, const uint8_t* payload,
+                                const float* scales, const uint32_t* flags, size_t C) {
+    if (C == 0) return SPL_OK;
+    if (payload == nullptr || scales == nullptr) return SPL_ERR_INVALID_ARG;
+    if (!aligned(payload, 16) || !aligned(scales, 4) || !aligned(flags, 4))
+        return SPL_ERR_ALIGNMENT;
+    const size_t esz = dt == SPL_F32 ? 4 : 2;
+    if (overlap(payload, C * SPL_RECORD_BYTES, scales, C * 4)) return SPL_ERR_INVALID_ARG;
+    for (int i = 0; i < num; ++i) {
+        const size_t n = t[i].n;
+        if (overlap(payload, C * SPL_RECORD_BYTES, t[i].delta, n * esz) ||
+            overlap(payload, C * SPL_RECORD_BYTES, t[i].ef, n * 4) ||
+            overlap(scales, C * 4, t[i].delta, n * esz) || overlap(scales, C * 4, t[i].ef, n * 4) ||
+            overlap(flags, 4, t[i].ef, n * 4) || overlap(flags, 4, t[i].delta, n * esz))
+            return SPL_ERR_INVALID_ARG;
+        for (int k = 0; k < i; ++k)
+            if (overlap(t[k].ef, t[k].n * 4, t[i].ef, n * 4) ||
+                overlap(t[k].ef, t[k].n * 4, t[i].delta, n * esz) ||
+                overlap(t[i].ef, n * 4, t[k].delta, t[k].n * esz))
+                return SPL_ERR_INVALID_ARG;
+    }
+    return SPL_OK;
+}
+
+spl_status spl_ef_compress_multi(const spl_tensor* tensors, int num_tensors, spl_dtype delta_dtype,
+                                 float beta, uint8_t* payload, float* scales, uint32_t* d_flags,
+                                 spl_stream_t stream) {
+    if (tensors == nullptr || num_tensors < 1) return SPL_ERR_INVALID_ARG;
+    if (delta_dtype != SPL_F32 && delta_dtype != SPL_BF16) return SPL_ERR_INVALID_ARG;
+    if (!std::isfinite(beta)) return SPL_ERR_INVALID_ARG;
+    size_t C = 0;
+    for (int i = 0; i < num_tensors; ++i) {
+        const spl_status st = check_tensor(tensors[i].delta, delta_dtype, tensors[i].ef, tensors[i].n);
+        if (st != SPL_OK) return st;
+        C += spl_num_chunks(tensors[i].n);
+        if (C > kMaxChunks) return SPL_ERR_INVALID_ARG;
+    }
+    const spl_status st = check_outputs(tensors, num_tensors, delta_dtype, payload, scales, d_flags, C);
+    if (st != SPL_OK) return st;
+    if (C == 0) return SPL_OK;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    size_t chunk0 = 0;
+    for (int first = 0; first < num_tensors; first += spl::kMaxTensorsPerLaunch) {
+        spl::CompressTable tab;
+        std::memset(&tab, 0, sizeof tab);
+        const int count = num_tensors - first < spl::kMaxTensorsPerLaunch
+                              ? num_tensors - first : spl::kMaxTensorsPerLaunch;
+        int64_t chunks = 0;
+        for (int i = 0; i < count; ++i) {
+            tab.delta[i] = tensors[first + i].delta;
+            tab.ef[i] = tensors[first + i].ef;
+            tab.n[i] = static_cast<int64_t>(tensors[first + i].n);
+            tab.chunk_begin[i] = chunks;
+            chunks += static_cast<int64_t>(spl_num_chunks(tensors[first + i].n));
+        }
+        tab.chunk_begin[count] = chunks;
+        tab.num = count;
+        const spl_status ls = cuda_status(spl::launch_ef_compress(
+            tab, delta_dtype == SPL_BF16, beta, payload + chunk0 * SPL_RECORD_BYTES,
+            scales + chunk0, d_flags, s));
+        if (ls != SPL_OK) return ls;
+        chunk0 += static_cast<size_t>(chunks);
+    }
+    return SPL_OK;
+}
+
+spl_status spl_ef_compress(const void* delta, spl_dtype delta_dtype, float* ef, size_t n,
+                           float beta, uint8_t* payload, float* scales, uint32_t* d_flags,
+                           spl_stream_t stream) {
+    const spl_tensor t = {delta, ef, n};
+    if (n == 0) {
+        if (delta_dtype != SPL_F32 && delta_dtype != SPL_BF16) return SPL_ERR_INVALID_ARG;
+        return std::isfinite(beta) ? SPL_OK : SPL_ERR_INVALID_ARG;
+    }
+    return spl_ef_compress_multi(&t, 1, delta_dtype, beta, payload, scales, d_flags, stream);
+}
+
+spl_status spl_decode_aggregate(const uint8_t* const* payloads, const float* const* scales, int P,
+                                size_t n, float* mean_out, float* theta, float lr,
+                                uint32_t* d_flags, spl_stream_t stream) {
+    if (P < 1 || P > SPL_MAX_PEERS) return SPL_ERR_INVALID_ARG;
+    if (theta != nullptr && !std::isfinite(lr)) return SPL_ERR_INVALID_ARG;
+    if (n == 0) return SPL_OK;
+    if (payloads == nullptr || scales == nullptr || mean_out == nullptr) return SPL_ERR_INVALID_ARG;
+    const size_t C = spl_num_chunks(n);
+    if (C > kMaxChunks) return SPL_ERR_INVALID_ARG;
+    if (!aligned(mean_out, 16) || !aligned(theta, 16) || !aligned(d_flags, 4))
+        return SPL_ERR_ALIGNMENT;
+    if (overlap(mean_out, n * 4, theta, n * 4)) return SPL_ERR_INVALID_ARG;
+    if (overlap(d_flags, 4, mean_out, n * 4) || overlap(d_flags, 4, theta, n * 4))
+        return SPL_ERR_INVALID_ARG;
+    spl::DecodeTable tab;
+    std::memset(&tab, 0, sizeof tab);
+    for (int p = 0; p < P; ++p) {
+        if (payloads[p] == nullptr || scales[p] == nullptr) return SPL_ERR_INVALID_ARG;
+        if (!aligned(payloads[p], 16) || !aligned(scales[p], 4)) return SPL_ERR_ALIGNMENT;
+        if (overlap(payloads[p], C * SPL_RECORD_BYTES, mean_out, n * 4) ||
+            overlap(payloads[p], C * SPL_RECORD_BYTES, theta, n * 4) ||
+            overlap(scales[p], C * 4, mean_out, n * 4) || overlap(scales[p], C * 4, theta, n * 4))
+            return SPL_ERR_INVALID_ARG;
+        tab.payload[p] = payloads[p];
+        tab.scale[p] = scales[p];
+    }
+    return cuda_status(spl::launch_decode_aggregate(tab, P, static_cast<int64_t>(n), mean_out,
+                                                    theta, lr, d_flags,
+                                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+spl_status spl_pack(const uint16_t* idx, const uint8_t* codes, size_t num_chunks, uint8_t* payload,
+                    spl_stream_t stream) {
+    if (num_chunks == 0) return SPL_OK;
+    if (idx == nullptr || codes == nullptr || payload == nullptr || num_chunks > kMaxChunks)
+        return SPL_ERR_INVALID_ARG;
+    if (!aligned(idx, 2) || !aligned(payload, 16)) return SPL_ERR_ALIGNMENT;
+    if (overlap(payload, num_chunks * SPL_RECORD_BYTES, idx, num_chunks * SPL_TOPK * 2) ||
+        overlap(payload, num_chunks * SPL_RECORD_BYTES, codes, num_chunks * SPL_TOPK))
+        return SPL_ERR_INVALID_ARG;
+    return cuda_status(spl::launch_pack(idx, codes, static_cast<int64_t>(num_chunks), payload,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+spl_status spl_unpack(const uint8_t* payload, size_t num_chunks, uint16_t* idx, uint8_t* codes,
+                      spl_stream_t stream) {
+    if (num_chunks == 0) return SPL_OK;
+    if (idx == nullptr || codes == nullptr || payload == nullptr || num_chunks > kMaxChunks)
+        return SPL_ERR_INVALID_ARG;
+    if (!aligned(idx, 2) || !aligned(payload, 16)) return SPL_ERR_ALIGNMENT;
+    if (overlap(payload, num_chunks * SPL_RECORD_BYTES, idx, num_chunks * SPL_TOPK * 2) ||
+        overlap(payload, num_chunks * SPL_RECORD_BYTES, codes, num_chunks * SPL_TOPK) ||
+        overlap(idx, num_chunks * SPL_TOPK * 2, codes, num_chunks * SPL_TOPK))
+        return SPL_ERR_INVALID_ARG;
+    return cuda_status(spl::launch_unpack(payload, static_cast<int64_t>(num_chunks), idx, codes,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

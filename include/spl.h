@@ -1,0 +1,156 @@
+/*
+ * spl.h: C ABI of the SparseLoCo pseudo-gradient codec on one GPU.
+ *
+ * The codec is defined in "The Sparse Frontier: SparseLoCo and the Compression Math Behind
+ * Permissionless Pre-Training" (blokz.dev), section "SparseLoCo: Three Compression Levers in
+ * One Pass" (items 1-3 and the per-chunk size equation) and section "Why Extreme Sparsity
+ * Doesn't Break Convergence" (error feedback; aggregation of the peers' sparse updates).
+ * The pages name no interface; these calls follow the steps the pages list.
+ *
+ * Fixed format (both sides of the wire):
+ *   - a pseudo-gradient of n values is cut into C = ceil(n / 4096) chunks of 4096 values; a
+ *     tail chunk is padded with zeros (the pads are never read from or written to memory);
+ *   - per chunk, the 64 entries of largest |a| are kept (ties go to the lower in-chunk index;
+ *     a NaN ranks above every number, and all NaNs rank equal);
+ *   - scale s = m / 1.5f (fp32, round to nearest), m = max |a| over the chunk;
+ *     2-bit code = (sign << 1) | mag with sign = (v < 0) and mag = (|v| > s); the decoded
+ *     value is +-0.5f*s (mag 0) or +-1.5f*s (mag 1);
+ *   - the record of a chunk is 112 bytes: entry r (r = 0..63, indices ascending) is the
+ *     14-bit field (code | idx << 2) at bits [14r, 14r + 14) of a 896-bit little-endian bit
+ *     string, least significant bit first (equivalently 28 little-endian uint32 words);
+ *   - the scales are a separate array of C fp32 values, so every record is 16-byte aligned.
+ *
+ * Conventions for every call:
+ *   - pointers named d_* or documented as "device" are device memory owned by the caller;
+ *     the library allocates nothing and keeps no per-call state;
+ *   - work is enqueued on `stream` (NULL = the legacy default stream) and never waited for:
+ *     results are valid once the stream has reached the call;
+ *   - argument errors are found on the host before anything is enqueued and returned
+ *     synchronously; SPL_ERR_CUDA means a launch failed (spl_last_cuda_error() gives the
+ *     cudaError_t value on the calling thread);
+ *   - conditions found on the device are OR-ed into *d_flags (if d_flags is not NULL), which
+ *     the caller reads after synchronising: SPL_FLAG_NONFINITE, SPL_FLAG_BAD_RECORD;
+ *   - device pointers to fp32/bf16 dense arrays and to records must be 16-byte aligned;
+ *     scales and flags 4-byte aligned; idx 2-byte aligned.
+ */
+#ifndef SPL_H_
+#define SPL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* spl_stream_t; /* a cudaStream_t */
+
+typedef enum {
+    SPL_OK = 0,
+    SPL_ERR_INVALID_ARG = 1, /* NULL pointer, bad size, non-finite beta/lr, overlap, bad dtype */
+    SPL_ERR_ALIGNMENT = 2,   /* a pointer breaks the alignment rule above */
+    SPL_ERR_CUDA = 3         /* a CUDA call failed; see spl_last_cuda_error() */
+} spl_status;
+
+typedef enum { SPL_F32 = 0, SPL_BF16 = 1 } spl_dtype;
+
+enum {
+    SPL_CHUNK = 4096,        /* "chunks of 4,096 parameters" (item 1) */
+    SPL_TOPK = 64,           /* "top-64 values by absolute magnitude" (item 1) */
+    SPL_RECORD_BYTES = 112,  /* "64 x 14 bits = 896 bits = 112 bytes" (per-chunk equation) */
+    SPL_MAX_PEERS = 256,     /* largest P accepted by spl_decode_aggregate */
+    SPL_MAX_TENSORS_PER_LAUNCH = 64 /* spl_ef_compress_multi splits larger tables */
+};
+
+enum { SPL_FLAG_NONFINITE = 1u, SPL_FLAG_BAD_RECORD = 2u };
+
+/* Number of 4096-value chunks of an n-value tensor: ceil(n / 4096). */
+size_t spl_num_chunks(size_t n);
+
+/* Static English text for a status code (never NULL). */
+const char* spl_status_string(int status);
+
+/* cudaError_t value of the last SPL_ERR_CUDA returned on the calling thread (0 if none). */
+int spl_last_cuda_error(void);
+
+/*
+ * Sender, one round: error feedback, chunk top-64, 2-bit quantisation, packing and the
+ * residual, fused in one pass over the tensor (items 1-3; "Error feedback accumulation").
+ *
+ *   a      = fmaf(beta, ef[i], delta[i])          (bf16 delta is widened exactly first)
+ *   record = the 64 entries of largest |a| per chunk, as above
+ *   ef[i]  = a - q[i] at the 64 kept positions (q = decoded value), a elsewhere
+ *
+ * delta:   device, n values of type delta_dtype (SPL_F32 or SPL_BF16), read only
+ * ef:      device, n fp32 values, read and overwritten (the error-feedback buffer)
+ * n:       number of values; n = 0 does nothing and accepts NULL pointers
+ * beta:    error-feedback decay, finite
+ * payload: device, spl_num_chunks(n) * 112 bytes, written
+ * scales:  device, spl_num_chunks(n) fp32, written
+ * d_flags: device uint32 or NULL; SPL_FLAG_NONFINITE is OR-ed in when some a is not finite
+ *          (the records are still written, deterministically)
+ * Outputs must not overlap the inputs or each other.
+ */
+spl_status spl_ef_compress(const void* delta, spl_dtype delta_dtype, float* ef, size_t n,
+                           float beta, uint8_t* payload, float* scales, uint32_t* d_flags,
+                           spl_stream_t stream);
+
+/* One tensor of a multi-tensor round: chunks never span two tensors. */
+typedef struct {
+    const void* delta; /* device, n values of the call's delta_dtype */
+    float* ef;         /* device, n fp32 */
+    size_t n;
+} spl_tensor;
+
+/*
+ * spl_ef_compress over a table of tensors, each chunked on its own (its last chunk padded),
+ * in one pass.  The records and scales of tensor i start at chunk sum_{j<i} ceil(n_j / 4096)
+ * of payload / scales.  `tensors` is a HOST array of num_tensors entries (num_tensors >= 1);
+ * entries with n = 0 are allowed.  Tables longer than SPL_MAX_TENSORS_PER_LAUNCH are
+ * enqueued as several launches on the same stream.
+ */
+spl_status spl_ef_compress_multi(const spl_tensor* tensors, int num_tensors,
+                                 spl_dtype delta_dtype, float beta, uint8_t* payload,
+                                 float* scales, uint32_t* d_flags, spl_stream_t stream);
+
+/*
+ * Receiver: decode P peers' records of one n-value tensor and write their mean; optionally
+ * apply the outer step theta <- theta - lr * mean in the same pass ("Sparse aggregation can
+ * improve model quality"; the pseudo-gradient is pre- minus post-inner-loop weights, "Why
+ * DiLoCo Alone Isn't Enough").
+ *
+ *   mean[i]  = (sum over peers p, in order p = 0..P-1, of q_p[i], fp32 from +0.0) / P
+ *   theta[i] = fmaf(-lr, mean[i], theta[i])
+ *
+ * payloads: HOST array of P device pointers, each spl_num_chunks(n) * 112 bytes
+ * scales:   HOST array of P device pointers, each spl_num_chunks(n) fp32
+ * P:        1 .. SPL_MAX_PEERS
+ * mean_out: device, n fp32, overwritten (not accumulated)
+ * theta:    device, n fp32, updated in place, or NULL (then lr is ignored)
+ * lr:       outer learning rate, finite when theta is given
+ * d_flags:  device uint32 or NULL; SPL_FLAG_BAD_RECORD is OR-ed in when some record has
+ *           indices that are not strictly ascending, or a NaN, infinite or negative scale;
+ *           such a record contributes nothing (the mean still divides by P)
+ * Entries that decode past n (the pads of a tail chunk) are dropped.  mean_out and theta must
+ * not overlap each other or any record or scale array.
+ */
+spl_status spl_decode_aggregate(const uint8_t* const* payloads, const float* const* scales,
+                                int P, size_t n, float* mean_out, float* theta, float lr,
+                                uint32_t* d_flags, spl_stream_t stream);
+
+/*
+ * Record layout helpers (per-chunk size equation): idx[C][64] and codes[C][64] to and from
+ * payload[C][112].  Only the low 12 bits of an index and the low 2 bits of a code are used;
+ * pack does not check ordering.  All pointers are device memory.
+ */
+spl_status spl_pack(const uint16_t* idx, const uint8_t* codes, size_t num_chunks,
+                    uint8_t* payload, spl_stream_t stream);
+spl_status spl_unpack(const uint8_t* payload, size_t num_chunks, uint16_t* idx,
+                      uint8_t* codes, spl_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPL_H_ */

@@ -1,0 +1,136 @@
+"""The C ABI on the host (CPU only): the library builds, loads, exports every symbol the
+header declares, and rejects bad arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import compressed_pseudo_gradient_gb300 as spl
+from compressed_pseudo_gradient_gb300 import build as lib_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spl.h")
+
+OK, INVALID, ALIGN = 0, 1, 2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return spl.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spl_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for fn in ("spl_ef_compress", "spl_ef_compress_multi", "spl_decode_aggregate", "spl_pack",
+               "spl_unpack", "spl_num_chunks", "spl_status_string", "spl_last_cuda_error"):
+        assert fn in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for fn in declared_functions():
+        assert hasattr(lib, fn), f"{fn} declared in spl.h but not exported"
+    assert os.path.exists(lib_build.LIB_PATH)
+
+
+def test_library_is_built_for_sm103a_only():
+    assert any("arch=compute_103a,code=sm_103a" in f for f in lib_build.ARCH)
+
+
+def test_num_chunks_and_status_strings(lib):
+    for n, c in [(0, 0), (1, 1), (4095, 1), (4096, 1), (4097, 2), (1 << 30, 262144)]:
+        assert lib.spl_num_chunks(n) == c
+        assert spl.num_chunks(n) == c
+    for s in range(4):
+        assert lib.spl_status_string(s)
+    assert lib.spl_status_string(99) == b"unknown status"
+    assert lib.spl_last_cuda_error() == 0
+
+
+# Fake device addresses: the checks below fail on the host before any CUDA call is made.
+A = 0x10000000
+B = 0x20000000
+Cp = 0x30000000
+D = 0x40000000
+
+
+def test_compress_argument_errors(lib):
+    f = lib.spl_ef_compress
+    n = 8192
+    assert f(None, 0, None, 0, 1.0, None, None, None, None) == OK            # empty: no-op
+    assert f(None, 0, B, n, 1.0, Cp, D, None, None) == INVALID                # NULL delta
+    assert f(A, 0, None, n, 1.0, Cp, D, None, None) == INVALID                # NULL ef
+    assert f(A, 0, B, n, 1.0, None, D, None, None) == INVALID                 # NULL payload
+    assert f(A, 7, B, n, 1.0, Cp, D, None, None) == INVALID                   # bad dtype
+    assert f(A, 0, B, n, float("nan"), Cp, D, None, None) == INVALID          # beta NaN
+    assert f(A, 0, B, n, float("inf"), Cp, D, None, None) == INVALID          # beta inf
+    assert f(A + 4, 0, B, n, 1.0, Cp, D, None, None) == ALIGN                 # delta 4-B
+    assert f(A, 0, B + 8, n, 1.0, Cp, D, None, None) == ALIGN                 # ef 8-B
+    assert f(A, 0, B, n, 1.0, Cp + 4, D, None, None) == ALIGN                 # payload
+    assert f(A, 0, B, n, 1.0, Cp, D + 2, None, None) == ALIGN                 # scales
+    assert f(A, 0, B, n, 1.0, Cp, D, D + 0x100002, None) == ALIGN             # flags
+    assert f(A, 0, A + 16, n, 1.0, Cp, D, None, None) == INVALID              # ef overlaps delta
+    assert f(A, 0, B, n, 1.0, B + 64, D, None, None) == INVALID               # payload in ef
+    assert f(A, 0, B, n, 1.0, Cp, Cp + 16, None, None) == INVALID             # scales in payload
+    assert f(A, 0, B, 1 << 44, 1.0, Cp, D, None, None) == INVALID             # too many chunks
+
+
+def test_compress_multi_argument_errors(lib):
+    T = spl._binding._Tensor
+    f = lib.spl_ef_compress_multi
+    tab = (T * 2)()
+    tab[0].delta, tab[0].ef, tab[0].n = A, B, 4096
+    tab[1].delta, tab[1].ef, tab[1].n = A + 0x100000, B + 0x100000, 100
+    assert f(None, 1, 0, 1.0, Cp, D, None, None) == INVALID
+    assert f(tab, 0, 0, 1.0, Cp, D, None, None) == INVALID
+    tab[1].ef = B + 0x800        # overlaps tensor 0's error buffer
+    assert f(tab, 2, 0, 1.0, Cp, D, None, None) == INVALID
+    tab[1].ef = B + 0x100004     # misaligned
+    assert f(tab, 2, 0, 1.0, Cp, D, None, None) == ALIGN
+    tab[0].n = tab[1].n = 0      # all empty: nothing to do
+    assert f(tab, 2, 0, 1.0, None, None, None, None) == OK
+
+
+def test_decode_argument_errors(lib):
+    f = lib.spl_decode_aggregate
+    P = 2
+    pl = (ctypes.c_void_p * P)(A, A + 0x100000)
+    sc = (ctypes.c_void_p * P)(B, B + 0x100000)
+    n = 8192
+    assert f(pl, sc, 0, n, Cp, None, 0.0, None, None) == INVALID             # P = 0
+    assert f(pl, sc, 257, n, Cp, None, 0.0, None, None) == INVALID           # P > max
+    assert f(pl, sc, P, 0, Cp, None, 0.0, None, None) == OK                  # empty
+    assert f(None, sc, P, n, Cp, None, 0.0, None, None) == INVALID
+    assert f(pl, sc, P, n, None, None, 0.0, None, None) == INVALID           # NULL mean
+    assert f(pl, sc, P, n, Cp, D, float("nan"), None, None) == INVALID       # lr NaN w/ theta
+    assert f(pl, sc, P, n, Cp + 8, None, 0.0, None, None) == ALIGN
+    assert f(pl, sc, P, n, Cp, D + 4, 0.7, None, None) == ALIGN
+    assert f(pl, sc, P, n, Cp, Cp + 4096, 0.7, None, None) == INVALID        # theta in mean
+    pl_bad = (ctypes.c_void_p * P)(A, A + 8)
+    assert f(pl_bad, sc, P, n, Cp, None, 0.0, None, None) == ALIGN
+    pl_null = (ctypes.c_void_p * P)(A, None)
+    assert f(pl_null, sc, P, n, Cp, None, 0.0, None, None) == INVALID
+    pl_alias = (ctypes.c_void_p * P)(A, Cp + 4096)                          # record in mean
+    assert f(pl_alias, sc, P, n, Cp, None, 0.0, None, None) == INVALID
+
+
+def test_pack_unpack_argument_errors(lib):
+    assert lib.spl_pack(None, None, 0, None, None) == OK
+    assert lib.spl_pack(None, B, 4, Cp, None) == INVALID
+    assert lib.spl_pack(A + 1, B, 4, Cp, None) == ALIGN
+    assert lib.spl_pack(A, B, 4, Cp + 8, None) == ALIGN
+    assert lib.spl_unpack(Cp, 4, None, B, None) == INVALID
+    assert lib.spl_unpack(Cp, 4, A, A + 8, None) == INVALID                  # codes in idx
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+    x = torch.zeros(4096)
+    with pytest.raises(ValueError):
+        spl.ef_compress(x, x.clone(), 1.0)

@@ -1,0 +1,401 @@
+"""GPU parity: the CUDA library against the CPU oracle on the same seeded inputs.
+
+Bar: payload bytes, indices, codes, scales and the error buffer bit-exact; the mean and theta
+within 1e-6 of max |reference| (and, with the fixed peer summation order, bit-exact where
+checked).  Small and medium cases compare every chunk; full workload sizes compare sampled
+chunks in the launch configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import compressed_pseudo_gradient_gb300 as spl
+import oracle
+from compressed_pseudo_gradient_gb300 import synth
+from parity_util import (assert_bit_equal, assert_close, check_compress_sampled,
+                         check_decode_sampled, gather_chunks, host, sample_chunks)
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(autouse=True)
+def _free():
+    yield
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def gpu_round(delta, ef, beta, flags=None):
+    return spl.ef_compress(delta, ef, beta, flags=flags)
+
+
+def compare_full_round(delta, ef, beta, what):
+    d_h, e_h = host(delta), host(ef)
+    payload, scales = gpu_round(delta, ef, beta)
+    torch.cuda.synchronize()
+    o_pl, o_sc, _ = oracle.ef_compress(d_h, e_h, beta, bf16=delta.dtype == torch.bfloat16)
+    assert_bit_equal(host(payload), o_pl, f"{what}: payload")
+    assert_bit_equal(host(scales), o_sc, f"{what}: scales")
+    assert_bit_equal(host(ef), e_h, f"{what}: error buffer")
+    return payload, scales, o_pl, o_sc
+
+
+# ---------------------------------------------------------------------------------------------
+# Tiny workload, every chunk: 2^20 fp32 N(0, 1e-3), beta 1, 3 rounds; mean of 4 peers
+# ---------------------------------------------------------------------------------------------
+def test_tiny_workload_all_chunks():
+    wl = synth.WORKLOADS["tiny"]
+    gen = synth.generator(0, DEV)
+    ef = torch.zeros(wl.n, device=DEV)
+    for r in range(wl.rounds):
+        delta = synth.delta_round(wl, gen, DEV)
+        compare_full_round(delta, ef, wl.beta, f"round {r}")
+    payloads, scales, o_pl, o_sc = [], [], [], []
+    for p in range(wl.peers):
+        g = synth.generator(1 + p, DEV)
+        d = synth.delta_round(wl, g, DEV)
+        e = torch.zeros(wl.n, device=DEV)
+        pl, sc, opl, osc = compare_full_round(d, e, wl.beta, f"peer {p}")
+        payloads.append(pl), scales.append(sc), o_pl.append(opl), o_sc.append(osc)
+    flags = torch.zeros(1, dtype=torch.int32, device=DEV)
+    mean = spl.decode_aggregate(payloads, scales, wl.n, flags=flags)
+    torch.cuda.synchronize()
+    o_mean, o_flags = oracle.decode_aggregate(o_pl, o_sc, wl.n)
+    assert int(flags.item()) == o_flags == 0
+    assert_close(host(mean), o_mean, "mean")
+    assert_bit_equal(host(mean), o_mean, "mean (fixed peer order)")
+    theta = synth.theta(wl.n, synth.generator(0, DEV), DEV)
+    th_h = host(theta)
+    spl.decode_aggregate(payloads, scales, wl.n, theta=theta, lr=0.7)
+    torch.cuda.synchronize()
+    oracle.decode_aggregate(o_pl, o_sc, wl.n, theta=th_h, lr=0.7)
+    assert_close(host(theta), th_h, "theta")
+    assert_bit_equal(host(theta), th_h, "theta (one fma)")
+
+
+# ---------------------------------------------------------------------------------------------
+# Sizes and edge cases
+# ---------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("n", [1, 63, 64, 65, 4095, 4096, 4097, 8191, 3 * 4096 + 1, 40 * 4096 + 123])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_edge_sizes(n, dtype):
+    gen = synth.generator(n, DEV)
+    delta = synth.laplace(n, 1e-4, gen, DEV).to(dtype)
+    ef = synth.normal(n, 1e-4, gen, DEV)
+    pl, sc, o_pl, o_sc = compare_full_round(delta, ef, 0.95, f"n={n}")
+    pl2, sc2, o_pl2, o_sc2 = compare_full_round(delta, ef, 0.95, f"n={n} round 2")
+    theta = synth.theta(n, gen, DEV)
+    th_h = host(theta)
+    mean = spl.decode_aggregate([pl, pl2, pl], [sc, sc2, sc], n, theta=theta, lr=0.7)
+    torch.cuda.synchronize()
+    o_mean, _ = oracle.decode_aggregate([o_pl, o_pl2, o_pl], [o_sc, o_sc2, o_sc], n, theta=th_h, lr=0.7)
+    assert_bit_equal(host(mean), o_mean, f"n={n}: mean")
+    assert_bit_equal(host(theta), th_h, f"n={n}: theta")
+
+
+def _chunks(*blocks):
+    return torch.cat([torch.as_tensor(b, dtype=torch.float32).reshape(-1) for b in blocks]).to(DEV)
+
+
+def test_degenerate_chunks():
+    rng = np.random.default_rng(0)
+    L = 4096
+    spikes = np.zeros(L, np.float32)
+    spikes[rng.choice(L, 64, replace=False)] = rng.choice([-1, 1], 64) * (1 + rng.random(64))
+    few = np.zeros(L, np.float32)
+    few[[5, 900, 4000]] = [0.5, -2.0, 1.0]
+    ties = np.round(rng.standard_normal(L) * 2).astype(np.float32)          # many equal |a|
+    coarse = (rng.integers(-3, 4, L) * 0.25).astype(np.float32)
+    sub = (rng.standard_normal(L) * 1e-39).astype(np.float32)               # subnormal values
+    tiny = np.full(L, np.float32(1.4e-45))                                  # smallest subnormal
+    big = rng.standard_normal(L).astype(np.float32)
+    big[77] = 3e38
+    delta = _chunks(np.zeros(L), np.full(L, -0.0), np.full(L, -2.5), np.arange(L) * -1.0,
+                    np.arange(L)[::-1].copy(), spikes, few, ties, coarse, sub, tiny, big)
+    ef = torch.zeros_like(delta)
+    compare_full_round(delta, ef, 1.0, "degenerate round 1")
+    compare_full_round(torch.zeros_like(delta), ef, 1.0, "degenerate round 2 (zero delta)")
+    compare_full_round(delta, ef, -0.5, "degenerate round 3 (negative beta)")
+
+
+def test_bf16_ties_stress():
+    """bf16 values have 8 significant bits: many exact ties at the threshold."""
+    gen = synth.generator(5, DEV)
+    n = 64 * 4096
+    x = (synth.normal(n, 1.0, gen, DEV) * 4).round() / 4
+    delta = x.to(torch.bfloat16)
+    ef = torch.zeros(n, device=DEV)
+    compare_full_round(delta, ef, 1.0, "bf16 ties")
+    compare_full_round(delta, ef, 1.0, "bf16 ties round 2")
+
+
+def test_nonfinite_inputs_flagged_and_deterministic():
+    n = 4 * 4096
+    gen = synth.generator(9, DEV)
+    delta = synth.laplace(n, 1e-4, gen, DEV)
+    delta[100] = float("inf")
+    delta[5000] = float("nan")
+    delta[9000] = -float("inf")
+    delta[9001] = float("nan")
+    ef = torch.zeros(n, device=DEV)
+    d_h, e_h = host(delta), host(ef)
+    flags = torch.zeros(1, dtype=torch.int32, device=DEV)
+    payload, scales = spl.ef_compress(delta, ef, 1.0, flags=flags)
+    torch.cuda.synchronize()
+    o_pl, o_sc, o_flags = oracle.ef_compress(d_h, e_h, 1.0)
+    assert int(flags.item()) & spl.FLAG_NONFINITE and o_flags & oracle.FLAG_NONFINITE
+    assert_bit_equal(host(payload), o_pl, "payload with non-finite values")
+    g_sc = host(scales)
+    assert np.array_equal(np.isnan(g_sc), np.isnan(o_sc))
+    fin = np.isfinite(o_sc)
+    assert_bit_equal(g_sc[fin], o_sc[fin], "finite scales")
+    g_e = host(ef)
+    same = (g_e == e_h) | (np.isnan(g_e) & np.isnan(e_h))
+    assert same.all()
+    assert int(flags.item()) & spl.FLAG_BAD_RECORD == 0
+
+
+# ---------------------------------------------------------------------------------------------
+# Heavy-tailed bf16 workload
+# ---------------------------------------------------------------------------------------------
+def test_heavy_tail_bf16_medium_all_chunks():
+    wl = synth.WORKLOADS["heavy_tail_bf16"]
+    n = 1 << 22
+    gen = synth.generator(0, DEV)
+    ef = torch.zeros(n, device=DEV)
+    for r in range(wl.rounds):
+        delta = synth.delta_round(wl, gen, DEV, n=n)
+        compare_full_round(delta, ef, wl.beta, f"heavy tail medium round {r}")
+
+
+def test_heavy_tail_bf16_full_size_sampled():
+    wl = synth.WORKLOADS["heavy_tail_bf16"]
+    n = wl.n
+    C = spl.num_chunks(n)
+    gen = synth.generator(0, DEV)
+    ef = torch.zeros(n, device=DEV)
+    for r in range(wl.rounds):
+        delta = synth.delta_round(wl, gen, DEV)
+        ids = sample_chunks(C, 200, seed=r)
+        check_compress_sampled(lambda: gpu_round(delta, ef, wl.beta), delta, ef, wl.beta, ids,
+                               f"heavy tail round {r}")
+    payloads, scales = [], []
+    for p in range(wl.peers):
+        d = synth.delta_round(wl, synth.generator(1 + p, DEV), DEV)
+        e = torch.zeros(n, device=DEV)
+        pl, sc = gpu_round(d, e, wl.beta)
+        payloads.append(pl), scales.append(sc)
+        del d, e
+    mean = spl.decode_aggregate(payloads, scales, n)
+    torch.cuda.synchronize()
+    check_decode_sampled(payloads, scales, n, mean, None, None, 0.0, sample_chunks(C, 200, 99),
+                         "heavy tail P=8")
+
+
+# ---------------------------------------------------------------------------------------------
+# 72B-class decoder layer, chunked per tensor (multi-tensor launch)
+# ---------------------------------------------------------------------------------------------
+SMALL_LAYER = tuple((name, (max(1, s[0] // 64),) + tuple(s[1:])) for name, s in synth.DECODER_LAYER_SHAPES)
+
+
+def test_decoder_layer_multi_tensor_small_all_chunks():
+    shapes = SMALL_LAYER + (("odd", (3, 1000)), ("empty", (0,)), ("one", (1,)))
+    gen = synth.generator(3, DEV)
+    deltas = [synth.row_scaled_normal(s, 2e-4, gen, DEV) if np.prod(s) else
+              torch.zeros(0, device=DEV) for _, s in shapes]
+    efs = [torch.zeros_like(d) for d in deltas]
+    for r in range(3):
+        d_h = [host(d) for d in deltas]
+        e_h = [host(e) for e in efs]
+        payload, scales = spl.ef_compress_multi(deltas, efs, 1.0)
+        torch.cuda.synchronize()
+        o_pl, o_sc = [], []
+        for d, e in zip(d_h, e_h):
+            if d.size:
+                p, s, _ = oracle.ef_compress(d, e, 1.0)
+                o_pl.append(p), o_sc.append(s)
+        assert_bit_equal(host(payload), np.concatenate(o_pl), f"layer round {r}: payload")
+        assert_bit_equal(host(scales), np.concatenate(o_sc), f"layer round {r}: scales")
+        for i, (e, oe) in enumerate(zip(efs, e_h)):
+            assert_bit_equal(host(e), oe, f"layer round {r}: error buffer {i}")
+        deltas = [synth.row_scaled_normal(s, 2e-4, gen, DEV) if np.prod(s) else
+                  torch.zeros(0, device=DEV) for _, s in shapes]
+
+
+def test_multi_tensor_matches_single_calls_and_splits_long_tables():
+    gen = synth.generator(4, DEV)
+    sizes = [int(x) for x in np.random.default_rng(4).integers(1, 3 * 4096, size=150)]
+    deltas = [synth.laplace(k, 1e-4, gen, DEV) for k in sizes]        # 150 tensors: 3 launches
+    efs = [synth.normal(k, 1e-4, gen, DEV) for k in sizes]
+    efs2 = [e.clone() for e in efs]
+    payload, scales = spl.ef_compress_multi(deltas, efs, 0.9)
+    singles = [spl.ef_compress(d, e, 0.9) for d, e in zip(deltas, efs2)]
+    torch.cuda.synchronize()
+    assert_bit_equal(host(payload), np.concatenate([host(p) for p, _ in singles]), "payload")
+    assert_bit_equal(host(scales), np.concatenate([host(s) for _, s in singles]), "scales")
+    for e, e2 in zip(efs, efs2):
+        assert_bit_equal(host(e), host(e2), "error buffer")
+
+
+def test_decoder_layer_full_size_sampled():
+    wl = synth.WORKLOADS["decoder_layer"]
+    gen = synth.generator(0, DEV)
+    deltas = synth.decoder_layer_round(gen, DEV)
+    efs = [torch.zeros_like(d) for d in deltas]
+    for r in range(2):
+        snaps = []
+        chunk0 = 0
+        for i, d in enumerate(deltas):
+            C = spl.num_chunks(d.numel())
+            ids = sample_chunks(C, 24, seed=10 * r + i)
+            snaps.append((ids, chunk0, gather_chunks(d, ids, d.numel()),
+                          gather_chunks(efs[i], ids, d.numel())))
+            chunk0 += C
+        payload, scales = spl.ef_compress_multi(deltas, efs, wl.beta)
+        torch.cuda.synchronize()
+        pl, sc = host(payload), host(scales)
+        for i, (ids, c0, (d_body, d_tail, full_ids), (e_body, e_tail, _)) in enumerate(snaps):
+            n_i = deltas[i].numel()
+            assert d_tail is None or n_i % 4096
+            o_pl, o_sc, _ = oracle.ef_compress(d_body, e_body, wl.beta)
+            rows = [c0 + c for c in full_ids]
+            assert_bit_equal(pl[rows], o_pl, f"layer tensor {i}: payload")
+            assert_bit_equal(sc[rows], o_sc, f"layer tensor {i}: scales")
+            e_after, _, _ = gather_chunks(efs[i], ids, n_i)
+            assert_bit_equal(e_after, e_body, f"layer tensor {i}: error buffer")
+        deltas = synth.decoder_layer_round(gen, DEV)
+    # decode of the own payload (P = 1) for one tensor slice of the concatenated records
+    n_q = deltas[0].numel()
+    Cq = spl.num_chunks(n_q)
+    mean = spl.decode_aggregate([payload[:Cq]], [scales[:Cq]], n_q)
+    torch.cuda.synchronize()
+    check_decode_sampled([payload[:Cq]], [scales[:Cq]], n_q, mean, None, None, 0.0,
+                         sample_chunks(Cq, 64, 5), "layer q_proj decode")
+
+
+# ---------------------------------------------------------------------------------------------
+# Large flat workload (the benchmark's compress launch) and the 24-peer receive workload
+# ---------------------------------------------------------------------------------------------
+def test_large_flat_full_size_sampled():
+    wl = synth.WORKLOADS["large_flat"]
+    n = wl.n
+    C = spl.num_chunks(n)
+    gen = synth.generator(0, DEV)
+    ef = torch.zeros(n, device=DEV)
+    flags = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for r in range(3):
+        delta = synth.delta_round(wl, gen, DEV)
+        check_compress_sampled(lambda: gpu_round(delta, ef, wl.beta, flags), delta, ef, wl.beta,
+                               sample_chunks(C, 256, seed=100 + r), f"large flat round {r}")
+        del delta
+    assert int(flags.item()) == 0
+
+
+def test_receive_24_peers_full_size_sampled():
+    wl = synth.WORKLOADS["receive"]
+    n = wl.n
+    C = spl.num_chunks(n)
+    payloads, scales = [], []
+    e = torch.empty(n, device=DEV)
+    for p in range(wl.peers):
+        d = synth.delta_round(wl, synth.generator(1 + p, DEV), DEV)
+        e.zero_()
+        pl, sc = gpu_round(d, e, wl.beta)
+        payloads.append(pl), scales.append(sc)
+        del d
+    del e
+    theta = synth.theta(n, synth.generator(0, DEV), DEV)
+    ids = sample_chunks(C, 256, seed=7)
+    t_body, t_tail, _ = gather_chunks(theta, ids, n)
+    flags = torch.zeros(1, dtype=torch.int32, device=DEV)
+    mean = spl.decode_aggregate(payloads, scales, n, theta=theta, lr=wl.lr, flags=flags)
+    torch.cuda.synchronize()
+    assert int(flags.item()) == 0
+    check_decode_sampled(payloads, scales, n, mean, (t_body, t_tail), theta, wl.lr, ids,
+                         "receive P=24")
+
+
+# ---------------------------------------------------------------------------------------------
+# Record layout helpers and malformed records
+# ---------------------------------------------------------------------------------------------
+def test_pack_unpack_match_oracle():
+    rng = np.random.default_rng(21)
+    C = 1000
+    idx = np.sort(np.stack([rng.choice(4096, 64, replace=False) for _ in range(C)]), 1)
+    idx = idx.astype(np.uint16)
+    codes = rng.integers(0, 4, (C, 64)).astype(np.uint8)
+    o_pl = oracle.pack(idx, codes)
+    g_pl = spl.pack(torch.from_numpy(idx.view(np.int16)).to(DEV), torch.from_numpy(codes).to(DEV))
+    g_idx, g_codes = spl.unpack(torch.from_numpy(o_pl).to(DEV))
+    torch.cuda.synchronize()
+    assert_bit_equal(host(g_pl), o_pl, "pack")
+    assert np.array_equal(host(g_idx).view(np.uint16), idx)
+    assert np.array_equal(host(g_codes), codes)
+
+
+def test_malformed_records_rejected_like_oracle():
+    n = 6 * 4096
+    gen = synth.generator(31, DEV)
+    pls, scs = [], []
+    for _ in range(3):
+        d = synth.laplace(n, 1e-4, gen, DEV)
+        pl, sc = gpu_round(d, torch.zeros(n, device=DEV), 1.0)
+        pls.append(host(pl)), scs.append(host(sc))
+    idx, codes = oracle.unpack(pls[1])
+    idx[0, [3, 4]] = idx[0, [4, 3]]           # chunk 0: not ascending
+    idx[2, 40] = idx[2, 39]                   # chunk 2: duplicate
+    idx[5, 63] = idx[5, 0]                    # chunk 5: wraps
+    pls[1] = oracle.pack(idx, codes)
+    scs[2][1] = np.nan                        # chunk 1 of peer 2
+    scs[2][3] = np.inf
+    scs[2][4] = -1.0
+    scs[0][5] = -0.0                          # -0.0 is a valid (zero) scale
+    flags = torch.zeros(1, dtype=torch.int32, device=DEV)
+    mean = spl.decode_aggregate([torch.from_numpy(p).to(DEV) for p in pls],
+                                [torch.from_numpy(s).to(DEV) for s in scs], n, flags=flags)
+    torch.cuda.synchronize()
+    o_mean, o_flags = oracle.decode_aggregate(pls, scs, n)
+    assert int(flags.item()) == o_flags == oracle.FLAG_BAD_RECORD
+    assert_bit_equal(host(mean), o_mean, "mean with rejected records")
+
+
+# ---------------------------------------------------------------------------------------------
+# Checkpoint/resume of the only codec state, and streams
+# ---------------------------------------------------------------------------------------------
+def test_resume_from_host_copy_of_error_buffer():
+    n = 50 * 4096 + 17
+    gen = synth.generator(41, DEV)
+    deltas = [synth.laplace(n, 1e-4, gen, DEV) for _ in range(3)]
+    ef_a = torch.zeros(n, device=DEV)
+    outs_a = [gpu_round(d, ef_a, 0.95) for d in deltas]
+    ef_b = torch.zeros(n, device=DEV)
+    for d in deltas[:2]:
+        gpu_round(d, ef_b, 0.95)
+    saved = ef_b.cpu()
+    del ef_b
+    ef_c = saved.to(DEV)
+    pl, sc = gpu_round(deltas[2], ef_c, 0.95)
+    torch.cuda.synchronize()
+    assert_bit_equal(host(pl), host(outs_a[2][0]), "resumed payload")
+    assert_bit_equal(host(sc), host(outs_a[2][1]), "resumed scales")
+    assert_bit_equal(host(ef_c), host(ef_a), "resumed error buffer")
+
+
+def test_side_stream_and_stream_order():
+    n = 20 * 4096
+    gen = synth.generator(51, DEV)
+    delta = synth.laplace(n, 1e-4, gen, DEV)
+    ef1 = torch.zeros(n, device=DEV)
+    ef2 = torch.zeros(n, device=DEV)
+    ref = gpu_round(delta, ef1, 0.95)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        out = gpu_round(delta, ef2, 0.95)
+        mean = spl.decode_aggregate([out[0]], [out[1]], n)
+    s.synchronize()
+    torch.cuda.synchronize()
+    assert_bit_equal(host(out[0]), host(ref[0]), "side-stream payload")
+    assert_bit_equal(host(ef2), host(ef1), "side-stream error buffer")
+    assert np.count_nonzero(host(mean)) == 64 * 20
