@@ -101,6 +101,12 @@ def max_over_ranks(x: float, device=None) -> float:
     return float(t.item())
 
 
+def rank_seed_base(rank: int) -> int:
+    """Seed block of a rank's peer: delta at base, its 24 peers' deltas at base + 1..24,
+    theta at base + 5000; blocks of different ranks never overlap."""
+    return 1 + 10000 * rank
+
+
 def aggregate_value(bytes_per_rank: int, world: int, max_seconds: float) -> float:
     """Whole-job GB/s: all ranks' bytes over the slowest rank's time."""
     return bytes_per_rank * world / max_seconds / 1e9
@@ -211,20 +217,21 @@ class ClockSampler:
 # ---------------------------------------------------------------------------------------------
 # The GPU arm
 # ---------------------------------------------------------------------------------------------
-def setup_workload(dev, seed_base: int):
+def setup_workload(dev, seed_base: int, n: int):
     import torch
     import compressed_pseudo_gradient_gb300 as spl
     from compressed_pseudo_gradient_gb300 import synth
 
-    buf = {}
-    buf["delta"] = synth.laplace(N_ELEMS, 1e-4, synth.generator(seed_base, dev), dev)
-    buf["ef"] = torch.zeros(N_ELEMS, dtype=torch.float32, device=dev)
-    buf["payload"] = torch.empty((N_CHUNKS, RECORD), dtype=torch.uint8, device=dev)
-    buf["scales"] = torch.empty(N_CHUNKS, dtype=torch.float32, device=dev)
+    C = (n + CHUNK - 1) // CHUNK
+    buf = {"n": n}
+    buf["delta"] = synth.laplace(n, 1e-4, synth.generator(seed_base, dev), dev)
+    buf["ef"] = torch.zeros(n, dtype=torch.float32, device=dev)
+    buf["payload"] = torch.empty((C, RECORD), dtype=torch.uint8, device=dev)
+    buf["scales"] = torch.empty(C, dtype=torch.float32, device=dev)
     peers_pl, peers_sc = [], []
-    tmp_e = torch.empty(N_ELEMS, dtype=torch.float32, device=dev)
+    tmp_e = torch.empty(n, dtype=torch.float32, device=dev)
     for p in range(PEERS):
-        d = synth.laplace(N_ELEMS, 1e-4, synth.generator(seed_base + 1 + p, dev), dev)
+        d = synth.laplace(n, 1e-4, synth.generator(seed_base + 1 + p, dev), dev)
         tmp_e.zero_()
         pl, sc = spl.ef_compress(d, tmp_e, BETA)
         peers_pl.append(pl)
@@ -232,8 +239,8 @@ def setup_workload(dev, seed_base: int):
         del d
     del tmp_e
     buf["peers_pl"], buf["peers_sc"] = peers_pl, peers_sc
-    buf["theta"] = synth.theta(N_ELEMS, synth.generator(seed_base + 1000, dev), dev)
-    buf["mean"] = torch.empty(N_ELEMS, dtype=torch.float32, device=dev)
+    buf["theta"] = synth.theta(n, synth.generator(seed_base + 5000, dev), dev)
+    buf["mean"] = torch.empty(n, dtype=torch.float32, device=dev)
     buf["flags"] = torch.zeros(1, dtype=torch.int32, device=dev)
     torch.cuda.synchronize(dev)
     torch.cuda.empty_cache()
@@ -251,7 +258,7 @@ def gpu_step(buf, ev=None):
     if ev:
         ev[1].record()
         ev[2].record()
-    spl.decode_aggregate(buf["peers_pl"], buf["peers_sc"], N_ELEMS, mean=buf["mean"],
+    spl.decode_aggregate(buf["peers_pl"], buf["peers_sc"], buf["n"], mean=buf["mean"],
                          theta=buf["theta"], lr=LR, flags=buf["flags"])
     if ev:
         ev[3].record()
@@ -261,7 +268,7 @@ def gpu_step(buf, ev=None):
 def run_gpu(args, dev, rank, world):
     import torch
 
-    buf = setup_workload(dev, seed_base=1 + 100 * rank)
+    buf = setup_workload(dev, seed_base=rank_seed_base(rank), n=args.elements)
     for _ in range(args.warmup):
         gpu_step(buf)
     torch.cuda.synchronize(dev)
@@ -322,7 +329,7 @@ def run_e2e(args, buf, dev):
         for d, h in zip(d_sc, h_sc):
             d.copy_(h, non_blocking=True)
         spl.ef_compress(d_delta, buf["ef"], BETA, payload=buf["payload"], scales=buf["scales"])
-        spl.decode_aggregate(d_pl, d_sc, N_ELEMS, mean=buf["mean"], theta=buf["theta"], lr=LR)
+        spl.decode_aggregate(d_pl, d_sc, buf["n"], mean=buf["mean"], theta=buf["theta"], lr=LR)
         out_pl.copy_(buf["payload"], non_blocking=True)
         out_sc.copy_(buf["scales"], non_blocking=True)
 
@@ -380,7 +387,7 @@ def cpu_sample_bytes(S: int) -> int:
 
 def cpu_baseline_from_device(buf, chunks: int):
     """The oracle on the first `chunks` chunks of the same workload (copied from the GPU)."""
-    S = min(chunks, N_CHUNKS)
+    S = min(chunks, (buf["n"] + CHUNK - 1) // CHUNK)
     sample = {
         "chunks": S,
         "delta": buf["delta"][:S * CHUNK].cpu().numpy(),
@@ -414,7 +421,7 @@ def make_cpu_sample(S: int, seed_base: int = 1):
         pl, sc, _ = oracle.ef_compress(d, np.zeros(n, np.float32), BETA)
         pls.append(pl)
         scs.append(sc)
-    theta = synth.theta(n, synth.generator(seed_base + 1000, cpu), cpu).numpy()
+    theta = synth.theta(n, synth.generator(seed_base + 5000, cpu), cpu).numpy()
     return {"chunks": S, "delta": delta, "ef": np.zeros(n, np.float32), "theta": theta,
             "peers_pl": pls, "peers_sc": scs}
 
@@ -455,13 +462,15 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=150)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--cpu-chunks", type=int, default=4096)
+    ap.add_argument("--cpu-chunks", type=int, default=32768)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--elements", type=int, default=N_ELEMS,
+                    help="pseudo-gradient size; smaller than 2^30 only for profiling captures")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -480,30 +489,33 @@ def main(argv=None):
     if rank != 0:
         return 0
 
+    n = args.elements
+    C = (n + CHUNK - 1) // CHUNK
+    step_bytes = compress_bytes(n, C) + decode_bytes(n, C, PEERS)
     comp_avg = statistics.mean(r["comp_ms"]) / 1e3
     dec_avg = statistics.mean(r["dec_ms"]) / 1e3
-    comp_gbs = compress_bytes(N_ELEMS, N_CHUNKS) / comp_avg / 1e9
-    dec_gbs = decode_bytes(N_ELEMS, N_CHUNKS, PEERS) / dec_avg / 1e9
+    comp_gbs = compress_bytes(n, C) / comp_avg / 1e9
+    dec_gbs = decode_bytes(n, C, PEERS) / dec_avg / 1e9
     peak, peak_kind = read_peaks()
     dominant = "ef_compress" if sum(r["comp_ms"]) >= sum(r["dec_ms"]) else "decode_aggregate"
     achieved = comp_gbs if dominant == "ef_compress" else dec_gbs
-    value = aggregate_value(STEP_BYTES, world, r["t_max"] / args.steps)
+    value = aggregate_value(step_bytes, world, r["t_max"] / args.steps)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * r["t_max"] / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {
-            "workload": WORKLOAD, "n": N_ELEMS, "chunks": N_CHUNKS, "peers": PEERS,
-            "beta": BETA, "lr": LR, "step_bytes": STEP_BYTES,
+            "workload": WORKLOAD if n == N_ELEMS else f"profiling case: {n} values, same recipe",
+            "n": n, "chunks": C, "peers": PEERS, "beta": BETA, "lr": LR, "step_bytes": step_bytes,
             "l2": "inputs (4 GiB per dense array) far exceed L2; no flush",
             "parallelism": f"independent peer per GPU x{world}",
             "ef_compress": {"ms": round(1e3 * comp_avg, 4), "GB/s": round(comp_gbs, 1),
                             "frac_of_hbm": round(comp_gbs / peak, 4),
-                            "Gelem/s": round(N_ELEMS / comp_avg / 1e9, 2)},
+                            "Gelem/s": round(n / comp_avg / 1e9, 2)},
             "decode_aggregate": {"ms": round(1e3 * dec_avg, 4), "GB/s": round(dec_gbs, 1),
                                  "frac_of_hbm": round(dec_gbs / peak, 4),
-                                 "Gelem/s": round(N_ELEMS / dec_avg / 1e9, 2)},
+                                 "Gelem/s": round(n / dec_avg / 1e9, 2)},
             "device_flags": r["flags"],
         },
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1),
@@ -515,7 +527,7 @@ def main(argv=None):
     }
     if r["e2e"] is not None:
         e = r["e2e"]
-        line["e2e"] = {"value": round(aggregate_value(STEP_BYTES, world, e["seconds"] / e["steps"]), 2),
+        line["e2e"] = {"value": round(aggregate_value(step_bytes, world, e["seconds"] / e["steps"]), 2),
                        "unit": "GB/s", "h2d_bytes_per_step": e["h2d"],
                        "d2h_bytes_per_step": e["d2h"], "steps": e["steps"]}
     if r["cpu"] is not None:

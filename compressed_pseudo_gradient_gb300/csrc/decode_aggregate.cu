@@ -9,16 +9,23 @@
 //
 // Design (HBM-bound: P x 116 B read per chunk, 16 KB of mean written, 32 KB of theta read and
 // written when the outer step is fused):
-//   - one 256-thread CTA per chunk, grid-stride over chunks with a persistent grid; the
-//     chunk's accumulator is 16 KB of shared memory, so the dense output is written exactly
-//     once and nothing is zero-filled or atomically added in global memory;
-//   - all P records (7 x 16 B each) and scales are fetched by all threads at once, together
-//     with the chunk's theta, so their latencies overlap;
-//   - one warp adds the peers into the accumulator in peer order (each lane owns entries r
-//     and r + 32; indices inside a valid record are strictly ascending, hence distinct), which
-//     fixes the fp32 summation order; it also checks each record and skips malformed ones;
-//   - the dense pass reads the accumulator, divides by P, stores the mean and the updated
-//     theta with streaming stores, and clears the accumulator for the next chunk.
+//   - one 256-thread CTA per chunk, grid-stride over chunks with a persistent grid; while a
+//     chunk is worked on, the next chunk's theta (one 16 KB bulk copy, TMA) and its P records
+//     (16-byte cp.async copies spread over the threads) fly into a shared-memory stage, all
+//     completing on one mbarrier; the next chunk's P scales travel as plain loads into
+//     registers (lane l of warp w holds peer 8 l + w's);
+//   - each warp unpacks whole records (one peer at a time): the 64 14-bit fields, a check that
+//     the indices ascend strictly and the scale is finite and non-negative, the decoded value
+//     of every entry, and, per 512-position slice of the chunk, the range of entry ranks that
+//     falls into it (a rejected record gets empty ranges);
+//   - warp w owns slice [512 w, 512 w + 512) of a 16 KB shared accumulator and adds its
+//     entries peer by peer, in order p = 0..P-1 (a valid record hits a position at most once),
+//     so every position is summed in fp32 in peer order from +0.0, as a plain sequential loop
+//     over peers would; no atomics, no cross-warp hazards;
+//   - the same warp then runs the dense pass over its slice: divide by P (correctly rounded,
+//     with a precomputed reciprocal), store the mean and the updated theta with streaming
+//     stores, clear the slice.  Peers are unpacked in groups of up to 64, so shared memory
+//     stays bounded for any P.
 #include <cfloat>
 
 #include "spl_device.cuh"
@@ -27,93 +34,222 @@
 namespace spl {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kPer = kChunk / kThreads;   // 16
-constexpr int kVec = kPer / 4;
+#ifndef SPL_DECODE_STAGES
+#define SPL_DECODE_STAGES 1
+#endif
 
-__global__ void __launch_bounds__(kThreads)
-k_decode_aggregate(const DecodeTable tab, int P, int64_t n, float* __restrict__ mean,
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kSlice = kChunk / kWarps;   // 512 positions per warp
+constexpr int kVec = kSlice / 128;        // 4 vectors of 4 per thread
+constexpr int kGroup = 64;                // peers unpacked per pass
+constexpr int kStages = SPL_DECODE_STAGES;
+
+__host__ __device__ constexpr size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+
+// Dynamic shared memory for P peers (offsets 16-byte aligned), G = min(P, 64):
+//   bar[2] | theta stage [S][4096] f32 | record stage [S][P][112] (+16) | acc [4096] f32 |
+//   entries [G][64] (position, value) | slice ranges [G][16] u8
+struct Layout {
+    size_t bar, theta, rec, acc, ent, rng, total;
+    __host__ __device__ explicit Layout(int P) {
+        const size_t G = static_cast<size_t>(P < kGroup ? P : kGroup);
+        bar = 0;
+        theta = 16;
+        rec = theta + kStages * kChunk * 4;
+        acc = rec + align16(kStages * static_cast<size_t>(P) * kRecordBytes) + 16;
+        ent = acc + kChunk * 4;
+        rng = ent + G * kTopK * 8;
+        total = rng + G * 16;
+    }
+};
+
+// All threads: start chunk c's copies into one stage.  Thread 0 arrives with the expected
+// theta bytes (a full chunk when the outer step is fused) and starts its bulk copy; the
+// record pieces (7 x 16 B per peer) are spread over the threads, each of which arrives once
+// its own copies have landed.  Arrivals per phase: min(7 P, 256) + 1.
+__device__ __forceinline__ void prefetch(const DecodeTable& tab, int P, int64_t c, bool full,
+                                         const float* theta, uint64_t* bar, uint8_t* st_rec,
+                                         float* st_theta, int tid) {
+    if (tid == 0) {
+        if (theta != nullptr && full) {
+            fence_async_smem();
+            mbar_expect_tx(bar, kChunk * 4);
+            bulk_load(st_theta, theta + c * kChunk, kChunk * 4, bar);
+        } else {
+            mbar_arrive(bar);
+        }
+    }
+    const int pieces = P * kRecordVec;
+    if (tid < pieces) {
+        for (int i = tid; i < pieces; i += kThreads) {
+            const int p = i / kRecordVec;
+            const int w = i - p * kRecordVec;
+            cp_async16(st_rec + i * 16, tab.payload[p] + c * kRecordBytes + w * 16);
+        }
+        cp_async_arrive(bar);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 4)
+k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __restrict__ mean,
                    float* __restrict__ theta, float neg_lr, uint32_t* __restrict__ flags) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    float* acc = reinterpret_cast<float*>(smem_raw);                             // 4096
-    uint4* rec = reinterpret_cast<uint4*>(smem_raw + kChunk * sizeof(float));    // P x 7
-    float* sc = reinterpret_cast<float*>(rec + P * kRecordVec);                  // P
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const Layout L(P);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + L.bar);
+    float* st_theta = reinterpret_cast<float*>(smem_raw + L.theta);
+    uint8_t* st_rec = smem_raw + L.rec;
+    float* acc = reinterpret_cast<float*>(smem_raw + L.acc);
+    uint2* ent = reinterpret_cast<uint2*>(smem_raw + L.ent);
+    uint8_t* rng = smem_raw + L.rng;
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
     const int64_t C = (n + kChunk - 1) / kChunk;
+    const int64_t G = gridDim.x;
+    if (static_cast<int64_t>(blockIdx.x) >= C) return;
     const float pf = static_cast<float>(P);
-    bool bad = false;
+    const int slice0 = kSlice * warp;    // this warp's positions: slice0 + 128 v + 4 lane + u
+    const int my_peer = 8 * lane + warp; // the peer whose scale this lane carries
 
 #pragma unroll
     for (int v = 0; v < kVec; ++v)
-        reinterpret_cast<float4*>(acc)[v * (kThreads) + tid] = make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4*>(&acc[slice0 + 128 * v + 4 * lane]) = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (tid == 0) {
+        const uint32_t arrivals = static_cast<uint32_t>(min(P * kRecordVec, kThreads) + 1);
+        for (int st = 0; st < kStages; ++st) mbar_init(&bars[st], arrivals);
+    }
+    __syncthreads();
+    for (int st = 0; st < kStages; ++st) {
+        const int64_t c = blockIdx.x + st * G;
+        if (c < C)
+            prefetch(tab, P, c, (c + 1) * kChunk <= n, theta, &bars[st],
+                     st_rec + st * P * kRecordBytes, st_theta + st * kChunk, tid);
+    }
+    float sc_cur = my_peer < P ? __ldcs(tab.scale[my_peer] + blockIdx.x) : 0.0f;
 
-    for (int64_t c = blockIdx.x; c < C; c += gridDim.x) {
+    bool bad = false;
+    bool aborted = false;
+    int it = 0;
+    int64_t c = blockIdx.x;
+    for (; c < C; c += G, ++it) {
+        const int st = it % kStages;
+        const uint32_t parity = static_cast<uint32_t>(it / kStages) & 1u;
+        const uint8_t* rec = st_rec + st * P * kRecordBytes;
         const int64_t base = c * kChunk;
         const bool full = base + kChunk <= n;
         const int valid = full ? kChunk : static_cast<int>(n - base);
 
+        const bool timed_out = !mbar_wait(&bars[st], parity);
         float4 th[kVec];
         if (theta != nullptr && full) {
 #pragma unroll
-            for (int v = 0; v < kVec; ++v) th[v] = ld_stream_f4(theta + base + v * 1024 + 4 * tid);
+            for (int v = 0; v < kVec; ++v)
+                th[v] = *reinterpret_cast<const float4*>(
+                    &st_theta[st * kChunk + slice0 + 128 * v + 4 * lane]);
         }
-        for (int i = tid; i < P * kRecordVec; i += kThreads) {
-            const int p = i / kRecordVec;
-            const int w = i - p * kRecordVec;
-            rec[i] = __ldcs(reinterpret_cast<const uint4*>(tab.payload[p] + c * kRecordBytes) + w);
-        }
-        for (int p = tid; p < P; p += kThreads) sc[p] = __ldcs(tab.scale[p] + c);
-        __syncthreads();
+        float sc_next = 0.0f;
 
-        if (warp == 0) {
-            for (int p = 0; p < P; ++p) {
-                const uint32_t* words = reinterpret_cast<const uint32_t*>(rec + p * kRecordVec);
-                const uint32_t f0 = record_field(words, lane);
-                const uint32_t f1 = record_field(words, lane + 32);
+        for (int g0 = 0; g0 < P; g0 += kGroup) {
+            const int gn = P - g0 < kGroup ? P - g0 : kGroup;
+            // ---- unpack: one warp per peer --------------------------------------------
+            for (int g = warp; g < gn; g += kWarps) {
+                const int p = g0 + g;
+                const uint32_t* words = reinterpret_cast<const uint32_t*>(rec + p * kRecordBytes);
+                const uint32_t f0 = record_field_fs(words, lane);
+                const uint32_t f1 = record_field_fs(words, lane + 32);
                 const uint32_t i0 = f0 >> 2;
                 const uint32_t i1 = f1 >> 2;
                 const uint32_t first_hi = __shfl_sync(0xffffffffu, i1, 0);
                 uint32_t next0 = __shfl_down_sync(0xffffffffu, i0, 1);
                 const uint32_t next1 = __shfl_down_sync(0xffffffffu, i1, 1);
                 if (lane == 31) next0 = first_hi;
-                const float s = sc[p];
-                const bool ok = i0 < next0 && (lane == 31 || i1 < next1) && s >= 0.0f &&
-                                s <= FLT_MAX;
-                if (!__all_sync(0xffffffffu, ok)) {
+                const float s = __shfl_sync(0xffffffffu, sc_cur, p >> 3);
+                const bool ok = __all_sync(0xffffffffu, i0 < next0 && (lane == 31 || i1 < next1)) &&
+                                s >= 0.0f && s <= FLT_MAX;
+                uint8_t* rg = rng + g * 16;
+                if (ok) {
+                    uint2* eg = ent + g * kTopK;
+                    eg[lane] = make_uint2(i0, __float_as_uint(level_value(f0 & 3u, s)));
+                    eg[lane + 32] = make_uint2(i1, __float_as_uint(level_value(f1 & 3u, s)));
+                    // rank of the first entry of slice k, for k = 0..8
+                    const int s0 = static_cast<int>(i0 >> 9);
+                    const int s1 = static_cast<int>(i1 >> 9);
+                    const int last_lo = __shfl_sync(0xffffffffu, s0, 31);
+                    int prev0 = __shfl_up_sync(0xffffffffu, s0, 1);
+                    int prev1 = __shfl_up_sync(0xffffffffu, s1, 1);
+                    if (lane == 0) {
+                        prev0 = -1;
+                        prev1 = last_lo;
+                    }
+                    for (int k = prev0 + 1; k <= s0; ++k) rg[k] = static_cast<uint8_t>(lane);
+                    for (int k = prev1 + 1; k <= s1; ++k) rg[k] = static_cast<uint8_t>(lane + 32);
+                    if (lane == 31)
+                        for (int k = s1 + 1; k <= kWarps; ++k) rg[k] = kTopK;
+                } else {
+                    if (lane <= kWarps) rg[lane] = 0;   // empty ranges: contributes nothing
                     bad = true;
-                    continue;
                 }
-                if (base + i0 < n) acc[i0] = __fadd_rn(acc[i0], level_value(f0 & 3u, s));
-                if (base + i1 < n) acc[i1] = __fadd_rn(acc[i1], level_value(f1 & 3u, s));
+            }
+            const bool last = g0 + kGroup >= P;
+            if (last) {
+                if (__syncthreads_or(timed_out)) {
+                    aborted = true;
+                    break;
+                }
+                // the stage has been read: start chunk c + S G's copies, and c + G's scales
+                const int64_t c2 = c + kStages * G;
+                if (c2 < C)
+                    prefetch(tab, P, c2, (c2 + 1) * kChunk <= n, theta, &bars[st],
+                             st_rec + st * P * kRecordBytes, st_theta + st * kChunk, tid);
+                if (my_peer < P && c + G < C) sc_next = __ldcs(tab.scale[my_peer] + c + G);
+            } else {
+                __syncthreads();
+            }
+            // ---- this warp's slice: add the entries peer by peer, in order --------------
+            int lo_n = rng[warp];
+            int hi_n = rng[warp + 1];
+            for (int g = 0; g < gn; ++g) {
+                const int lo = lo_n;
+                const int hi = hi_n;
+                if (g + 1 < gn) {
+                    lo_n = rng[(g + 1) * 16 + warp];
+                    hi_n = rng[(g + 1) * 16 + warp + 1];
+                }
+                for (int r = lo + lane; r < hi; r += 32) {
+                    const uint2 e = ent[g * kTopK + r];
+                    acc[e.x] = __fadd_rn(acc[e.x], __uint_as_float(e.y));
+                }
                 __syncwarp();
             }
+            __syncthreads();   // entries and ranges are rewritten by the next pass
         }
-        __syncthreads();
+        if (aborted) break;
+        sc_cur = sc_next;
 
+        // ---- dense pass over this warp's slice: mean, outer step --------------------------
 #pragma unroll
         for (int v = 0; v < kVec; ++v) {
-            const int j0 = v * 1024 + 4 * tid;
-            float4 s4 = reinterpret_cast<float4*>(acc)[j0 >> 2];
-            reinterpret_cast<float4*>(acc)[j0 >> 2] = make_float4(0.f, 0.f, 0.f, 0.f);
-            s4.x = __fdiv_rn(s4.x, pf);
-            s4.y = __fdiv_rn(s4.y, pf);
-            s4.z = __fdiv_rn(s4.z, pf);
-            s4.w = __fdiv_rn(s4.w, pf);
+            const int j0 = slice0 + 128 * v + 4 * lane;
+            float4 m4 = *reinterpret_cast<const float4*>(&acc[j0]);
+            *reinterpret_cast<float4*>(&acc[j0]) = make_float4(0.f, 0.f, 0.f, 0.f);
+            m4.x = div_rn(m4.x, pf, rp);
+            m4.y = div_rn(m4.y, pf, rp);
+            m4.z = div_rn(m4.z, pf, rp);
+            m4.w = div_rn(m4.w, pf, rp);
             if (full) {
-                st_stream_f4(mean + base + j0, s4);
+                st_stream_f4(mean + base + j0, m4);
                 if (theta != nullptr) {
                     float4 t4 = th[v];
-                    t4.x = __fmaf_rn(neg_lr, s4.x, t4.x);
-                    t4.y = __fmaf_rn(neg_lr, s4.y, t4.y);
-                    t4.z = __fmaf_rn(neg_lr, s4.z, t4.z);
-                    t4.w = __fmaf_rn(neg_lr, s4.w, t4.w);
+                    t4.x = __fmaf_rn(neg_lr, m4.x, t4.x);
+                    t4.y = __fmaf_rn(neg_lr, m4.y, t4.y);
+                    t4.z = __fmaf_rn(neg_lr, m4.z, t4.z);
+                    t4.w = __fmaf_rn(neg_lr, m4.w, t4.w);
                     st_stream_f4(theta + base + j0, t4);
                 }
             } else {
-                const float m[4] = {s4.x, s4.y, s4.z, s4.w};
+                const float m[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int j = j0 + u;
@@ -126,7 +262,18 @@ k_decode_aggregate(const DecodeTable tab, int P, int64_t n, float* __restrict__ 
             }
         }
     }
-    if (bad && flags != nullptr) atomicOr(flags, kFlagBadRecord);
+    if (aborted && tid == 0) {
+        // copies still in flight may land late: wait for them (bounded) before the CTA's
+        // shared memory is released: the stage that timed out and any armed after it
+        for (int k = 0; k < kStages; ++k) {
+            const int it2 = it + k;
+            if (c + k * G < C) mbar_wait(&bars[it2 % kStages], static_cast<uint32_t>(it2 / kStages) & 1u);
+        }
+    }
+    if (flags != nullptr) {
+        if (bad && lane == 0) atomicOr(flags, kFlagBadRecord);
+        if (aborted && tid == 0) atomicOr(flags, kFlagTimeout);
+    }
 }
 
 }  // namespace
@@ -136,12 +283,16 @@ cudaError_t launch_decode_aggregate(const DecodeTable& tab, int P, int64_t n, fl
                                     cudaStream_t stream) {
     const int64_t C = (n + kChunk - 1) / kChunk;
     if (C == 0) return cudaSuccess;
-    const size_t smem = kChunk * sizeof(float) + static_cast<size_t>(P) * (kRecordBytes + 4);
-    const int resident = persistent_grid(reinterpret_cast<const void*>(&k_decode_aggregate),
-                                         kThreads, smem);
+    const size_t smem = Layout(P).total;
+    const void* kern = reinterpret_cast<const void*>(&k_decode_aggregate);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const int resident = persistent_grid(kern, kThreads, smem);
     if (resident <= 0) return cudaErrorInvalidConfiguration;
     const int grid = static_cast<int>(C < resident ? C : resident);
-    k_decode_aggregate<<<grid, kThreads, smem, stream>>>(tab, P, n, mean, theta, -lr, flags);
+    const float rp = 1.0f / static_cast<float>(P);   // correctly rounded on the host
+    k_decode_aggregate<<<grid, kThreads, smem, stream>>>(tab, P, rp, n, mean, theta, -lr, flags);
     return cudaGetLastError();
 }
 

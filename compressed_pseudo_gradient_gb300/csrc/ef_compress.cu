@@ -7,20 +7,22 @@
 // accumulation": what is not sent stays in the buffer for the next round).
 //
 // Design (HBM-bound: 8 B read + 4 B written per fp32 value, 116 B written per chunk):
-//   - one 256-thread CTA per 4096-value chunk, grid-stride over chunks with a grid of
-//     SMs x resident CTAs; each thread keeps 16 values in registers, loaded as four 16-byte
-//     vectors at chunk offsets v*1024 + 4*tid (v = 0..3), so every warp access is 512
-//     contiguous bytes; the error buffer is read and written exactly once, with streaming
-//     cache hints;
-//   - the 64th-largest |a| is found by a radix select on the 31-bit magnitude keys:
-//     shared-memory histograms of key bits [30:20], [19:9] and [8:0], each restricted to the
-//     keys that match the digits found so far, stopping early once the boundary bin is taken
-//     whole; no sort and no global scratch;
-//   - keys above the threshold, and threshold ties in index order, are marked in a 4096-bit
-//     shared bitmap, so one warp compacts the 64 indices in ascending order with popc scans;
-//   - the threads that own the chosen values compute their codes and residuals in registers
-//     and store the whole chunk of the error buffer once; one warp packs the 64 fields into
-//     the 112-byte record with shuffles and 16-byte stores.
+//   - one 256-thread CTA per 4096-value chunk, grid-stride over chunks with a persistent grid
+//     (SMs x resident CTAs); while a chunk is worked on, the next chunk's error buffer and
+//     delta fly into a shared-memory stage as two 1-D bulk copies (TMA, no multicast, no
+//     cluster) completing on an mbarrier, whose wait is bounded in time;
+//   - each thread takes 16 values from the stage into registers (four 16-byte vectors at
+//     chunk offsets v*1024 + 4*tid), forms a = fma(beta, e, delta) and the 31-bit magnitude
+//     keys, and keeps them there for the whole chunk; the error buffer is written back once,
+//     from registers, with streaming stores;
+//   - the 64th-largest key is found by a radix select: shared-memory histograms of key bits
+//     [30:20], then [19:9] and [8:0] restricted to the keys matching the digits found so far,
+//     stopping as soon as the boundary bin is taken whole; ties at the final threshold go to
+//     the lowest indices; the chosen positions end up in a 4096-bit shared bitmap;
+//   - one warp turns the bitmap into per-word prefix counts, from which every thread that
+//     owns a chosen value knows its rank in ascending index order; it computes the code and
+//     the residual in registers and writes its 14-bit field to shared memory; one warp then
+//     assembles the 112-byte record (28 words) and stores it as seven 16-byte vectors.
 #include "spl_device.cuh"
 #include "spl_kernels.h"
 
@@ -34,16 +36,18 @@ constexpr int kVec = kPer / 4;             // 4 vectors of 4 per thread
 constexpr int kBitmapWords = kChunk / 32;  // 128
 
 struct Smem {
-    uint32_t hist[2][2048];
-    uint32_t sel_bm[kBitmapWords];  // keys strictly above the threshold prefix
-    uint32_t eq_bm[kBitmapWords];   // keys equal to the threshold prefix (tie candidates)
-    uint32_t fin_bm[kBitmapWords];  // the 64 chosen positions
+    float stage_e[kChunk];          // prefetched error-buffer chunk (bulk copy)
+    uint32_t stage_d[kChunk];       // prefetched delta chunk: fp32, or bf16 in the first half
+    uint32_t hist[2048];            // bins of key bits [30:20], then [19:9] if needed
+    uint32_t hist3[512];            // bins of key bits [8:0] (many-candidate path)
+    uint32_t sel_bm[kBitmapWords];  // chosen positions (complete once the select is done)
+    uint32_t eq_bm[kBitmapWords];   // ties at the final threshold (many-candidate path)
     uint32_t warp_tot[kWarps];
     uint32_t warp_max[kWarps];
     uint32_t bcast[3];              // digit, count above the digit's bin, count in the bin
-    float scale;
-    uint16_t sel_idx[kTopK];
-    uint8_t code_at[kChunk];
+    uint16_t fields[kTopK];         // the record's 64 fields, in ascending index order
+    alignas(16) uint16_t pre[kBitmapWords];   // chosen positions before each bitmap word
+    uint64_t bar;                   // completes when the stage's bulk copies have landed
 };
 
 // Block-wide search of the bin holding the need-th largest key (counting from the top bin).
@@ -87,88 +91,130 @@ __device__ __forceinline__ void find_digit(Smem& sm, const uint32_t* hist, uint3
     }
 }
 
+// The chunk a CTA works on: its tensor's pointers advanced to the chunk, and its extent.
+struct ChunkRef {
+    const void* delta;
+    float* ef;
+    int valid;
+    bool full;
+};
+
 template <bool kBf16>
-__device__ __forceinline__ void load_accumulate(const void* delta, const float* ef, int valid,
-                                                bool full, float beta, int tid,
-                                                float (&a)[kPer]) {
-    if (full) {
-        float4 e4[kVec];
+__device__ __forceinline__ ChunkRef locate(const CompressTable& tab, int64_t c) {
+    int t = 0;
+    int hi = tab.num;
+    while (hi - t > 1) {
+        const int mid = (t + hi) >> 1;
+        if (tab.chunk_begin[mid] <= c) t = mid; else hi = mid;
+    }
+    const int64_t base = (c - tab.chunk_begin[t]) * kChunk;
+    const int64_t n = tab.n[t];
+    ChunkRef r;
+    r.ef = tab.ef[t] + base;
+    r.delta = kBf16
+        ? static_cast<const void*>(static_cast<const uint16_t*>(tab.delta[t]) + base)
+        : static_cast<const void*>(static_cast<const float*>(tab.delta[t]) + base);
+    r.full = base + kChunk <= n;
+    r.valid = r.full ? kChunk : static_cast<int>(n - base);
+    return r;
+}
+
+// One thread: start the bulk copies of a full chunk's error buffer and delta into the stage.
+template <bool kBf16>
+__device__ __forceinline__ void prefetch(Smem& sm, const ChunkRef& r) {
+    constexpr uint32_t kDeltaBytes = kChunk * (kBf16 ? 2 : 4);
+    fence_async_smem();
+    mbar_expect_tx(&sm.bar, kChunk * 4 + kDeltaBytes);
+    bulk_load(sm.stage_e, r.ef, kChunk * 4, &sm.bar);
+    bulk_load(sm.stage_d, r.delta, kDeltaBytes, &sm.bar);
+}
+
+// a = fmaf(beta, e, delta) for this thread's 16 values, from the stage (full chunks).
+template <bool kBf16>
+__device__ __forceinline__ void accumulate_from_stage(const Smem& sm, float beta, int tid,
+                                                      float (&a)[kPer]) {
 #pragma unroll
-        for (int v = 0; v < kVec; ++v) e4[v] = ld_stream_f4(ef + v * 1024 + 4 * tid);
+    for (int v = 0; v < kVec; ++v) {
+        const int j0 = v * 1024 + 4 * tid;
+        const float4 e4 = *reinterpret_cast<const float4*>(&sm.stage_e[j0]);
+        float d[4];
         if constexpr (kBf16) {
-            uint2 d2[kVec];
-            const uint16_t* d = static_cast<const uint16_t*>(delta);
-#pragma unroll
-            for (int v = 0; v < kVec; ++v) d2[v] = ld_stream_u2(d + v * 1024 + 4 * tid);
-#pragma unroll
-            for (int v = 0; v < kVec; ++v) {
-                a[4 * v + 0] = __fmaf_rn(beta, e4[v].x, bf16_bits_to_float(d2[v].x & 0xffffu));
-                a[4 * v + 1] = __fmaf_rn(beta, e4[v].y, bf16_bits_to_float(d2[v].x >> 16));
-                a[4 * v + 2] = __fmaf_rn(beta, e4[v].z, bf16_bits_to_float(d2[v].y & 0xffffu));
-                a[4 * v + 3] = __fmaf_rn(beta, e4[v].w, bf16_bits_to_float(d2[v].y >> 16));
-            }
+            const uint2 d2 = *reinterpret_cast<const uint2*>(
+                reinterpret_cast<const uint16_t*>(sm.stage_d) + j0);
+            d[0] = bf16_bits_to_float(d2.x & 0xffffu);
+            d[1] = bf16_bits_to_float(d2.x >> 16);
+            d[2] = bf16_bits_to_float(d2.y & 0xffffu);
+            d[3] = bf16_bits_to_float(d2.y >> 16);
         } else {
-            float4 d4[kVec];
-            const float* d = static_cast<const float*>(delta);
-#pragma unroll
-            for (int v = 0; v < kVec; ++v) d4[v] = ld_stream_f4(d + v * 1024 + 4 * tid);
-#pragma unroll
-            for (int v = 0; v < kVec; ++v) {
-                a[4 * v + 0] = __fmaf_rn(beta, e4[v].x, d4[v].x);
-                a[4 * v + 1] = __fmaf_rn(beta, e4[v].y, d4[v].y);
-                a[4 * v + 2] = __fmaf_rn(beta, e4[v].z, d4[v].z);
-                a[4 * v + 3] = __fmaf_rn(beta, e4[v].w, d4[v].w);
-            }
+            const float4 d4 = *reinterpret_cast<const float4*>(&sm.stage_d[j0]);
+            d[0] = d4.x; d[1] = d4.y; d[2] = d4.z; d[3] = d4.w;
         }
-    } else {
-#pragma unroll
-        for (int v = 0; v < kVec; ++v)
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int j = v * 1024 + 4 * tid + u;
-                float d = 0.0f, e = 0.0f;
-                if (j < valid) {
-                    e = ef[j];
-                    d = kBf16 ? bf16_bits_to_float(static_cast<const uint16_t*>(delta)[j])
-                              : static_cast<const float*>(delta)[j];
-                }
-                a[4 * v + u] = j < valid ? __fmaf_rn(beta, e, d) : 0.0f;   // pads are +0
-            }
+        a[4 * v + 0] = __fmaf_rn(beta, e4.x, d[0]);
+        a[4 * v + 1] = __fmaf_rn(beta, e4.y, d[1]);
+        a[4 * v + 2] = __fmaf_rn(beta, e4.z, d[2]);
+        a[4 * v + 3] = __fmaf_rn(beta, e4.w, d[3]);
     }
 }
 
+// The same for a tail chunk, straight from global memory; pads are +0.
 template <bool kBf16>
-__global__ void __launch_bounds__(kThreads, 3)
+__device__ __forceinline__ void accumulate_tail(const ChunkRef& r, float beta, int tid,
+                                                float (&a)[kPer]) {
+#pragma unroll
+    for (int v = 0; v < kVec; ++v)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int j = v * 1024 + 4 * tid + u;
+            float d = 0.0f, e = 0.0f;
+            if (j < r.valid) {
+                e = r.ef[j];
+                d = kBf16 ? bf16_bits_to_float(static_cast<const uint16_t*>(r.delta)[j])
+                          : static_cast<const float*>(r.delta)[j];
+            }
+            a[4 * v + u] = j < r.valid ? __fmaf_rn(beta, e, d) : 0.0f;
+        }
+}
+
+#ifndef SPL_COMPRESS_MIN_BLOCKS
+#define SPL_COMPRESS_MIN_BLOCKS 3
+#endif
+
+template <bool kBf16>
+__global__ void __launch_bounds__(kThreads, SPL_COMPRESS_MIN_BLOCKS)
 k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload,
               float* __restrict__ scales, uint32_t* __restrict__ flags) {
-    __shared__ __align__(16) Smem sm;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
     const int64_t total = tab.chunk_begin[tab.num];
+    if (static_cast<int64_t>(blockIdx.x) >= total) return;
+
+    if (tid == 0) {
+        mbar_init(&sm.bar, 1);
+        const ChunkRef r0 = locate<kBf16>(tab, blockIdx.x);
+        if (r0.full) prefetch<kBf16>(sm, r0);
+    }
+    __syncthreads();
+
+    uint32_t parity = 0;
     bool nonfinite = false;
+    bool aborted = false;
 
     for (int64_t c = blockIdx.x; c < total; c += gridDim.x) {
-        int t = 0;
-        {
-            int hi = tab.num;
-            while (hi - t > 1) {
-                const int mid = (t + hi) >> 1;
-                if (tab.chunk_begin[mid] <= c) t = mid; else hi = mid;
-            }
-        }
-        const int64_t base = (c - tab.chunk_begin[t]) * kChunk;
-        const int64_t n = tab.n[t];
-        float* ef = tab.ef[t] + base;
-        const void* delta = kBf16
-            ? static_cast<const void*>(static_cast<const uint16_t*>(tab.delta[t]) + base)
-            : static_cast<const void*>(static_cast<const float*>(tab.delta[t]) + base);
-        const bool full = base + kChunk <= n;
-        const int valid = full ? kChunk : static_cast<int>(n - base);
+        const ChunkRef r = locate<kBf16>(tab, c);
 
-        // ---- a = beta * e + delta, and the magnitude keys --------------------------------
+        // ---- a = beta * e + delta (from the prefetched stage), and the magnitude keys -----
         float a[kPer];
-        load_accumulate<kBf16>(delta, ef, valid, full, beta, tid, a);
+        bool timed_out = false;
+        if (r.full) {
+            timed_out = !mbar_wait(&sm.bar, parity);
+            parity ^= 1u;
+            accumulate_from_stage<kBf16>(sm, beta, tid, a);
+        } else {
+            accumulate_tail<kBf16>(r, beta, tid, a);
+        }
         uint32_t key[kPer];
         uint32_t kmax = 0;
 #pragma unroll
@@ -180,143 +226,163 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
 
         // ---- clear the histograms and bitmaps; chunk max --------------------------------
         {
-            uint4* h4 = reinterpret_cast<uint4*>(&sm.hist[0][0]);
+            uint4* h4 = reinterpret_cast<uint4*>(&sm.hist[0]);
             const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) h4[tid + i * kThreads] = z;   // 2 x 2048 words
+            h4[tid] = z;                      // 2048 words
+            h4[tid + kThreads] = z;
+            if (tid < 128) reinterpret_cast<uint4*>(&sm.hist3[0])[tid] = z;   // 512 words
             if (tid < kBitmapWords) sm.sel_bm[tid] = 0;
             else sm.eq_bm[tid - kBitmapWords] = 0;
             kmax = __reduce_max_sync(0xffffffffu, kmax);
             if (lane == 0) sm.warp_max[warp] = kmax;
         }
-        __syncthreads();
+        if (__syncthreads_or(timed_out)) {
+            aborted = true;
+            break;
+        }
+        // the stage has been read by every thread: start the next chunk's copies
+        if (tid == 0 && c + gridDim.x < total) {
+            const ChunkRef rn = locate<kBf16>(tab, c + gridDim.x);
+            if (rn.full) prefetch<kBf16>(sm, rn);
+        }
         uint32_t mkey = 0;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) mkey = max(mkey, sm.warp_max[w]);
 
-        // ---- radix select of the 64th largest key ---------------------------------------
+        // ---- select: histogram of key bits [30:20] -> the bin D holding the 64th key ----
 #pragma unroll
-        for (int i = 0; i < kPer; ++i) atomicAdd(&sm.hist[0][key[i] >> 20], 1u);
+        for (int i = 0; i < kPer; ++i) atomicAdd(&sm.hist[key[i] >> 20], 1u);
         __syncthreads();
-        find_digit<2048>(sm, sm.hist[0], kTopK, tid, lane, warp);
+        find_digit<2048>(sm, sm.hist, kTopK, tid, lane, warp);
         __syncthreads();
-        uint32_t need = kTopK - sm.bcast[1];
-        uint32_t prefix = sm.bcast[0] << 20;
-        uint32_t pmask = 0x7ffu << 20;
-        bool done = sm.bcast[2] == need;
+        uint32_t need = kTopK - sm.bcast[1];      // keys still to take from bin D
+        const uint32_t dig = sm.bcast[0];
+        const uint32_t in_bin = sm.bcast[2];
 
-        if (!done) {
-            // hist[0] is free again: clear the 512 bins the last pass uses
-            sm.hist[0][tid] = 0;
-            sm.hist[0][tid + kThreads] = 0;
+        if (in_bin == need) {
+            // ---- bin D is taken whole: every key at or above it is in -------------------
+#pragma unroll
+            for (int v = 0; v < kVec; ++v)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int j = v * 1024 + 4 * tid + u;
+                    if ((key[4 * v + u] >> 20) >= dig) atomicOr(&sm.sel_bm[j >> 5], 1u << (j & 31));
+                }
+            __syncthreads();
+        } else {
+            // ---- resolve bin D: radix passes on key bits [19:9] and [8:0] ---------------
+            uint32_t prefix = dig << 20;
+            uint32_t pmask = 0x7ffu << 20;
+            {   // the first pass's bins have been read: clear them for the second pass
+                uint4* h4 = reinterpret_cast<uint4*>(&sm.hist[0]);
+                h4[tid] = make_uint4(0, 0, 0, 0);
+                h4[tid + kThreads] = make_uint4(0, 0, 0, 0);
+            }
+            __syncthreads();
 #pragma unroll
             for (int i = 0; i < kPer; ++i)
-                if ((key[i] & pmask) == prefix) atomicAdd(&sm.hist[1][(key[i] >> 9) & 0x7ffu], 1u);
+                if ((key[i] & pmask) == prefix) atomicAdd(&sm.hist[(key[i] >> 9) & 0x7ffu], 1u);
             __syncthreads();
-            find_digit<2048>(sm, sm.hist[1], need, tid, lane, warp);
+            find_digit<2048>(sm, sm.hist, need, tid, lane, warp);
             __syncthreads();
             need -= sm.bcast[1];
             prefix |= sm.bcast[0] << 9;
             pmask |= 0x7ffu << 9;
-            done = sm.bcast[2] == need;
-        }
-        if (!done) {
+            if (sm.bcast[2] != need) {
 #pragma unroll
-            for (int i = 0; i < kPer; ++i)
-                if ((key[i] & pmask) == prefix) atomicAdd(&sm.hist[0][key[i] & 0x1ffu], 1u);
-            __syncthreads();
-            find_digit<512>(sm, sm.hist[0], need, tid, lane, warp);
-            __syncthreads();
-            need -= sm.bcast[1];
-            prefix |= sm.bcast[0];
-            pmask = 0x7fffffffu;
-        }
-
-        // ---- mark keys above the threshold prefix, and the tie candidates ---------------
-#pragma unroll
-        for (int v = 0; v < kVec; ++v)
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const uint32_t mk = key[4 * v + u] & pmask;
-                const int j = v * 1024 + 4 * tid + u;
-                if (mk > prefix) atomicOr(&sm.sel_bm[j >> 5], 1u << (j & 31));
-                else if (mk == prefix) atomicOr(&sm.eq_bm[j >> 5], 1u << (j & 31));
+                for (int i = 0; i < kPer; ++i)
+                    if ((key[i] & pmask) == prefix) atomicAdd(&sm.hist3[key[i] & 0x1ffu], 1u);
+                __syncthreads();
+                find_digit<512>(sm, sm.hist3, need, tid, lane, warp);
+                __syncthreads();
+                need -= sm.bcast[1];
+                prefix |= sm.bcast[0];
+                pmask = 0x7fffffffu;
             }
-        __syncthreads();
+            // keys above the final prefix are in; ties at it go by index, lowest first
+#pragma unroll
+            for (int v = 0; v < kVec; ++v)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t mk = key[4 * v + u] & pmask;
+                    const int j = v * 1024 + 4 * tid + u;
+                    if (mk > prefix) atomicOr(&sm.sel_bm[j >> 5], 1u << (j & 31));
+                    else if (mk == prefix) atomicOr(&sm.eq_bm[j >> 5], 1u << (j & 31));
+                }
+            __syncthreads();
+            if (warp == 0) {
+                uint32_t eqw[4];
+                uint32_t cnt = 0;
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) {
+                    eqw[qq] = sm.eq_bm[4 * lane + qq];
+                    cnt += __popc(eqw[qq]);
+                }
+                uint32_t incl = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                const uint32_t before = incl - cnt;
+                uint32_t take = need > before ? min(need - before, cnt) : 0u;
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) {
+                    uint32_t w = eqw[qq];
+                    uint32_t kept = 0;
+                    while (take != 0u && w != 0u) {
+                        const uint32_t low = w & (0u - w);
+                        kept |= low;
+                        w ^= low;
+                        --take;
+                    }
+                    sm.sel_bm[4 * lane + qq] |= kept;
+                }
+            }
+            __syncthreads();
+        }
 
-        // ---- one warp: take the first `need` ties, compact the 64 indices ascending ------
+        // ---- warp 0: chosen positions before each bitmap word ----------------------------
         if (warp == 0) {
-            uint32_t eqw[4];
-            uint32_t cnt = 0;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                eqw[q] = sm.eq_bm[4 * lane + q];
-                cnt += __popc(eqw[q]);
-            }
-            uint32_t incl = cnt;
+            const uint4 w4 = *reinterpret_cast<const uint4*>(&sm.sel_bm[4 * lane]);
+            const uint32_t c0 = __popc(w4.x), c1 = __popc(w4.y), c2 = __popc(w4.z);
+            const uint32_t mine = c0 + c1 + c2 + __popc(w4.w);
+            uint32_t incl = mine;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
                 if (lane >= o) incl += y;
             }
-            const uint32_t before = incl - cnt;
-            uint32_t take = need > before ? min(need - before, cnt) : 0u;
-            uint32_t fin[4];
-            uint32_t fcnt = 0;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint32_t w = eqw[q];
-                uint32_t kept = 0;
-                while (take != 0u && w != 0u) {
-                    const uint32_t low = w & (0u - w);
-                    kept |= low;
-                    w ^= low;
-                    --take;
-                }
-                fin[q] = sm.sel_bm[4 * lane + q] | kept;
-                sm.fin_bm[4 * lane + q] = fin[q];
-                fcnt += __popc(fin[q]);
-            }
-            uint32_t pos = fcnt;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t y = __shfl_up_sync(0xffffffffu, pos, o);
-                if (lane >= o) pos += y;
-            }
-            pos -= fcnt;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint32_t w = fin[q];
-                while (w != 0u) {
-                    const int b = __ffs(w) - 1;
-                    if (pos < kTopK) sm.sel_idx[pos] = static_cast<uint16_t>(128 * lane + 32 * q + b);
-                    ++pos;
-                    w &= w - 1u;
-                }
-            }
-            if (lane == 0) sm.scale = __fdiv_rn(__uint_as_float(mkey), 1.5f);
+            const uint32_t p0 = incl - mine;
+            *reinterpret_cast<uint2*>(&sm.pre[4 * lane]) =
+                make_uint2(p0 | ((p0 + c0) << 16), (p0 + c0 + c1) | ((p0 + c0 + c1 + c2) << 16));
         }
         __syncthreads();
 
-        // ---- owners: codes and residuals; store the error buffer once -------------------
-        const float s = sm.scale;
+        // ---- owners: rank, code and residual of each chosen value ------------------------
+        const float s = __fdiv_rn(__uint_as_float(mkey), 1.5f);
 #pragma unroll
         for (int v = 0; v < kVec; ++v) {
             const int j0 = v * 1024 + 4 * tid;
-            const uint32_t bits = sm.fin_bm[j0 >> 5] >> (j0 & 31);
+            const uint32_t word = sm.sel_bm[j0 >> 5];
+            const int sh = j0 & 31;
+            if (((word >> sh) & 0xfu) == 0u) continue;
+            const uint32_t base_rank = sm.pre[j0 >> 5];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                if ((bits >> u) & 1u) {
+                if ((word >> (sh + u)) & 1u) {
+                    const uint32_t rank = base_rank + __popc(word & ((1u << (sh + u)) - 1u));
                     const uint32_t code = quant_code(a[4 * v + u], s);
                     a[4 * v + u] = __fsub_rn(a[4 * v + u], level_value(code, s));
-                    sm.code_at[j0 + u] = static_cast<uint8_t>(code);
+                    if (rank < kTopK)
+                        sm.fields[rank] = static_cast<uint16_t>(code | (static_cast<uint32_t>(j0 + u) << 2));
                 }
             }
         }
-        if (full) {
+        if (r.full) {
 #pragma unroll
             for (int v = 0; v < kVec; ++v)
-                st_stream_f4(ef + v * 1024 + 4 * tid,
+                st_stream_f4(r.ef + v * 1024 + 4 * tid,
                              make_float4(a[4 * v], a[4 * v + 1], a[4 * v + 2], a[4 * v + 3]));
         } else {
 #pragma unroll
@@ -324,23 +390,39 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int j = v * 1024 + 4 * tid + u;
-                    if (j < valid) ef[j] = a[4 * v + u];
+                    if (j < r.valid) r.ef[j] = a[4 * v + u];
                 }
         }
         __syncthreads();
 
         // ---- one warp: pack the record and write the scale ------------------------------
         if (warp == 0) {
-            const uint32_t i0 = sm.sel_idx[lane];
-            const uint32_t i1 = sm.sel_idx[lane + 32];
-            const uint32_t f0 = sm.code_at[i0] | (i0 << 2);
-            const uint32_t f1 = sm.code_at[i1] | (i1 << 2);
-            const uint32_t word = record_word(f0, f1, lane);
+            const int w = lane < kRecordWords ? lane : kRecordWords - 1;
+            const int r_first = (32 * w) / kFieldBits;
+            const int r_last = (32 * w + 31) / kFieldBits;
+            uint32_t word = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int r = r_first + k;
+                if (r <= r_last) {
+                    const uint32_t f = sm.fields[r];
+                    const int off = kFieldBits * r - 32 * w;
+                    word |= off >= 0 ? (f << off) : (f >> (-off));
+                }
+            }
             store_record(payload + c * kRecordBytes, word, lane);
             if (lane == 0) scales[c] = s;
         }
     }
-    if (nonfinite && flags != nullptr) atomicOr(flags, kFlagNonFinite);
+    if (aborted && tid == 0) {
+        // the copy that did not complete may still land: wait once more (bounded) before
+        // the CTA's shared memory is released
+        mbar_wait(&sm.bar, parity ^ 1u);
+    }
+    if (flags != nullptr) {
+        if (nonfinite) atomicOr(flags, kFlagNonFinite);
+        if (aborted && tid == 0) atomicOr(flags, kFlagTimeout);
+    }
 }
 
 }  // namespace
@@ -352,13 +434,17 @@ cudaError_t launch_ef_compress(const CompressTable& tab, bool bf16, float beta,
     if (total == 0) return cudaSuccess;
     const void* kern = bf16 ? reinterpret_cast<const void*>(&k_ef_compress<true>)
                             : reinterpret_cast<const void*>(&k_ef_compress<false>);
-    const int resident = persistent_grid(kern, kThreads, 0);
+    const size_t smem = sizeof(Smem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const int resident = persistent_grid(kern, kThreads, smem);
     if (resident <= 0) return cudaErrorInvalidConfiguration;
     const int grid = static_cast<int>(total < resident ? total : resident);
     if (bf16)
-        k_ef_compress<true><<<grid, kThreads, 0, stream>>>(tab, beta, payload, scales, flags);
+        k_ef_compress<true><<<grid, kThreads, smem, stream>>>(tab, beta, payload, scales, flags);
     else
-        k_ef_compress<false><<<grid, kThreads, 0, stream>>>(tab, beta, payload, scales, flags);
+        k_ef_compress<false><<<grid, kThreads, smem, stream>>>(tab, beta, payload, scales, flags);
     return cudaGetLastError();
 }
 

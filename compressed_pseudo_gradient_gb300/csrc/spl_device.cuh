@@ -19,6 +19,10 @@ constexpr int kRecordVec = kRecordBytes / 16;    // 7 x 16 bytes
 
 constexpr uint32_t kFlagNonFinite = 1u;
 constexpr uint32_t kFlagBadRecord = 2u;
+constexpr uint32_t kFlagTimeout = 4u;
+
+// Upper bound on any wait for an asynchronous copy: a healthy copy lands in microseconds.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 // |a| as an ordered integer key: for non-NaN floats, unsigned order of (bits & 0x7fffffff)
 // equals order of |a|.  Every NaN maps to one key just above +Inf, so NaNs rank first and
@@ -43,6 +47,25 @@ __device__ __forceinline__ float level_value(uint32_t code, float s) {
     return (code & 2u) ? -q : q;
 }
 
+// x / d rounded to nearest, given rd = RN(1 / d): Markstein's correction step (P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990): q0 = RN(x * rd), the remainder x - q0 * d is exact in one fma, and
+// RN(q0 + rem * rd) is the correctly rounded quotient.  The tests compare it with the
+// correctly rounded division for every divisor 1..256 over every significand, over every
+// dividend below 2^-111 (quotients near and below the normal range), and on zeros,
+// infinities and NaN.
+// The correction is exact while q0 is zero or a normal number: tiny nonzero quotients (and
+// infinities or NaN, for which the remainder is NaN) take the correctly rounded division.
+__device__ __forceinline__ float div_rn(float x, float d, float rd) {
+    const float q0 = __fmul_rn(x, rd);
+    const float aq = fabsf(q0);
+    if ((aq < 2.3509887e-38f && aq != 0.0f) || !(aq <= 3.402823466e38f))  // 2^-125, FLT_MAX
+        return __fdiv_rn(x, d);
+    const float rem = __fmaf_rn(-q0, d, x);
+    const float q = __fmaf_rn(rem, rd, q0);
+    return aq == 0.0f ? q0 : q;   // keeps the sign of a zero quotient
+}
+
 // 16-byte streaming accesses: the codec touches every dense byte exactly once.
 __device__ __forceinline__ float4 ld_stream_f4(const float* p) {
     return __ldcs(reinterpret_cast<const float4*>(p));
@@ -56,6 +79,87 @@ __device__ __forceinline__ void st_stream_f4(float* p, float4 v) {
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t h16) {
     return __uint_as_float(h16 << 16);
+}
+
+// ---- 1-D bulk copies (TMA, no multicast, no cluster launch) completed on an mbarrier ------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_inval(uint64_t* bar) {
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Orders this thread's earlier generic-proxy shared-memory accesses before later bulk copies.
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Global -> shared copy of `bytes` (a multiple of 16; both addresses 16-byte aligned).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// 16-byte global -> shared copy (cp.async) whose completion is later reported to an mbarrier.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+                 : "memory");
+}
+
+// One arrival on the mbarrier once all of this thread's earlier cp.async copies have landed
+// (counted against the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0u;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits for the phase with the given parity to complete, for at most kWaitLimitNs.
+// Returns false on timeout (the caller reports kFlagTimeout and stops).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
 }
 
 // Builds record word w (0..27) of a chunk from the 64 fields held by one warp: lane l holds
@@ -99,6 +203,15 @@ __device__ __forceinline__ uint32_t record_field(const uint32_t* words, int r) {
     uint32_t v = words[w] >> off;
     if (off > 32 - kFieldBits) v |= words[w + 1] << (32 - off);
     return v & ((1u << kFieldBits) - 1u);
+}
+
+// The same with one funnel shift.  Reads words[w + 1] even when the field ends inside
+// words[w] (its bits are masked off), so the word after the record must be readable shared
+// memory.
+__device__ __forceinline__ uint32_t record_field_fs(const uint32_t* words, int r) {
+    const int bit = kFieldBits * r;
+    const int w = bit >> 5;
+    return __funnelshift_r(words[w], words[w + 1], bit & 31) & ((1u << kFieldBits) - 1u);
 }
 
 }  // namespace spl

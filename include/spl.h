@@ -29,7 +29,9 @@
  *     synchronously; SPL_ERR_CUDA means a launch failed (spl_last_cuda_error() gives the
  *     cudaError_t value on the calling thread);
  *   - conditions found on the device are OR-ed into *d_flags (if d_flags is not NULL), which
- *     the caller reads after synchronising: SPL_FLAG_NONFINITE, SPL_FLAG_BAD_RECORD;
+ *     the caller reads after synchronising: SPL_FLAG_NONFINITE, SPL_FLAG_BAD_RECORD, and
+ *     SPL_FLAG_TIMEOUT (an asynchronous copy into shared memory did not complete within one
+ *     second; the kernel stopped early and its outputs are incomplete);
  *   - device pointers to fp32/bf16 dense arrays and to records must be 16-byte aligned;
  *     scales and flags 4-byte aligned; idx 2-byte aligned.
  */
@@ -63,7 +65,7 @@ enum {
     SPL_MAX_TENSORS_PER_LAUNCH = 64 /* spl_ef_compress_multi splits larger tables */
 };
 
-enum { SPL_FLAG_NONFINITE = 1u, SPL_FLAG_BAD_RECORD = 2u };
+enum { SPL_FLAG_NONFINITE = 1u, SPL_FLAG_BAD_RECORD = 2u, SPL_FLAG_TIMEOUT = 4u };
 
 /* Number of 4096-value chunks of an n-value tensor: ceil(n / 4096). */
 size_t spl_num_chunks(size_t n);
