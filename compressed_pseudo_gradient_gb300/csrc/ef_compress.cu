@@ -34,6 +34,8 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kPer = kChunk / kThreads;    // 16 values per thread
 constexpr int kVec = kPer / 4;             // 4 vectors of 4 per thread
 constexpr int kBitmapWords = kChunk / 32;  // 128
+constexpr uint32_t kWindow = 16u << 23;    // 16 octaves of magnitude keys
+constexpr uint32_t kNotFound = 0xffffffffu;
 
 struct Smem {
     float stage_e[kChunk];          // prefetched error-buffer chunk (bulk copy)
@@ -45,6 +47,8 @@ struct Smem {
     uint32_t warp_tot[kWarps];
     uint32_t warp_max[kWarps];
     uint32_t bcast[3];              // digit, count above the digit's bin, count in the bin
+    uint2 cand[32];                 // (key, index) of the keys in the boundary bin
+    uint32_t ncand;
     uint16_t fields[kTopK];         // the record's 64 fields, in ascending index order
     alignas(16) uint16_t pre[kBitmapWords];   // chosen positions before each bitmap word
     uint64_t bar;                   // completes when the stage's bulk copies have landed
@@ -175,6 +179,111 @@ __device__ __forceinline__ void accumulate_tail(const ChunkRef& r, float beta, i
         }
 }
 
+// Generic select (any data): radix passes on key bits [30:20], [19:9] and [8:0], each over
+// the keys matching the digits found so far, stopping once the boundary bin is taken whole;
+// ties at the final threshold go to the lowest indices.  Marks the 64 chosen positions in
+// sm.sel_bm.  Entered by all threads with sm.hist3 and sm.sel_bm/eq_bm cleared; clears hist.
+__device__ __forceinline__ void generic_select(Smem& sm, const uint32_t (&key)[kPer], int tid,
+                                               int lane, int warp) {
+    {
+        uint4* h4 = reinterpret_cast<uint4*>(&sm.hist[0]);
+        h4[tid] = make_uint4(0, 0, 0, 0);
+        h4[tid + kThreads] = make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) atomicAdd(&sm.hist[key[i] >> 20], 1u);
+    __syncthreads();
+    find_digit<2048>(sm, sm.hist, kTopK, tid, lane, warp);
+    __syncthreads();
+    uint32_t need = kTopK - sm.bcast[1];      // keys still to take from bin D
+    const uint32_t dig = sm.bcast[0];
+    const uint32_t in_bin = sm.bcast[2];
+
+    if (in_bin == need) {
+        // ---- bin D is taken whole: every key at or above it is in -------------------
+#pragma unroll
+        for (int v = 0; v < kVec; ++v)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int j = v * 1024 + 4 * tid + u;
+                if ((key[4 * v + u] >> 20) >= dig) atomicOr(&sm.sel_bm[j >> 5], 1u << (j & 31));
+            }
+        __syncthreads();
+    } else {
+        // ---- resolve bin D: radix passes on key bits [19:9] and [8:0] ---------------
+        uint32_t prefix = dig << 20;
+        uint32_t pmask = 0x7ffu << 20;
+        {   // the first pass's bins have been read: clear them for the second pass
+            uint4* h4 = reinterpret_cast<uint4*>(&sm.hist[0]);
+            h4[tid] = make_uint4(0, 0, 0, 0);
+            h4[tid + kThreads] = make_uint4(0, 0, 0, 0);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < kPer; ++i)
+            if ((key[i] & pmask) == prefix) atomicAdd(&sm.hist[(key[i] >> 9) & 0x7ffu], 1u);
+        __syncthreads();
+        find_digit<2048>(sm, sm.hist, need, tid, lane, warp);
+        __syncthreads();
+        need -= sm.bcast[1];
+        prefix |= sm.bcast[0] << 9;
+        pmask |= 0x7ffu << 9;
+        if (sm.bcast[2] != need) {
+#pragma unroll
+            for (int i = 0; i < kPer; ++i)
+                if ((key[i] & pmask) == prefix) atomicAdd(&sm.hist3[key[i] & 0x1ffu], 1u);
+            __syncthreads();
+            find_digit<512>(sm, sm.hist3, need, tid, lane, warp);
+            __syncthreads();
+            need -= sm.bcast[1];
+            prefix |= sm.bcast[0];
+            pmask = 0x7fffffffu;
+        }
+        // keys above the final prefix are in; ties at it go by index, lowest first
+#pragma unroll
+        for (int v = 0; v < kVec; ++v)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t mk = key[4 * v + u] & pmask;
+                const int j = v * 1024 + 4 * tid + u;
+                if (mk > prefix) atomicOr(&sm.sel_bm[j >> 5], 1u << (j & 31));
+                else if (mk == prefix) atomicOr(&sm.eq_bm[j >> 5], 1u << (j & 31));
+            }
+        __syncthreads();
+        if (warp == 0) {
+            uint32_t eqw[4];
+            uint32_t cnt = 0;
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+                eqw[qq] = sm.eq_bm[4 * lane + qq];
+                cnt += __popc(eqw[qq]);
+            }
+            uint32_t incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const uint32_t before = incl - cnt;
+            uint32_t take = need > before ? min(need - before, cnt) : 0u;
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+                uint32_t w = eqw[qq];
+                uint32_t kept = 0;
+                while (take != 0u && w != 0u) {
+                    const uint32_t low = w & (0u - w);
+                    kept |= low;
+                    w ^= low;
+                    --take;
+                }
+                sm.sel_bm[4 * lane + qq] |= kept;
+            }
+        }
+        __syncthreads();
+    }
+}
+
 #ifndef SPL_COMPRESS_MIN_BLOCKS
 #define SPL_COMPRESS_MIN_BLOCKS 3
 #endif
@@ -233,6 +342,10 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
             if (tid < 128) reinterpret_cast<uint4*>(&sm.hist3[0])[tid] = z;   // 512 words
             if (tid < kBitmapWords) sm.sel_bm[tid] = 0;
             else sm.eq_bm[tid - kBitmapWords] = 0;
+            if (tid == 0) {
+                sm.ncand = 0;
+                sm.bcast[0] = kNotFound;
+            }
             kmax = __reduce_max_sync(0xffffffffu, kmax);
             if (lane == 0) sm.warp_max[warp] = kmax;
         }
@@ -249,98 +362,58 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) mkey = max(mkey, sm.warp_max[w]);
 
-        // ---- select: histogram of key bits [30:20] -> the bin D holding the 64th key ----
-#pragma unroll
-        for (int i = 0; i < kPer; ++i) atomicAdd(&sm.hist[key[i] >> 20], 1u);
-        __syncthreads();
-        find_digit<2048>(sm, sm.hist, kTopK, tid, lane, warp);
-        __syncthreads();
-        uint32_t need = kTopK - sm.bcast[1];      // keys still to take from bin D
-        const uint32_t dig = sm.bcast[0];
-        const uint32_t in_bin = sm.bcast[2];
-
-        if (in_bin == need) {
-            // ---- bin D is taken whole: every key at or above it is in -------------------
-#pragma unroll
-            for (int v = 0; v < kVec; ++v)
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int j = v * 1024 + 4 * tid + u;
-                    if ((key[4 * v + u] >> 20) >= dig) atomicOr(&sm.sel_bm[j >> 5], 1u << (j & 31));
-                }
-            __syncthreads();
-        } else {
-            // ---- resolve bin D: radix passes on key bits [19:9] and [8:0] ---------------
-            uint32_t prefix = dig << 20;
-            uint32_t pmask = 0x7ffu << 20;
-            {   // the first pass's bins have been read: clear them for the second pass
-                uint4* h4 = reinterpret_cast<uint4*>(&sm.hist[0]);
-                h4[tid] = make_uint4(0, 0, 0, 0);
-                h4[tid + kThreads] = make_uint4(0, 0, 0, 0);
-            }
-            __syncthreads();
+        // ---- select, fast path: 2048 bins of 1/128 octave over the 16 octaves below the
+        //      largest key; the 64th key almost always falls inside, and its bin holds only a
+        //      few keys, which warp 0 ranks directly.  Otherwise: the generic radix select.
+        const bool windowed = mkey < kKeyInf;
+        const uint32_t lo_key = mkey > kWindow ? mkey - kWindow : 0u;
+        if (windowed) {
 #pragma unroll
             for (int i = 0; i < kPer; ++i)
-                if ((key[i] & pmask) == prefix) atomicAdd(&sm.hist[(key[i] >> 9) & 0x7ffu], 1u);
-            __syncthreads();
-            find_digit<2048>(sm, sm.hist, need, tid, lane, warp);
-            __syncthreads();
-            need -= sm.bcast[1];
-            prefix |= sm.bcast[0] << 9;
-            pmask |= 0x7ffu << 9;
-            if (sm.bcast[2] != need) {
-#pragma unroll
-                for (int i = 0; i < kPer; ++i)
-                    if ((key[i] & pmask) == prefix) atomicAdd(&sm.hist3[key[i] & 0x1ffu], 1u);
-                __syncthreads();
-                find_digit<512>(sm, sm.hist3, need, tid, lane, warp);
-                __syncthreads();
-                need -= sm.bcast[1];
-                prefix |= sm.bcast[0];
-                pmask = 0x7fffffffu;
-            }
-            // keys above the final prefix are in; ties at it go by index, lowest first
-#pragma unroll
-            for (int v = 0; v < kVec; ++v)
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const uint32_t mk = key[4 * v + u] & pmask;
-                    const int j = v * 1024 + 4 * tid + u;
-                    if (mk > prefix) atomicOr(&sm.sel_bm[j >> 5], 1u << (j & 31));
-                    else if (mk == prefix) atomicOr(&sm.eq_bm[j >> 5], 1u << (j & 31));
-                }
-            __syncthreads();
-            if (warp == 0) {
-                uint32_t eqw[4];
-                uint32_t cnt = 0;
-#pragma unroll
-                for (int qq = 0; qq < 4; ++qq) {
-                    eqw[qq] = sm.eq_bm[4 * lane + qq];
-                    cnt += __popc(eqw[qq]);
-                }
-                uint32_t incl = cnt;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += y;
-                }
-                const uint32_t before = incl - cnt;
-                uint32_t take = need > before ? min(need - before, cnt) : 0u;
-#pragma unroll
-                for (int qq = 0; qq < 4; ++qq) {
-                    uint32_t w = eqw[qq];
-                    uint32_t kept = 0;
-                    while (take != 0u && w != 0u) {
-                        const uint32_t low = w & (0u - w);
-                        kept |= low;
-                        w ^= low;
-                        --take;
-                    }
-                    sm.sel_bm[4 * lane + qq] |= kept;
-                }
-            }
-            __syncthreads();
+                if (key[i] >= lo_key) atomicAdd(&sm.hist[min((key[i] - lo_key) >> 16, 2047u)], 1u);
         }
+        __syncthreads();
+        if (windowed) find_digit<2048>(sm, sm.hist, kTopK, tid, lane, warp);
+        __syncthreads();
+        bool selected = false;
+        if (windowed && sm.bcast[0] != kNotFound) {
+            const uint32_t need = kTopK - sm.bcast[1];
+            const uint32_t dig = sm.bcast[0];
+            const uint32_t in_bin = sm.bcast[2];
+            if (in_bin == need || in_bin <= 32u) {
+                const bool rank_bin = in_bin != need;
+#pragma unroll
+                for (int v = 0; v < kVec; ++v)
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const uint32_t kk = key[4 * v + u];
+                        if (kk < lo_key) continue;
+                        const uint32_t bin = min((kk - lo_key) >> 16, 2047u);
+                        const int j = v * 1024 + 4 * tid + u;
+                        if (bin > dig || (bin == dig && !rank_bin)) {
+                            atomicOr(&sm.sel_bm[j >> 5], 1u << (j & 31));
+                        } else if (bin == dig) {
+                            const uint32_t slot = atomicAdd(&sm.ncand, 1u);
+                            if (slot < 32u) sm.cand[slot] = make_uint2(kk, static_cast<uint32_t>(j));
+                        }
+                    }
+                __syncthreads();
+                if (rank_bin && warp == 0) {
+                    const uint2 me = static_cast<uint32_t>(lane) < in_bin ? sm.cand[lane] : make_uint2(0u, 0u);
+                    uint32_t rank = 0;
+                    for (uint32_t o = 0; o < in_bin; ++o) {
+                        const uint32_t ok = __shfl_sync(0xffffffffu, me.x, o);
+                        const uint32_t oj = __shfl_sync(0xffffffffu, me.y, o);
+                        rank += (ok > me.x || (ok == me.x && oj < me.y)) ? 1u : 0u;
+                    }
+                    if (static_cast<uint32_t>(lane) < in_bin && rank < need)
+                        atomicOr(&sm.sel_bm[me.y >> 5], 1u << (me.y & 31));
+                    __syncwarp();
+                }
+                selected = true;
+            }
+        }
+        if (!selected) generic_select(sm, key, tid, lane, warp);
 
         // ---- warp 0: chosen positions before each bitmap word ----------------------------
         if (warp == 0) {

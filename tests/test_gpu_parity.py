@@ -119,6 +119,43 @@ def test_degenerate_chunks():
     compare_full_round(delta, ef, -0.5, "degenerate round 3 (negative beta)")
 
 
+def test_select_window_edges():
+    """Chunks built around the compress kernel's fast path: its histogram spans the 16 octaves
+    below the chunk max and ranks a boundary bin of at most 32 keys directly; everything else
+    takes the generic radix select.  Both must agree with the oracle."""
+    rng = np.random.default_rng(17)
+    L = 4096
+    base = (rng.random(L).astype(np.float32) * 0.5 + 0.25)               # ~[0.25, 0.75)
+
+    def chunk(f):
+        c = base.copy() * rng.choice([-1.0, 1.0], L).astype(np.float32)
+        f(c)
+        return c
+
+    def spikes_far_above(c):       # 63 values 2^40 above: 64th key 40 octaves below the max
+        c[rng.choice(L, 63, replace=False)] = 2.0 ** 40
+    def spikes_just_inside(c):     # 63 values 2^14 above: the 64th key inside the window
+        c[rng.choice(L, 63, replace=False)] = 2.0 ** 14
+    def ties(count):
+        def f(c):                  # `count` keys equal at the threshold, 40 above it
+            pos = rng.choice(L, 40 + count, replace=False)
+            c[pos[:40]] = 2.0
+            c[pos[40:]] = -1.0     # the rest of the chunk stays below 0.75
+        return f
+    def one_per_bin(c):            # distinct powers of two: each key alone in its bin
+        c[:] = 0.0
+        c[rng.choice(L, 80, replace=False)] = 2.0 ** -np.arange(80, dtype=np.float32) * 8
+    def exact_bin(c):              # exactly 64 keys at or above one value
+        c[rng.choice(L, 64, replace=False)] = 3.0
+    blocks = [chunk(spikes_far_above), chunk(spikes_just_inside), chunk(ties(20)),
+              chunk(ties(24)), chunk(ties(25)), chunk(ties(33)), chunk(ties(200)),
+              chunk(one_per_bin), chunk(exact_bin)]
+    delta = _chunks(*blocks)
+    ef = torch.zeros_like(delta)
+    compare_full_round(delta, ef, 1.0, "window edges round 1")
+    compare_full_round(delta, ef, 0.5, "window edges round 2")
+
+
 def test_bf16_ties_stress():
     """bf16 values have 8 significant bits: many exact ties at the threshold."""
     gen = synth.generator(5, DEV)
