@@ -15,17 +15,16 @@
 //     completing on one mbarrier; the next chunk's P scales travel as plain loads into
 //     registers (lane l of warp w holds peer 8 l + w's);
 //   - each warp unpacks whole records (one peer at a time): the 64 14-bit fields, a check that
-//     the indices ascend strictly and the scale is finite and non-negative, the decoded value
-//     of every entry, and, per 512-position slice of the chunk, the range of entry ranks that
-//     falls into it (a rejected record gets empty ranges);
-//   - warp w owns slice [512 w, 512 w + 512) of a 16 KB shared accumulator and adds its
-//     entries peer by peer, in order p = 0..P-1 (a valid record hits a position at most once),
-//     so every position is summed in fp32 in peer order from +0.0, as a plain sequential loop
-//     over peers would; no atomics, no cross-warp hazards;
-//   - the same warp then runs the dense pass over its slice: divide by P (correctly rounded,
-//     with a precomputed reciprocal), store the mean and the updated theta with streaming
-//     stores, clear the slice.  Peers are unpacked in groups of up to 64, so shared memory
-//     stays bounded for any P.
+//     the indices ascend strictly and the scale is finite and non-negative, and the decoded
+//     value of every entry, stored as (position, value) pairs;
+//   - then one warp adds the peers into a 16 KB shared accumulator in order p = 0..P-1, two
+//     entries per lane (distinct positions within a valid record), so every position is summed
+//     in fp32 in peer order from +0.0, as a plain sequential loop over peers would, with no
+//     atomics; a single warp keeps every lane busy and the instruction count minimal, while
+//     the other resident CTAs keep the SM fed;
+//   - the dense pass divides by P (correctly rounded, with a precomputed reciprocal), stores
+//     the mean and the updated theta with streaming stores and clears the accumulator.  Peers
+//     are unpacked in groups of up to 64, so shared memory stays bounded for any P.
 #include <cfloat>
 
 #include "spl_device.cuh"
@@ -49,9 +48,9 @@ __host__ __device__ constexpr size_t align16(size_t x) { return (x + 15) & ~size
 
 // Dynamic shared memory for P peers (offsets 16-byte aligned), G = min(P, 64):
 //   bar[2] | theta stage [S][4096] f32 | record stage [S][P][112] (+16) | acc [4096] f32 |
-//   entries [G][64] (position, value) | slice ranges [G][16] u8
+//   entries [G][64] (position, value) | validity [G] u32
 struct Layout {
-    size_t bar, theta, rec, acc, ent, rng, total;
+    size_t bar, theta, rec, acc, ent, ok, total;
     __host__ __device__ explicit Layout(int P) {
         const size_t G = static_cast<size_t>(P < kGroup ? P : kGroup);
         bar = 0;
@@ -59,8 +58,8 @@ struct Layout {
         rec = theta + kStages * kChunk * 4;
         acc = rec + align16(kStages * static_cast<size_t>(P) * kRecordBytes) + 16;
         ent = acc + kChunk * 4;
-        rng = ent + G * kTopK * 8;
-        total = rng + G * 16;
+        ok = ent + G * kTopK * 8;
+        total = ok + align16(G * 4);
     }
 };
 
@@ -101,7 +100,7 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
     uint8_t* st_rec = smem_raw + L.rec;
     float* acc = reinterpret_cast<float*>(smem_raw + L.acc);
     uint2* ent = reinterpret_cast<uint2*>(smem_raw + L.ent);
-    uint8_t* rng = smem_raw + L.rng;
+    uint32_t* okp = reinterpret_cast<uint32_t*>(smem_raw + L.ok);
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -168,29 +167,14 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
                 const float s = __shfl_sync(0xffffffffu, sc_cur, p >> 3);
                 const bool ok = __all_sync(0xffffffffu, i0 < next0 && (lane == 31 || i1 < next1)) &&
                                 s >= 0.0f && s <= FLT_MAX;
-                uint8_t* rg = rng + g * 16;
                 if (ok) {
                     uint2* eg = ent + g * kTopK;
                     eg[lane] = make_uint2(i0, __float_as_uint(level_value(f0 & 3u, s)));
                     eg[lane + 32] = make_uint2(i1, __float_as_uint(level_value(f1 & 3u, s)));
-                    // rank of the first entry of slice k, for k = 0..8
-                    const int s0 = static_cast<int>(i0 >> 9);
-                    const int s1 = static_cast<int>(i1 >> 9);
-                    const int last_lo = __shfl_sync(0xffffffffu, s0, 31);
-                    int prev0 = __shfl_up_sync(0xffffffffu, s0, 1);
-                    int prev1 = __shfl_up_sync(0xffffffffu, s1, 1);
-                    if (lane == 0) {
-                        prev0 = -1;
-                        prev1 = last_lo;
-                    }
-                    for (int k = prev0 + 1; k <= s0; ++k) rg[k] = static_cast<uint8_t>(lane);
-                    for (int k = prev1 + 1; k <= s1; ++k) rg[k] = static_cast<uint8_t>(lane + 32);
-                    if (lane == 31)
-                        for (int k = s1 + 1; k <= kWarps; ++k) rg[k] = kTopK;
                 } else {
-                    if (lane <= kWarps) rg[lane] = 0;   // empty ranges: contributes nothing
                     bad = true;
                 }
+                if (lane == 0) okp[g] = ok ? 1u : 0u;
             }
             const bool last = g0 + kGroup >= P;
             if (last) {
@@ -207,28 +191,33 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
             } else {
                 __syncthreads();
             }
-            // ---- this warp's slice: add the entries peer by peer, in order --------------
-            int lo_n = rng[warp];
-            int hi_n = rng[warp + 1];
-            for (int g = 0; g < gn; ++g) {
-                const int lo = lo_n;
-                const int hi = hi_n;
-                if (g + 1 < gn) {
-                    lo_n = rng[(g + 1) * 16 + warp];
-                    hi_n = rng[(g + 1) * 16 + warp + 1];
+            // ---- one warp: add the peers in order, two entries per lane -------------------
+            if (warp == 0) {
+                uint2 e0n = ent[lane];
+                uint2 e1n = ent[lane + 32];
+                uint32_t okn = okp[0];
+                for (int g = 0; g < gn; ++g) {
+                    const uint2 e0 = e0n;
+                    const uint2 e1 = e1n;
+                    const uint32_t ok = okn;
+                    if (g + 1 < gn) {
+                        e0n = ent[(g + 1) * kTopK + lane];
+                        e1n = ent[(g + 1) * kTopK + lane + 32];
+                        okn = okp[g + 1];
+                    }
+                    if (ok != 0u) {
+                        acc[e0.x] = __fadd_rn(acc[e0.x], __uint_as_float(e0.y));
+                        acc[e1.x] = __fadd_rn(acc[e1.x], __uint_as_float(e1.y));
+                    }
+                    __syncwarp();
                 }
-                for (int r = lo + lane; r < hi; r += 32) {
-                    const uint2 e = ent[g * kTopK + r];
-                    acc[e.x] = __fadd_rn(acc[e.x], __uint_as_float(e.y));
-                }
-                __syncwarp();
             }
-            __syncthreads();   // entries and ranges are rewritten by the next pass
+            __syncthreads();   // the accumulator is complete; entries are rewritten next pass
         }
         if (aborted) break;
         sc_cur = sc_next;
 
-        // ---- dense pass over this warp's slice: mean, outer step --------------------------
+        // ---- dense pass: mean, outer step --------------------------------------------------
 #pragma unroll
         for (int v = 0; v < kVec; ++v) {
             const int j0 = slice0 + 128 * v + 4 * lane;

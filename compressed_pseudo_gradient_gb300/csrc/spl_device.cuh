@@ -54,16 +54,17 @@ __device__ __forceinline__ float level_value(uint32_t code, float s) {
 // correctly rounded division for every divisor 1..256 over every significand, over every
 // dividend below 2^-111 (quotients near and below the normal range), and on zeros,
 // infinities and NaN.
-// The correction is exact while q0 is zero or a normal number: tiny nonzero quotients (and
-// infinities or NaN, for which the remainder is NaN) take the correctly rounded division.
+// The correction is exact while q0 is zero or a normal number: a zero quotient is q0 itself
+// (keeping its sign), and tiny nonzero quotients (and infinities or NaN, for which the
+// remainder is NaN) take the correctly rounded division, on a branch that is rarely taken.
 __device__ __forceinline__ float div_rn(float x, float d, float rd) {
     const float q0 = __fmul_rn(x, rd);
+    const float rem = __fmaf_rn(-q0, d, x);
+    const float q = __fmaf_rn(rem, rd, q0);
     const float aq = fabsf(q0);
     if ((aq < 2.3509887e-38f && aq != 0.0f) || !(aq <= 3.402823466e38f))  // 2^-125, FLT_MAX
         return __fdiv_rn(x, d);
-    const float rem = __fmaf_rn(-q0, d, x);
-    const float q = __fmaf_rn(rem, rd, q0);
-    return aq == 0.0f ? q0 : q;   // keeps the sign of a zero quotient
+    return aq == 0.0f ? q0 : q;
 }
 
 // 16-byte streaming accesses: the codec touches every dense byte exactly once.
