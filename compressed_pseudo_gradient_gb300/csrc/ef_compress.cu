@@ -40,8 +40,7 @@ constexpr uint32_t kNotFound = 0xffffffffu;
 struct Smem {
     float stage_e[kChunk];          // prefetched error-buffer chunk (bulk copy)
     uint32_t stage_d[kChunk];       // prefetched delta chunk: fp32, or bf16 in the first half
-    uint32_t hist[2048];            // bins of key bits [30:20], then [19:9] if needed
-    uint32_t hist3[512];            // bins of key bits [8:0] (many-candidate path)
+    uint32_t hist[2048];            // histogram bins (one select pass at a time)
     uint32_t sel_bm[kBitmapWords];  // chosen positions (complete once the select is done)
     uint32_t eq_bm[kBitmapWords];   // ties at the final threshold (many-candidate path)
     uint32_t warp_tot[kWarps];
@@ -182,7 +181,7 @@ __device__ __forceinline__ void accumulate_tail(const ChunkRef& r, float beta, i
 // Generic select (any data): radix passes on key bits [30:20], [19:9] and [8:0], each over
 // the keys matching the digits found so far, stopping once the boundary bin is taken whole;
 // ties at the final threshold go to the lowest indices.  Marks the 64 chosen positions in
-// sm.sel_bm.  Entered by all threads with sm.hist3 and sm.sel_bm/eq_bm cleared; clears hist.
+// sm.sel_bm.  Entered by all threads with sm.sel_bm/eq_bm cleared; clears hist itself.
 __device__ __noinline__ void generic_select(Smem& sm, const uint32_t (&key)[kPer], int tid,
                                                int lane, int warp) {
     {
@@ -230,11 +229,14 @@ __device__ __noinline__ void generic_select(Smem& sm, const uint32_t (&key)[kPer
         prefix |= sm.bcast[0] << 9;
         pmask |= 0x7ffu << 9;
         if (sm.bcast[2] != need) {
+            sm.hist[tid] = 0;                 // the second pass's bins have been read
+            sm.hist[tid + kThreads] = 0;
+            __syncthreads();
 #pragma unroll
             for (int i = 0; i < kPer; ++i)
-                if ((key[i] & pmask) == prefix) atomicAdd(&sm.hist3[key[i] & 0x1ffu], 1u);
+                if ((key[i] & pmask) == prefix) atomicAdd(&sm.hist[key[i] & 0x1ffu], 1u);
             __syncthreads();
-            find_digit<512>(sm, sm.hist3, need, tid, lane, warp);
+            find_digit<512>(sm, sm.hist, need, tid, lane, warp);
             __syncthreads();
             need -= sm.bcast[1];
             prefix |= sm.bcast[0];
@@ -339,7 +341,6 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
             const uint4 z = make_uint4(0, 0, 0, 0);
             h4[tid] = z;                      // 2048 words
             h4[tid + kThreads] = z;
-            if (tid < 128) reinterpret_cast<uint4*>(&sm.hist3[0])[tid] = z;   // 512 words
             if (tid < kBitmapWords) sm.sel_bm[tid] = 0;
             else sm.eq_bm[tid - kBitmapWords] = 0;
             if (tid == 0) {
@@ -385,17 +386,20 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
             const uint32_t in_bin = sm.bcast[2];
             if (in_bin == need || in_bin <= 32u) {
                 const bool rank_bin = in_bin != need;
+                // bin D as a key range [k_lo, k_hi): keys at or above k_hi are in, keys in the
+                // range are in when the bin is taken whole, else they are the candidates
+                const uint32_t k_lo = lo_key + (dig << 16);
+                const uint32_t k_hi = k_lo + (1u << 16);
+                const uint32_t k_in = rank_bin ? k_hi : k_lo;
 #pragma unroll
                 for (int v = 0; v < kVec; ++v)
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const uint32_t kk = key[4 * v + u];
-                        if (kk < lo_key) continue;
-                        const uint32_t bin = (kk - lo_key) >> 16;
                         const int j = v * 1024 + 4 * tid + u;
-                        if (bin > dig || (bin == dig && !rank_bin)) {
+                        if (kk >= k_in) {
                             atomicOr(&sm.sel_bm[j >> 5], 1u << (j & 31));
-                        } else if (bin == dig) {
+                        } else if (kk >= k_lo) {
                             const uint32_t slot = atomicAdd(&sm.ncand, 1u);
                             if (slot < 32u) sm.cand[slot] = make_uint2(kk, static_cast<uint32_t>(j));
                         }
