@@ -265,6 +265,141 @@ def gpu_step(buf, ev=None):
     return 2   # kernels launched
 
 
+def host_link_gbs(dev, nbytes: int = 1 << 30) -> float:
+    """Measured host-link bandwidth with both directions busy: a pinned H2D and a D2H copy of
+    nbytes each on two streams at once; (2 nbytes) / time of the slower, best of 3."""
+    import torch
+    h_in = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h_out = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d_out = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    best = 0.0
+    for _ in range(3):
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        with torch.cuda.stream(s1):
+            d_in.copy_(h_in, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h_out.copy_(d_out, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        best = max(best, 2 * nbytes / (time.perf_counter() - t0) / 1e9)
+    return best
+
+
+def run_offload(args, dev):
+    """Compress of the 2^30-value Laplace workload with the error buffer in pinned host
+    memory: the buffer's 8 bytes per value cross the host link, delta stays in HBM."""
+    import torch
+    import compressed_pseudo_gradient_gb300 as spl
+    from compressed_pseudo_gradient_gb300 import synth
+
+    n = args.elements
+    C = (n + CHUNK - 1) // CHUNK
+    delta = synth.laplace(n, 1e-4, synth.generator(1, dev), dev)
+    ef = torch.zeros(n, dtype=torch.float32).pin_memory()
+    payload = torch.empty((C, RECORD), dtype=torch.uint8, device=dev)
+    scales = torch.empty(C, dtype=torch.float32, device=dev)
+    link = host_link_gbs(dev)
+    for _ in range(args.warmup):
+        spl.ef_compress(delta, ef, BETA, payload=payload, scales=scales)
+    torch.cuda.synchronize(dev)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(args.steps):
+        spl.ef_compress(delta, ef, BETA, payload=payload, scales=scales)
+    end.record()
+    torch.cuda.synchronize(dev)
+    secs = start.elapsed_time(end) / 1e3 / args.steps
+    link_bytes = 8 * n
+    line = {"metric": METRIC, "value": round(compress_bytes(n, C) / secs / 1e9, 2),
+            "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * secs, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "offload: compress 2^30 fp32 with the error buffer in pinned "
+                                   "host memory", "n": n,
+                       "host_link": {"bytes_per_step": link_bytes,
+                                     "achieved_gbs": round(link_bytes / secs / 1e9, 1),
+                                     "measured_peak_gbs": round(link, 1),
+                                     "frac": round(link_bytes / secs / 1e9 / link, 4)}},
+            "gpu_launches": args.steps}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_other_workload(args, dev):
+    """Times one round of another workload (same metric: algorithmic bytes per second).
+    heavy_tail_bf16: 2^27 bf16 compress + 8-peer mean; decoder_layer: the 72B-class layer's
+    nine tensors compressed in one multi-tensor call; tiny: 2^20 compress + 4-peer mean."""
+    import torch
+    import compressed_pseudo_gradient_gb300 as spl
+    from compressed_pseudo_gradient_gb300 import synth
+
+    wl = synth.WORKLOADS[args.workload]
+    gen = synth.generator(1, dev)
+    if wl.name == "decoder_layer":
+        deltas = synth.decoder_layer_round(gen, dev)
+        efs = [torch.zeros_like(d) for d in deltas]
+        sizes = [d.numel() for d in deltas]
+        C = sum((k + CHUNK - 1) // CHUNK for k in sizes)
+        payload = torch.empty((C, RECORD), dtype=torch.uint8, device=dev)
+        scales = torch.empty(C, dtype=torch.float32, device=dev)
+        step_bytes = sum(compress_bytes(k, (k + CHUNK - 1) // CHUNK) for k in sizes)
+
+        def step():
+            spl.ef_compress_multi(deltas, efs, wl.beta, payload=payload, scales=scales)
+            return 1
+        n, dtype = sum(sizes), "f32"
+    else:
+        n = wl.n
+        C = (n + CHUNK - 1) // CHUNK
+        delta = synth.delta_round(wl, gen, dev)
+        ef = torch.zeros(n, dtype=torch.float32, device=dev)
+        payload = torch.empty((C, RECORD), dtype=torch.uint8, device=dev)
+        scales = torch.empty(C, dtype=torch.float32, device=dev)
+        pls, scs = [], []
+        tmp = torch.empty(n, dtype=torch.float32, device=dev)
+        for p in range(wl.peers):
+            d = synth.delta_round(wl, synth.generator(2 + p, dev), dev)
+            tmp.zero_()
+            pl, sc = spl.ef_compress(d, tmp, wl.beta)
+            pls.append(pl)
+            scs.append(sc)
+        mean = torch.empty(n, dtype=torch.float32, device=dev)
+        esz = 2 if delta.dtype == torch.bfloat16 else 4
+        step_bytes = (esz + 8) * n + (RECORD + 4) * C + decode_bytes(n, C, wl.peers, theta=False)
+
+        def step():
+            spl.ef_compress(delta, ef, wl.beta, payload=payload, scales=scales)
+            spl.decode_aggregate(pls, scs, n, mean=mean)
+            return 2
+        dtype = "bf16" if esz == 2 else "f32"
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    launches = 0
+    start.record()
+    for _ in range(args.steps):
+        launches += step()
+    end.record()
+    torch.cuda.synchronize(dev)
+    secs = start.elapsed_time(end) / 1e3
+    peak, kind = read_peaks()
+    value = step_bytes * args.steps / secs / 1e9
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * secs / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
+            "config": {"workload": wl.name, "n": n, "step_bytes": step_bytes,
+                       "frac_of_hbm": round(value / peak, 4), "peak_kind": kind},
+            "gpu_launches": launches}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_gpu(args, dev, rank, world):
     import torch
 
@@ -469,6 +604,10 @@ def main(argv=None):
     ap.add_argument("--cpu-chunks", type=int, default=32768)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="receive",
+                    choices=["receive", "heavy_tail_bf16", "decoder_layer", "tiny", "offload"],
+                    help="receive (default): the headline step; the others time one round of "
+                         "another workload on one GPU")
     ap.add_argument("--elements", type=int, default=N_ELEMS,
                     help="pseudo-gradient size; smaller than 2^30 only for profiling captures")
     args = ap.parse_args(argv)
@@ -484,6 +623,12 @@ def main(argv=None):
     rank, world, local = dist_env()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if args.workload != "receive":
+        if world != 1:
+            raise SystemExit("--workload other than receive runs on one GPU")
+        if args.workload == "offload":
+            return run_offload(args, dev)
+        return run_other_workload(args, dev)
     dist_init("nccl")
     r = run_gpu(args, dev, rank, world)
     if rank != 0:

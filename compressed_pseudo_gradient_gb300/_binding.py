@@ -113,18 +113,33 @@ def num_chunks(n: int) -> int:
     return (int(n) + CHUNK - 1) // CHUNK
 
 
+def _ef_tensor(ef: torch.Tensor, dev: torch.device) -> torch.Tensor:
+    """The error buffer: an fp32 CUDA tensor on dev, or a pinned CPU tensor (host-resident)."""
+    if isinstance(ef, torch.Tensor) and not ef.is_cuda:
+        if not ef.is_pinned():
+            raise ValueError("a CPU error buffer must be in pinned memory")
+        if ef.dtype != torch.float32 or not ef.is_contiguous():
+            raise ValueError("the error buffer must be contiguous fp32")
+        return ef
+    _cuda(ef, "ef", (torch.float32,))
+    if ef.device != dev:
+        raise ValueError("delta and ef must be on the same device")
+    return ef
+
+
 def ef_compress(delta: torch.Tensor, ef: torch.Tensor, beta: float, *, payload=None,
                 scales=None, flags=None):
     """One sender round (spl_ef_compress); ``ef`` is updated in place.
 
-    delta: fp32 or bf16 CUDA tensor of n values; ef: fp32 CUDA tensor of n values.
+    delta: fp32 or bf16 CUDA tensor of n values; ef: fp32 tensor of n values, on the same
+    GPU or in pinned host memory (then read and written over the host link).
     Returns (payload uint8 [C, 112], scales fp32 [C]).
     """
     lib = library()
     _cuda(delta, "delta", (torch.float32, torch.bfloat16))
-    _cuda(ef, "ef", (torch.float32,))
-    if ef.numel() != delta.numel() or ef.device != delta.device:
-        raise ValueError("delta and ef must have the same size and device")
+    _ef_tensor(ef, delta.device)
+    if ef.numel() != delta.numel():
+        raise ValueError("delta and ef must have the same size")
     dev = delta.device
     n = delta.numel()
     C = num_chunks(n)
@@ -158,8 +173,8 @@ def ef_compress_multi(deltas, efs, beta: float, *, payload=None, scales=None, fl
     C = 0
     for i, (d, e) in enumerate(zip(deltas, efs)):
         _cuda(d, f"deltas[{i}]", (torch.float32, torch.bfloat16))
-        _cuda(e, f"efs[{i}]", (torch.float32,))
-        if d.dtype != dtype or d.device != dev or e.device != dev or e.numel() != d.numel():
+        _ef_tensor(e, dev)
+        if d.dtype != dtype or d.device != dev or e.numel() != d.numel():
             raise ValueError(f"tensor {i}: dtype/device/size mismatch")
         table[i].delta = d.data_ptr() if d.numel() else None
         table[i].ef = e.data_ptr() if e.numel() else None

@@ -123,23 +123,31 @@ __device__ __forceinline__ ChunkRef locate(const CompressTable& tab, int64_t c) 
 }
 
 // One thread: start the bulk copies of a full chunk's error buffer and delta into the stage.
-template <bool kBf16>
+// With the error buffer in host memory (kEfHost) only delta is staged: the buffer is read and
+// written over the host link with plain 16-byte accesses.
+template <bool kBf16, bool kEfHost>
 __device__ __forceinline__ void prefetch(Smem& sm, const ChunkRef& r) {
     constexpr uint32_t kDeltaBytes = kChunk * (kBf16 ? 2 : 4);
     fence_async_smem();
-    mbar_expect_tx(&sm.bar, kChunk * 4 + kDeltaBytes);
-    bulk_load(sm.stage_e, r.ef, kChunk * 4, &sm.bar);
+    mbar_expect_tx(&sm.bar, (kEfHost ? 0u : kChunk * 4u) + kDeltaBytes);
+    if constexpr (!kEfHost) bulk_load(sm.stage_e, r.ef, kChunk * 4, &sm.bar);
     bulk_load(sm.stage_d, r.delta, kDeltaBytes, &sm.bar);
 }
 
-// a = fmaf(beta, e, delta) for this thread's 16 values, from the stage (full chunks).
-template <bool kBf16>
-__device__ __forceinline__ void accumulate_from_stage(const Smem& sm, float beta, int tid,
-                                                      float (&a)[kPer]) {
+// a = fmaf(beta, e, delta) for this thread's 16 values, from the stage (full chunks); with
+// the error buffer in host memory, e comes straight from there.
+template <bool kBf16, bool kEfHost>
+__device__ __forceinline__ void accumulate_from_stage(const Smem& sm, const ChunkRef& r,
+                                                      float beta, int tid, float (&a)[kPer]) {
+    float4 eh[kVec];
+    if constexpr (kEfHost) {
+#pragma unroll
+        for (int v = 0; v < kVec; ++v) eh[v] = ld_stream_f4(r.ef + v * 1024 + 4 * tid);
+    }
 #pragma unroll
     for (int v = 0; v < kVec; ++v) {
         const int j0 = v * 1024 + 4 * tid;
-        const float4 e4 = *reinterpret_cast<const float4*>(&sm.stage_e[j0]);
+        const float4 e4 = kEfHost ? eh[v] : *reinterpret_cast<const float4*>(&sm.stage_e[j0]);
         float d[4];
         if constexpr (kBf16) {
             const uint2 d2 = *reinterpret_cast<const uint2*>(
@@ -290,7 +298,7 @@ __device__ __noinline__ void generic_select(Smem& sm, const uint32_t (&key)[kPer
 #define SPL_COMPRESS_MIN_BLOCKS 4
 #endif
 
-template <bool kBf16>
+template <bool kBf16, bool kEfHost>
 __global__ void __launch_bounds__(kThreads, SPL_COMPRESS_MIN_BLOCKS)
 k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload,
               float* __restrict__ scales, uint32_t* __restrict__ flags) {
@@ -305,7 +313,7 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
     if (tid == 0) {
         mbar_init(&sm.bar, 1);
         const ChunkRef r0 = locate<kBf16>(tab, blockIdx.x);
-        if (r0.full) prefetch<kBf16>(sm, r0);
+        if (r0.full) prefetch<kBf16, kEfHost>(sm, r0);
     }
     __syncthreads();
 
@@ -322,7 +330,7 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
         if (r.full) {
             timed_out = !mbar_wait(&sm.bar, parity);
             parity ^= 1u;
-            accumulate_from_stage<kBf16>(sm, beta, tid, a);
+            accumulate_from_stage<kBf16, kEfHost>(sm, r, beta, tid, a);
         } else {
             accumulate_tail<kBf16>(r, beta, tid, a);
         }
@@ -357,7 +365,7 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
         // the stage has been read by every thread: start the next chunk's copies
         if (tid == 0 && c + gridDim.x < total) {
             const ChunkRef rn = locate<kBf16>(tab, c + gridDim.x);
-            if (rn.full) prefetch<kBf16>(sm, rn);
+            if (rn.full) prefetch<kBf16, kEfHost>(sm, rn);
         }
         uint32_t mkey = 0;
 #pragma unroll
@@ -505,15 +513,10 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
     }
 }
 
-}  // namespace
-
-cudaError_t launch_ef_compress(const CompressTable& tab, bool bf16, float beta,
-                               uint8_t* payload, float* scales, uint32_t* flags,
-                               cudaStream_t stream) {
-    const int64_t total = tab.chunk_begin[tab.num];
-    if (total == 0) return cudaSuccess;
-    const void* kern = bf16 ? reinterpret_cast<const void*>(&k_ef_compress<true>)
-                            : reinterpret_cast<const void*>(&k_ef_compress<false>);
+template <bool kBf16, bool kEfHost>
+cudaError_t launch_variant(const CompressTable& tab, int64_t total, float beta, uint8_t* payload,
+                           float* scales, uint32_t* flags, cudaStream_t stream) {
+    const void* kern = reinterpret_cast<const void*>(&k_ef_compress<kBf16, kEfHost>);
     const size_t smem = sizeof(Smem);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
@@ -521,11 +524,22 @@ cudaError_t launch_ef_compress(const CompressTable& tab, bool bf16, float beta,
     const int resident = persistent_grid(kern, kThreads, smem);
     if (resident <= 0) return cudaErrorInvalidConfiguration;
     const int grid = static_cast<int>(total < resident ? total : resident);
-    if (bf16)
-        k_ef_compress<true><<<grid, kThreads, smem, stream>>>(tab, beta, payload, scales, flags);
-    else
-        k_ef_compress<false><<<grid, kThreads, smem, stream>>>(tab, beta, payload, scales, flags);
+    k_ef_compress<kBf16, kEfHost><<<grid, kThreads, smem, stream>>>(tab, beta, payload, scales, flags);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_ef_compress(const CompressTable& tab, bool bf16, bool ef_host, float beta,
+                               uint8_t* payload, float* scales, uint32_t* flags,
+                               cudaStream_t stream) {
+    const int64_t total = tab.chunk_begin[tab.num];
+    if (total == 0) return cudaSuccess;
+    if (bf16)
+        return ef_host ? launch_variant<true, true>(tab, total, beta, payload, scales, flags, stream)
+                       : launch_variant<true, false>(tab, total, beta, payload, scales, flags, stream);
+    return ef_host ? launch_variant<false, true>(tab, total, beta, payload, scales, flags, stream)
+                   : launch_variant<false, false>(tab, total, beta, payload, scales, flags, stream);
 }
 
 }  // namespace spl

@@ -28,6 +28,17 @@ bool overlap(const void* p, size_t n, const void* q, size_t m) {
 
 constexpr size_t kMaxChunks = 0x7fffffff;   // chunk indices stay below 2^31
 
+// CUDA memory type of a pointer (cudaMemoryTypeDevice, cudaMemoryTypeHost for pinned host
+// memory, ...), or -1 when the runtime cannot tell (the error is cleared).
+int memory_type(const void* p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    return static_cast<int>(at.type);
+}
+
 }  // namespace
 
 namespace spl {
@@ -124,6 +135,21 @@ spl_status spl_ef_compress_multi(const spl_tensor* tensors, int num_tensors, spl
     const spl_status st = check_outputs(tensors, num_tensors, delta_dtype, payload, scales, d_flags, C);
     if (st != SPL_OK) return st;
     if (C == 0) return SPL_OK;
+    // delta, records and scales are read or written in bulk by the copy engine of each SM:
+    // they must be device memory; error buffers may be device memory or pinned host memory
+    // (one kind for the whole table)
+    int ef_kind = -2;
+    for (int i = 0; i < num_tensors; ++i) {
+        if (tensors[i].n == 0) continue;
+        if (memory_type(tensors[i].delta) != cudaMemoryTypeDevice) return SPL_ERR_INVALID_ARG;
+        const int k = memory_type(tensors[i].ef);
+        if (k != cudaMemoryTypeDevice && k != cudaMemoryTypeHost) return SPL_ERR_INVALID_ARG;
+        if (ef_kind != -2 && k != ef_kind) return SPL_ERR_INVALID_ARG;
+        ef_kind = k;
+    }
+    if (memory_type(payload) != cudaMemoryTypeDevice || memory_type(scales) != cudaMemoryTypeDevice)
+        return SPL_ERR_INVALID_ARG;
+    const bool ef_host = ef_kind == cudaMemoryTypeHost;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     size_t chunk0 = 0;
@@ -143,7 +169,7 @@ spl_status spl_ef_compress_multi(const spl_tensor* tensors, int num_tensors, spl
         tab.chunk_begin[count] = chunks;
         tab.num = count;
         const spl_status ls = cuda_status(spl::launch_ef_compress(
-            tab, delta_dtype == SPL_BF16, beta, payload + chunk0 * SPL_RECORD_BYTES,
+            tab, delta_dtype == SPL_BF16, ef_host, beta, payload + chunk0 * SPL_RECORD_BYTES,
             scales + chunk0, d_flags, s));
         if (ls != SPL_OK) return ls;
         chunk0 += static_cast<size_t>(chunks);
@@ -188,6 +214,14 @@ spl_status spl_decode_aggregate(const uint8_t* const* payloads, const float* con
         tab.payload[p] = payloads[p];
         tab.scale[p] = scales[p];
     }
+    // records and theta arrive by asynchronous copies into shared memory: device memory only
+    for (int p = 0; p < P; ++p)
+        if (memory_type(payloads[p]) != cudaMemoryTypeDevice ||
+            memory_type(scales[p]) != cudaMemoryTypeDevice)
+            return SPL_ERR_INVALID_ARG;
+    if (memory_type(mean_out) != cudaMemoryTypeDevice ||
+        (theta != nullptr && memory_type(theta) != cudaMemoryTypeDevice))
+        return SPL_ERR_INVALID_ARG;
     return cuda_status(spl::launch_decode_aggregate(tab, P, static_cast<int64_t>(n), mean_out,
                                                     theta, lr, d_flags,
                                                     reinterpret_cast<cudaStream_t>(stream)));

@@ -24,7 +24,9 @@ struct DecodeTable {
     const float* scale[kMaxPeers];
 };
 
-cudaError_t launch_ef_compress(const CompressTable& tab, bool bf16, float beta,
+// ef_host: the tensors' error buffers are pinned host memory, read and written over the host
+// link with plain accesses (delta stays in device memory).
+cudaError_t launch_ef_compress(const CompressTable& tab, bool bf16, bool ef_host, float beta,
                                uint8_t* payload, float* scales, uint32_t* flags,
                                cudaStream_t stream);
 

@@ -85,14 +85,19 @@ int spl_last_cuda_error(void);
  *   ef[i]  = a - q[i] at the 64 kept positions (q = decoded value), a elsewhere
  *
  * delta:   device, n values of type delta_dtype (SPL_F32 or SPL_BF16), read only
- * ef:      device, n fp32 values, read and overwritten (the error-feedback buffer)
+ * ef:      n fp32 values, read and overwritten (the error-feedback buffer): device memory, or
+ *          pinned host memory (cudaHostAlloc / cudaHostRegister) so that a buffer too large
+ *          for HBM can stay in host memory; the kernel then reads and writes it over the
+ *          host link with plain accesses, which bounds the call's throughput.  Pageable or
+ *          managed memory is rejected (SPL_ERR_INVALID_ARG).
  * n:       number of values; n = 0 does nothing and accepts NULL pointers
  * beta:    error-feedback decay, finite
  * payload: device, spl_num_chunks(n) * 112 bytes, written
  * scales:  device, spl_num_chunks(n) fp32, written
  * d_flags: device uint32 or NULL; SPL_FLAG_NONFINITE is OR-ed in when some a is not finite
  *          (the records are still written, deterministically)
- * Outputs must not overlap the inputs or each other.
+ * Outputs must not overlap the inputs or each other.  delta, payload and scales must be
+ * device memory (SPL_ERR_INVALID_ARG otherwise).
  */
 spl_status spl_ef_compress(const void* delta, spl_dtype delta_dtype, float* ef, size_t n,
                            float beta, uint8_t* payload, float* scales, uint32_t* d_flags,
@@ -110,7 +115,8 @@ typedef struct {
  * in one pass.  The records and scales of tensor i start at chunk sum_{j<i} ceil(n_j / 4096)
  * of payload / scales.  `tensors` is a HOST array of num_tensors entries (num_tensors >= 1);
  * entries with n = 0 are allowed.  Tables longer than SPL_MAX_TENSORS_PER_LAUNCH are
- * enqueued as several launches on the same stream.
+ * enqueued as several launches on the same stream.  The error buffers of one table are all
+ * device memory or all pinned host memory.
  */
 spl_status spl_ef_compress_multi(const spl_tensor* tensors, int num_tensors,
                                  spl_dtype delta_dtype, float beta, uint8_t* payload,
@@ -135,7 +141,8 @@ spl_status spl_ef_compress_multi(const spl_tensor* tensors, int num_tensors,
  *           indices that are not strictly ascending, or a NaN, infinite or negative scale;
  *           such a record contributes nothing (the mean still divides by P)
  * Entries that decode past n (the pads of a tail chunk) are dropped.  mean_out and theta must
- * not overlap each other or any record or scale array.
+ * not overlap each other or any record or scale array.  All arrays are device memory
+ * (SPL_ERR_INVALID_ARG otherwise).
  */
 spl_status spl_decode_aggregate(const uint8_t* const* payloads, const float* const* scales,
                                 int P, size_t n, float* mean_out, float* theta, float lr,

@@ -436,3 +436,67 @@ def test_side_stream_and_stream_order():
     assert_bit_equal(host(out[0]), host(ref[0]), "side-stream payload")
     assert_bit_equal(host(ef2), host(ef1), "side-stream error buffer")
     assert np.count_nonzero(host(mean)) == 64 * 20
+
+
+# ---------------------------------------------------------------------------------------------
+# Error buffer resident in pinned host memory (read and written over the host link)
+# ---------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_error_buffer_in_pinned_host_memory(dtype):
+    n = 37 * 4096 + 101
+    gen = synth.generator(61, DEV)
+    ef_dev = synth.normal(n, 1e-4, gen, DEV)
+    ef_host = ef_dev.cpu().pin_memory()
+    for r in range(3):
+        delta = synth.laplace(n, 1e-4, gen, DEV).to(dtype)
+        d_h, e_h = host(delta), host(ef_dev)
+        pl_d, sc_d = spl.ef_compress(delta, ef_dev, 0.95)
+        pl_h, sc_h = spl.ef_compress(delta, ef_host, 0.95)
+        torch.cuda.synchronize()
+        assert_bit_equal(host(pl_h), host(pl_d), f"round {r}: payload (host vs device buffer)")
+        assert_bit_equal(host(sc_h), host(sc_d), f"round {r}: scales")
+        assert_bit_equal(ef_host.numpy(), host(ef_dev), f"round {r}: error buffer")
+        o_pl, o_sc, _ = oracle.ef_compress(d_h, e_h, 0.95, bf16=dtype == torch.bfloat16)
+        assert_bit_equal(host(pl_h), o_pl, f"round {r}: payload vs oracle")
+        assert_bit_equal(ef_host.numpy(), e_h, f"round {r}: error buffer vs oracle")
+
+
+def test_multi_tensor_host_error_buffers():
+    gen = synth.generator(62, DEV)
+    sizes = [5000, 4096, 1, 9 * 4096 + 7]
+    deltas = [synth.laplace(k, 1e-4, gen, DEV) for k in sizes]
+    efs_dev = [synth.normal(k, 1e-4, gen, DEV) for k in sizes]
+    efs_host = [e.cpu().pin_memory() for e in efs_dev]
+    pl_d, sc_d = spl.ef_compress_multi(deltas, efs_dev, 1.0)
+    pl_h, sc_h = spl.ef_compress_multi(deltas, efs_host, 1.0)
+    torch.cuda.synchronize()
+    assert_bit_equal(host(pl_h), host(pl_d), "payload")
+    assert_bit_equal(host(sc_h), host(sc_d), "scales")
+    for a, b in zip(efs_host, efs_dev):
+        assert_bit_equal(a.numpy(), host(b), "error buffer")
+    with pytest.raises(spl.SplError):            # one kind of memory per table
+        spl.ef_compress_multi(deltas[:2], [efs_dev[0], efs_host[1]], 1.0)
+
+
+def test_memory_kinds_that_bulk_copies_cannot_read_are_rejected():
+    import ctypes
+    lib = spl.library()
+    n = 8192
+    delta = torch.zeros(n, device=DEV)
+    ef = torch.zeros(n, device=DEV)
+    payload = torch.empty((2, 112), dtype=torch.uint8, device=DEV)
+    scales = torch.empty(2, device=DEV)
+    pageable = np.zeros(n + 8, np.float32)
+    pp = pageable.ctypes.data + (-pageable.ctypes.data) % 16
+    st = torch.cuda.current_stream().cuda_stream
+    assert lib.spl_ef_compress(delta.data_ptr(), 0, pp, n, 1.0, payload.data_ptr(),
+                               scales.data_ptr(), None, st) == 1      # pageable error buffer
+    pinned = torch.zeros(n).pin_memory()
+    assert lib.spl_ef_compress(pinned.data_ptr(), 0, ef.data_ptr(), n, 1.0, payload.data_ptr(),
+                               scales.data_ptr(), None, st) == 1      # delta in host memory
+    mean = torch.empty(n, device=DEV)
+    parr = (ctypes.c_void_p * 1)(payload.data_ptr())
+    sarr = (ctypes.c_void_p * 1)(scales.data_ptr())
+    assert lib.spl_decode_aggregate(parr, sarr, 1, n, mean.data_ptr(), pinned.data_ptr(), 0.7,
+                                    None, st) == 1                    # theta in host memory
+    torch.cuda.synchronize()
