@@ -69,6 +69,8 @@ def _load():
         lib.orc_ef_compress.restype = u32
         lib.orc_decode_aggregate.argtypes = [vp, vp, ctypes.c_int, i64, vp, vp, f32]
         lib.orc_decode_aggregate.restype = u32
+        lib.orc_peer_stats.argtypes = [vp, vp, ctypes.c_int, i64, vp, vp, vp, vp, vp]
+        lib.orc_peer_stats.restype = None
         for name in ("orc_chunk", "orc_topk", "orc_record_bytes"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -173,3 +175,23 @@ def decode_aggregate(payloads, scales, n: int, theta: np.ndarray | None = None,
         tptr = _ptr(theta)
     flags = _load().orc_decode_aggregate(parr, sarr, P, n, _ptr(mean), tptr, np.float32(lr))
     return mean, int(flags)
+
+
+def peer_stats(payloads, scales, n: int) -> dict:
+    """Per-peer statistics of the accepted records (rejected, big, negative, max_scale, sumsq).
+
+    The Sparse Frontier, "What the Blockchain Does (and Doesn't Do)": crafted sparse updates
+    look different from naturally concentrated ones.
+    """
+    P = len(payloads)
+    C = num_chunks(n)
+    pl = [np.ascontiguousarray(p, dtype=np.uint8).reshape(C, RECORD_BYTES) for p in payloads]
+    sc = [np.ascontiguousarray(s, dtype=np.float32).reshape(C) for s in scales]
+    parr = (ctypes.c_void_p * P)(*[_ptr(p) for p in pl])
+    sarr = (ctypes.c_void_p * P)(*[_ptr(s) for s in sc])
+    out = {"rejected": np.zeros(P, np.uint32), "big": np.zeros(P, np.uint32),
+           "negative": np.zeros(P, np.uint32), "max_scale": np.zeros(P, np.float32),
+           "sumsq": np.zeros(P, np.float64)}
+    _load().orc_peer_stats(parr, sarr, P, n, _ptr(out["rejected"]), _ptr(out["big"]),
+                           _ptr(out["negative"]), _ptr(out["max_scale"]), _ptr(out["sumsq"]))
+    return out

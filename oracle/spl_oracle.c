@@ -275,3 +275,44 @@ uint32_t orc_decode_aggregate(const uint8_t* const* payloads, const float* const
     }
     return flags;
 }
+
+/* ------------------------------------------------------------------------------------------
+ * Receiver statistics per peer, for screening updates that look unlike the rest ([SF] "What
+ * the Blockchain Does (and Doesn't Do)": a crafted sparse update looks different from a
+ * naturally concentrated one).  Over the 64 entries of every accepted record of peer p:
+ *   big[p]       entries with the magnitude bit set (|q| = 1.5 s)
+ *   negative[p]  entries with the sign bit set
+ *   max_scale[p] the largest scale among accepted records (0 if none)
+ *   sumsq[p]     the sum of q^2 (fp64; q^2 is exact in fp64), records in chunk order
+ * and rejected[p], the number of rejected records.  Arrays of P, overwritten.
+ * ---------------------------------------------------------------------------------------- */
+void orc_peer_stats(const uint8_t* const* payloads, const float* const* scales, int P, int64_t n,
+                    uint32_t* rejected, uint32_t* big, uint32_t* negative, float* max_scale,
+                    double* sumsq) {
+    int64_t C = orc_num_chunks(n);
+    int p;
+    uint16_t idx[ORC_TOPK];
+    uint8_t code[ORC_TOPK];
+    for (p = 0; p < P; ++p) {
+        int64_t c;
+        rejected[p] = big[p] = negative[p] = 0;
+        max_scale[p] = 0.0f;
+        sumsq[p] = 0.0;
+        for (c = 0; c < C; ++c) {
+            float s = scales[p][c];
+            int r;
+            orc_unpack_record(payloads[p] + c * ORC_RECORD_BYTES, idx, code);
+            if (!orc_record_ok(idx, s)) {
+                rejected[p] += 1;
+                continue;
+            }
+            if (s > max_scale[p]) max_scale[p] = s;
+            for (r = 0; r < ORC_TOPK; ++r) {
+                double q = (double)orc_level(code[r], s);
+                big[p] += code[r] & 1u;
+                negative[p] += (code[r] >> 1) & 1u;
+                sumsq[p] += q * q;
+            }
+        }
+    }
+}

@@ -493,3 +493,48 @@ def test_malformed_records_are_rejected():
         mean, flags = oracle.decode_aggregate([p0, p1], [s0, np.array([bad_s], np.float32)], n)
         assert flags & oracle.FLAG_BAD_RECORD
         assert (mean == good).all()
+
+
+# ---------------------------------------------------------------------------------------------
+# Receiver statistics per peer
+# ---------------------------------------------------------------------------------------------
+def test_peer_stats_by_hand():
+    """A chunk with 64 planted values and scale 1: counts and sum of squares by hand."""
+    pos = np.array([7 + 61 * r for r in range(64)])
+    vals = np.full(64, 0.75, np.float32)            # |v| <= s: code 0, q = 0.5
+    vals[:10] = 1.5                                  # max: code 1, q = 1.5 (s = 1)
+    vals[10:14] = -1.25                              # code 3, q = -1.5
+    vals[14:20] = -0.5                               # code 2, q = -0.5
+    delta = np.zeros(4096, np.float32)
+    delta[pos] = vals
+    pl, sc, _ = oracle.ef_compress(delta, np.zeros(4096, np.float32), 1.0)
+    assert sc[0] == F32(1.0)
+    bad_idx, bad_codes = oracle.unpack(pl)
+    bad_idx[0, [0, 1]] = bad_idx[0, [1, 0]]
+    bad = oracle.pack(bad_idx, bad_codes)
+    st = oracle.peer_stats([pl, bad, pl], [sc, sc, np.array([np.nan], np.float32)], 4096)
+    assert st["rejected"].tolist() == [0, 1, 1]
+    assert st["big"].tolist() == [14, 0, 0]
+    assert st["negative"].tolist() == [10, 0, 0]
+    assert st["max_scale"].tolist() == [1.0, 0.0, 0.0]
+    assert st["sumsq"][0] == 14 * 2.25 + 50 * 0.25
+    assert st["sumsq"][1] == 0.0
+
+
+def test_peer_stats_sum_of_squares_is_the_decode_norm():
+    n = 6 * 4096 + 10
+    payloads, scales = [], []
+    for seed in (70, 71, 72):
+        p, s = _peer(seed, n)
+        payloads.append(p)
+        scales.append(s)
+    st = oracle.peer_stats(payloads, scales, n)
+    for k, (p, s) in enumerate(zip(payloads, scales)):
+        idx, codes = oracle.unpack(p)
+        # every entry of the record, pads included, as placed by a dense decode of a padded tensor
+        q = np.array([oracle.level(int(c), float(s[ch])) for ch in range(idx.shape[0])
+                      for c in codes[ch]], np.float64)
+        assert st["sumsq"][k] == pytest.approx(float(np.sum(q * q)), rel=1e-12)
+        assert st["big"][k] == int((codes & 1).sum())
+        assert st["negative"][k] == int((codes >> 1).sum())
+        assert st["max_scale"][k] == s.max()
