@@ -259,7 +259,7 @@ def gpu_step(buf, ev=None):
         ev[1].record()
         ev[2].record()
     spl.decode_aggregate(buf["peers_pl"], buf["peers_sc"], buf["n"], mean=buf["mean"],
-                         theta=buf["theta"], lr=LR, flags=buf["flags"])
+                         theta=buf["theta"], lr=LR, flags=buf["flags"], stats=buf.get("stats"))
     if ev:
         ev[3].record()
     return 2   # kernels launched
@@ -404,6 +404,9 @@ def run_gpu(args, dev, rank, world):
     import torch
 
     buf = setup_workload(dev, seed_base=rank_seed_base(rank), n=args.elements)
+    if args.decode_stats:
+        import compressed_pseudo_gradient_gb300 as spl
+        buf["stats"] = spl.new_peer_stats(PEERS, dev)
     for _ in range(args.warmup):
         gpu_step(buf)
     torch.cuda.synchronize(dev)
@@ -608,6 +611,8 @@ def main(argv=None):
                     choices=["receive", "heavy_tail_bf16", "decoder_layer", "tiny", "offload"],
                     help="receive (default): the headline step; the others time one round of "
                          "another workload on one GPU")
+    ap.add_argument("--decode-stats", action="store_true",
+                    help="also gather the per-peer statistics in the receive pass")
     ap.add_argument("--elements", type=int, default=N_ELEMS,
                     help="pseudo-gradient size; smaller than 2^30 only for profiling captures")
     args = ap.parse_args(argv)
@@ -662,6 +667,7 @@ def main(argv=None):
                                  "frac_of_hbm": round(dec_gbs / peak, 4),
                                  "Gelem/s": round(n / dec_avg / 1e9, 2)},
             "device_flags": r["flags"],
+            "decode_stats": bool(args.decode_stats),
         },
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",

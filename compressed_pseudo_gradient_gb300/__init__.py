@@ -25,7 +25,9 @@ from ._binding import (  # noqa: F401
     ef_compress_multi,
     library,
     library_path,
+    new_peer_stats,
     num_chunks,
     pack,
+    read_peer_stats,
     unpack,
 )

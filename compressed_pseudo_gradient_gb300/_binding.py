@@ -72,6 +72,9 @@ def library():
         lib.spl_decode_aggregate.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), ci, sz, vp,
                                              vp, cf, vp, vp]
         lib.spl_decode_aggregate.restype = ci
+        lib.spl_decode_aggregate_stats.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), ci,
+                                                   sz, vp, vp, cf, vp, vp, vp]
+        lib.spl_decode_aggregate_stats.restype = ci
         lib.spl_pack.argtypes, lib.spl_pack.restype = [vp, vp, sz, vp, vp], ci
         lib.spl_unpack.argtypes, lib.spl_unpack.restype = [vp, sz, vp, vp, vp], ci
         _lib = lib
@@ -198,10 +201,30 @@ def ef_compress_multi(deltas, efs, beta: float, *, payload=None, scales=None, fl
     return payload, scales
 
 
+PEER_STATS_BYTES = 24
+
+
+def new_peer_stats(P: int, device) -> torch.Tensor:
+    """A zeroed device buffer for P spl_peer_stats entries (uint8 [P, 24])."""
+    return torch.zeros((P, PEER_STATS_BYTES), dtype=torch.uint8, device=device)
+
+
+def read_peer_stats(stats: torch.Tensor) -> dict:
+    """Host copy of a peer-statistics buffer as numpy arrays: rejected, big, negative (uint32),
+    max_scale (float32), sumsq (float64)."""
+    import numpy as np
+    raw = stats.detach().cpu().numpy().reshape(-1, PEER_STATS_BYTES)
+    u = raw[:, :12].copy().view(np.uint32)
+    return {"rejected": u[:, 0].copy(), "big": u[:, 1].copy(), "negative": u[:, 2].copy(),
+            "max_scale": raw[:, 12:16].copy().view(np.float32)[:, 0].copy(),
+            "sumsq": raw[:, 16:24].copy().view(np.float64)[:, 0].copy()}
+
+
 def decode_aggregate(payloads, scales, n: int, *, mean=None, theta=None, lr: float = 0.0,
-                     flags=None):
+                     flags=None, stats=None):
     """Mean of P peers' decoded records, optionally fused with theta -= lr * mean in place
-    (spl_decode_aggregate).  Returns mean (fp32 [n])."""
+    (spl_decode_aggregate).  With ``stats`` (from new_peer_stats, accumulated into), also the
+    per-peer statistics (spl_decode_aggregate_stats).  Returns mean (fp32 [n])."""
     lib = library()
     P = len(payloads)
     if P != len(scales) or P < 1:
@@ -227,9 +250,17 @@ def decode_aggregate(payloads, scales, n: int, *, mean=None, theta=None, lr: flo
     parr = (ctypes.c_void_p * P)(*[p.data_ptr() for p in payloads])
     sarr = (ctypes.c_void_p * P)(*[s.data_ptr() for s in scales])
     with torch.cuda.device(dev):
-        st = lib.spl_decode_aggregate(parr, sarr, P, int(n), mean.data_ptr(), tptr, float(lr),
-                                      _flags_ptr(flags, dev), _stream(dev))
-    _check("spl_decode_aggregate", st)
+        if stats is None:
+            st = lib.spl_decode_aggregate(parr, sarr, P, int(n), mean.data_ptr(), tptr, float(lr),
+                                          _flags_ptr(flags, dev), _stream(dev))
+        else:
+            _cuda(stats, "stats", (torch.uint8,))
+            if stats.numel() < P * PEER_STATS_BYTES or stats.device != dev:
+                raise ValueError("stats must hold P x 24 bytes on the inputs' device")
+            st = lib.spl_decode_aggregate_stats(parr, sarr, P, int(n), mean.data_ptr(), tptr,
+                                                float(lr), stats.data_ptr(),
+                                                _flags_ptr(flags, dev), _stream(dev))
+    _check("spl_decode_aggregate_stats" if stats is not None else "spl_decode_aggregate", st)
     return mean
 
 

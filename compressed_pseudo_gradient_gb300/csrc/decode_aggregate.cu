@@ -16,7 +16,8 @@
 //     registers (lane l of warp w holds peer 8 l + w's);
 //   - each warp unpacks whole records (one peer at a time): the 64 14-bit fields, a check that
 //     the indices ascend strictly and the scale is finite and non-negative, and the decoded
-//     value of every entry, stored as (position, value) pairs;
+//     value of every entry, stored as (position, value) pairs (with statistics, the warp also
+//     counts the record's magnitude and sign bits and keeps them beside its scale);
 //   - then one warp adds the peers into a 16 KB shared accumulator in order p = 0..P-1, two
 //     entries per lane (distinct positions within a valid record), so every position is summed
 //     in fp32 in peer order from +0.0, as a plain sequential loop over peers would, with no
@@ -48,10 +49,12 @@ __host__ __device__ constexpr size_t align16(size_t x) { return (x + 15) & ~size
 
 // Dynamic shared memory for P peers (offsets 16-byte aligned), G = min(P, 64):
 //   bar[2] | theta stage [S][4096] f32 | record stage [S][P][112] (+16) | acc [4096] f32 |
-//   entries [G][64] (position, value) | validity [G] u32
+//   entries [G][64] (position, value) | validity [G] u32 |
+//   with statistics only: (scale, magnitude | sign << 8 bit counts) [G] | per-peer totals of this CTA: sum of squares and its
+//   Kahan compensation [2][P] f32 | rejected, big, negative [3][P] u32 | max scale [P] f32
 struct Layout {
-    size_t bar, theta, rec, acc, ent, ok, total;
-    __host__ __device__ explicit Layout(int P) {
+    size_t bar, theta, rec, acc, ent, ok, sgrp, st_sq, st_cnt, st_max, total;
+    __host__ __device__ Layout(int P, bool stats) {
         const size_t G = static_cast<size_t>(P < kGroup ? P : kGroup);
         bar = 0;
         theta = 16;
@@ -59,7 +62,11 @@ struct Layout {
         acc = rec + align16(kStages * static_cast<size_t>(P) * kRecordBytes) + 16;
         ent = acc + kChunk * 4;
         ok = ent + G * kTopK * 8;
-        total = ok + align16(G * 4);
+        sgrp = ok + align16(G * 4);
+        st_sq = sgrp + align16(G * 8);
+        st_cnt = st_sq + align16(static_cast<size_t>(P) * 8);
+        st_max = st_cnt + align16(3 * static_cast<size_t>(P) * 4);
+        total = stats ? st_max + align16(static_cast<size_t>(P) * 4) : sgrp;
     }
 };
 
@@ -90,17 +97,24 @@ __device__ __forceinline__ void prefetch(const DecodeTable& tab, int P, int64_t 
     }
 }
 
+template <bool kStats>
 __global__ void __launch_bounds__(kThreads, 4)
 k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __restrict__ mean,
-                   float* __restrict__ theta, float neg_lr, uint32_t* __restrict__ flags) {
+                   float* __restrict__ theta, float neg_lr, PeerStats* __restrict__ stats,
+                   uint32_t* __restrict__ flags) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    const Layout L(P);
+    const Layout L(P, kStats);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + L.bar);
     float* st_theta = reinterpret_cast<float*>(smem_raw + L.theta);
     uint8_t* st_rec = smem_raw + L.rec;
     float* acc = reinterpret_cast<float*>(smem_raw + L.acc);
     uint2* ent = reinterpret_cast<uint2*>(smem_raw + L.ent);
     uint32_t* okp = reinterpret_cast<uint32_t*>(smem_raw + L.ok);
+    uint2* sgrp = reinterpret_cast<uint2*>(smem_raw + L.sgrp);
+    float* st_sum = reinterpret_cast<float*>(smem_raw + L.st_sq);        // [P]
+    float* st_comp = st_sum + P;                                           // [P]
+    uint32_t* st_cnt = reinterpret_cast<uint32_t*>(smem_raw + L.st_cnt);   // [3][P]
+    float* st_max = reinterpret_cast<float*>(smem_raw + L.st_max);
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -115,6 +129,13 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
 #pragma unroll
     for (int v = 0; v < kVec; ++v)
         *reinterpret_cast<float4*>(&acc[slice0 + 128 * v + 4 * lane]) = make_float4(0.f, 0.f, 0.f, 0.f);
+    if constexpr (kStats) {
+        for (int p = tid; p < P; p += kThreads) {
+            st_sum[p] = st_comp[p] = 0.0f;
+            st_cnt[p] = st_cnt[P + p] = st_cnt[2 * P + p] = 0u;
+            st_max[p] = 0.0f;
+        }
+    }
     if (tid == 0) {
         const uint32_t arrivals = static_cast<uint32_t>(min(P * kRecordVec, kThreads) + 1);
         for (int st = 0; st < kStages; ++st) mbar_init(&bars[st], arrivals);
@@ -171,6 +192,13 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
                     uint2* eg = ent + g * kTopK;
                     eg[lane] = make_uint2(i0, __float_as_uint(level_value(f0 & 3u, s)));
                     eg[lane + 32] = make_uint2(i1, __float_as_uint(level_value(f1 & 3u, s)));
+                    if (kStats) {
+                        const uint32_t nbig = __popc(__ballot_sync(0xffffffffu, f0 & 1u)) +
+                                              __popc(__ballot_sync(0xffffffffu, f1 & 1u));
+                        const uint32_t nneg = __popc(__ballot_sync(0xffffffffu, f0 & 2u)) +
+                                              __popc(__ballot_sync(0xffffffffu, f1 & 2u));
+                        if (lane == 0) sgrp[g] = make_uint2(__float_as_uint(s), nbig | nneg << 8);
+                    }
                 } else {
                     bad = true;
                 }
@@ -190,6 +218,35 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
                 if (my_peer < P && c + G < C) sc_next = __ldcs(tab.scale[my_peer] + c + G);
             } else {
                 __syncthreads();
+            }
+            // ---- the other warps, meanwhile: per-peer statistics, one record per thread ----
+            // (a group holds at most 64 peers; peer p is always thread 32 + p mod 64)
+            if (kStats && tid >= 32 && tid - 32 < gn) {
+                const int g = tid - 32;
+                const int p = g0 + g;
+                if (okp[g] == 0u) {
+                    st_cnt[p] += 1u;
+                } else {
+                    const uint2 sg = sgrp[g];
+                    const float s = __uint_as_float(sg.x);
+                    const uint32_t nbig = sg.y & 0xffu;
+                    const uint32_t nneg = sg.y >> 8;
+                    const float lo = level_value(0u, s);
+                    const float hi = level_value(1u, s);
+                    // every entry decodes to +-RN(0.5 s) or +-RN(1.5 s): the record's sum of
+                    // squares from the two counts, in fp32 (fp64 is scarce on this GPU), added
+                    // to the CTA's total with Kahan compensation
+                    const float t = __fmaf_rn(__fmul_rn(hi, hi), static_cast<float>(nbig),
+                                              __fmul_rn(__fmul_rn(lo, lo),
+                                                        static_cast<float>(kTopK - nbig)));
+                    const float y = __fsub_rn(t, st_comp[p]);
+                    const float z = __fadd_rn(st_sum[p], y);
+                    st_comp[p] = __fsub_rn(__fsub_rn(z, st_sum[p]), y);
+                    st_sum[p] = z;
+                    st_cnt[P + p] += nbig;
+                    st_cnt[2 * P + p] += nneg;
+                    st_max[p] = fmaxf(st_max[p], s);
+                }
             }
             // ---- one warp: add the peers in order, two entries per lane -------------------
             if (warp == 0) {
@@ -259,6 +316,19 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
             if (c + k * G < C) mbar_wait(&bars[it2 % kStages], static_cast<uint32_t>(it2 / kStages) & 1u);
         }
     }
+    if constexpr (kStats) {
+        __syncthreads();
+        for (int p = tid; p < P; p += kThreads) {
+            PeerStats* o = stats + p;
+            if (st_cnt[p]) atomicAdd(&o->rejected, st_cnt[p]);
+            if (st_cnt[P + p]) atomicAdd(&o->big, st_cnt[P + p]);
+            if (st_cnt[2 * P + p]) atomicAdd(&o->negative, st_cnt[2 * P + p]);
+            if (st_max[p] > 0.0f)   // non-negative floats order like their bit patterns
+                atomicMax(reinterpret_cast<unsigned int*>(&o->max_scale), __float_as_uint(st_max[p]));
+            if (st_sum[p] != 0.0f)
+                atomicAdd(&o->sumsq, static_cast<double>(st_sum[p]) - static_cast<double>(st_comp[p]));
+        }
+    }
     if (flags != nullptr) {
         if (bad && lane == 0) atomicOr(flags, kFlagBadRecord);
         if (aborted && tid == 0) atomicOr(flags, kFlagTimeout);
@@ -268,12 +338,13 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
 }  // namespace
 
 cudaError_t launch_decode_aggregate(const DecodeTable& tab, int P, int64_t n, float* mean,
-                                    float* theta, float lr, uint32_t* flags,
+                                    float* theta, float lr, PeerStats* stats, uint32_t* flags,
                                     cudaStream_t stream) {
     const int64_t C = (n + kChunk - 1) / kChunk;
     if (C == 0) return cudaSuccess;
-    const size_t smem = Layout(P).total;
-    const void* kern = reinterpret_cast<const void*>(&k_decode_aggregate);
+    const size_t smem = Layout(P, stats != nullptr).total;
+    const void* kern = stats != nullptr ? reinterpret_cast<const void*>(&k_decode_aggregate<true>)
+                                        : reinterpret_cast<const void*>(&k_decode_aggregate<false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -281,7 +352,12 @@ cudaError_t launch_decode_aggregate(const DecodeTable& tab, int P, int64_t n, fl
     if (resident <= 0) return cudaErrorInvalidConfiguration;
     const int grid = static_cast<int>(C < resident ? C : resident);
     const float rp = 1.0f / static_cast<float>(P);   // correctly rounded on the host
-    k_decode_aggregate<<<grid, kThreads, smem, stream>>>(tab, P, rp, n, mean, theta, -lr, flags);
+    if (stats != nullptr)
+        k_decode_aggregate<true><<<grid, kThreads, smem, stream>>>(tab, P, rp, n, mean, theta, -lr,
+                                                                   stats, flags);
+    else
+        k_decode_aggregate<false><<<grid, kThreads, smem, stream>>>(tab, P, rp, n, mean, theta, -lr,
+                                                                    stats, flags);
     return cudaGetLastError();
 }
 

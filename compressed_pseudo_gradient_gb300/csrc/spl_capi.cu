@@ -135,9 +135,9 @@ spl_status spl_ef_compress_multi(const spl_tensor* tensors, int num_tensors, spl
     const spl_status st = check_outputs(tensors, num_tensors, delta_dtype, payload, scales, d_flags, C);
     if (st != SPL_OK) return st;
     if (C == 0) return SPL_OK;
-    // delta, records and scales are read or written in bulk by the copy engine of each SM:
-    // they must be device memory; error buffers may be device memory or pinned host memory
-    // (one kind for the whole table)
+    // delta (and a device-resident error buffer) arrive by bulk copies (TMA) into shared
+    // memory: device memory; an error buffer may instead be pinned host memory, then read and
+    // written with plain accesses (one kind for the whole table)
     int ef_kind = -2;
     for (int i = 0; i < num_tensors; ++i) {
         if (tensors[i].n == 0) continue;
@@ -147,8 +147,6 @@ spl_status spl_ef_compress_multi(const spl_tensor* tensors, int num_tensors, spl
         if (ef_kind != -2 && k != ef_kind) return SPL_ERR_INVALID_ARG;
         ef_kind = k;
     }
-    if (memory_type(payload) != cudaMemoryTypeDevice || memory_type(scales) != cudaMemoryTypeDevice)
-        return SPL_ERR_INVALID_ARG;
     const bool ef_host = ef_kind == cudaMemoryTypeHost;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -188,9 +186,11 @@ spl_status spl_ef_compress(const void* delta, spl_dtype delta_dtype, float* ef, 
     return spl_ef_compress_multi(&t, 1, delta_dtype, beta, payload, scales, d_flags, stream);
 }
 
-spl_status spl_decode_aggregate(const uint8_t* const* payloads, const float* const* scales, int P,
-                                size_t n, float* mean_out, float* theta, float lr,
-                                uint32_t* d_flags, spl_stream_t stream) {
+static_assert(sizeof(spl_peer_stats) == sizeof(spl::PeerStats), "spl_peer_stats layout");
+
+static spl_status decode_impl(const uint8_t* const* payloads, const float* const* scales, int P,
+                              size_t n, float* mean_out, float* theta, float lr,
+                              spl_peer_stats* d_stats, uint32_t* d_flags, spl_stream_t stream) {
     if (P < 1 || P > SPL_MAX_PEERS) return SPL_ERR_INVALID_ARG;
     if (theta != nullptr && !std::isfinite(lr)) return SPL_ERR_INVALID_ARG;
     if (n == 0) return SPL_OK;
@@ -214,17 +214,32 @@ spl_status spl_decode_aggregate(const uint8_t* const* payloads, const float* con
         tab.payload[p] = payloads[p];
         tab.scale[p] = scales[p];
     }
-    // records and theta arrive by asynchronous copies into shared memory: device memory only
-    for (int p = 0; p < P; ++p)
-        if (memory_type(payloads[p]) != cudaMemoryTypeDevice ||
-            memory_type(scales[p]) != cudaMemoryTypeDevice)
-            return SPL_ERR_INVALID_ARG;
-    if (memory_type(mean_out) != cudaMemoryTypeDevice ||
-        (theta != nullptr && memory_type(theta) != cudaMemoryTypeDevice))
+    // theta arrives by bulk copies (TMA) into shared memory: device memory only (records and
+    // scales are read with plain and 16-byte asynchronous loads, the outputs written with
+    // plain stores; those take any memory the device can address)
+    if (theta != nullptr && memory_type(theta) != cudaMemoryTypeDevice) return SPL_ERR_INVALID_ARG;
+    return cuda_status(spl::launch_decode_aggregate(
+        tab, P, static_cast<int64_t>(n), mean_out, theta, lr,
+        reinterpret_cast<spl::PeerStats*>(d_stats), d_flags, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+spl_status spl_decode_aggregate(const uint8_t* const* payloads, const float* const* scales, int P,
+                                size_t n, float* mean_out, float* theta, float lr,
+                                uint32_t* d_flags, spl_stream_t stream) {
+    return decode_impl(payloads, scales, P, n, mean_out, theta, lr, nullptr, d_flags, stream);
+}
+
+spl_status spl_decode_aggregate_stats(const uint8_t* const* payloads, const float* const* scales,
+                                      int P, size_t n, float* mean_out, float* theta, float lr,
+                                      spl_peer_stats* d_stats, uint32_t* d_flags,
+                                      spl_stream_t stream) {
+    if (P < 1 || P > SPL_MAX_PEERS || d_stats == nullptr) return SPL_ERR_INVALID_ARG;
+    if (!aligned(d_stats, 8)) return SPL_ERR_ALIGNMENT;
+    const size_t sb = static_cast<size_t>(P) * sizeof(spl_peer_stats);
+    if (overlap(d_stats, sb, mean_out, n * 4) || overlap(d_stats, sb, theta, n * 4) ||
+        overlap(d_stats, sb, d_flags, 4))
         return SPL_ERR_INVALID_ARG;
-    return cuda_status(spl::launch_decode_aggregate(tab, P, static_cast<int64_t>(n), mean_out,
-                                                    theta, lr, d_flags,
-                                                    reinterpret_cast<cudaStream_t>(stream)));
+    return decode_impl(payloads, scales, P, n, mean_out, theta, lr, d_stats, d_flags, stream);
 }
 
 spl_status spl_pack(const uint16_t* idx, const uint8_t* codes, size_t num_chunks, uint8_t* payload,

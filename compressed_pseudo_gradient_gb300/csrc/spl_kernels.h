@@ -30,8 +30,17 @@ cudaError_t launch_ef_compress(const CompressTable& tab, bool bf16, bool ef_host
                                uint8_t* payload, float* scales, uint32_t* flags,
                                cudaStream_t stream);
 
+// Per-peer statistics (same layout as spl_peer_stats in spl.h), accumulated by the kernel.
+struct PeerStats {
+    uint32_t rejected;
+    uint32_t big;
+    uint32_t negative;
+    float max_scale;
+    double sumsq;
+};
+
 cudaError_t launch_decode_aggregate(const DecodeTable& tab, int P, int64_t n, float* mean,
-                                    float* theta, float lr, uint32_t* flags,
+                                    float* theta, float lr, PeerStats* stats, uint32_t* flags,
                                     cudaStream_t stream);
 
 cudaError_t launch_pack(const uint16_t* idx, const uint8_t* codes, int64_t C,

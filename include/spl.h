@@ -96,8 +96,8 @@ int spl_last_cuda_error(void);
  * scales:  device, spl_num_chunks(n) fp32, written
  * d_flags: device uint32 or NULL; SPL_FLAG_NONFINITE is OR-ed in when some a is not finite
  *          (the records are still written, deterministically)
- * Outputs must not overlap the inputs or each other.  delta, payload and scales must be
- * device memory (SPL_ERR_INVALID_ARG otherwise).
+ * Outputs must not overlap the inputs or each other.  delta must be device memory
+ * (SPL_ERR_INVALID_ARG otherwise); payload, scales and d_flags any memory the device can write.
  */
 spl_status spl_ef_compress(const void* delta, spl_dtype delta_dtype, float* ef, size_t n,
                            float beta, uint8_t* payload, float* scales, uint32_t* d_flags,
@@ -141,12 +141,37 @@ spl_status spl_ef_compress_multi(const spl_tensor* tensors, int num_tensors,
  *           indices that are not strictly ascending, or a NaN, infinite or negative scale;
  *           such a record contributes nothing (the mean still divides by P)
  * Entries that decode past n (the pads of a tail chunk) are dropped.  mean_out and theta must
- * not overlap each other or any record or scale array.  All arrays are device memory
- * (SPL_ERR_INVALID_ARG otherwise).
+ * not overlap each other or any record or scale array.  theta must be device memory
+ * (SPL_ERR_INVALID_ARG otherwise); the other arrays any memory the device can address.
  */
 spl_status spl_decode_aggregate(const uint8_t* const* payloads, const float* const* scales,
                                 int P, size_t n, float* mean_out, float* theta, float lr,
                                 uint32_t* d_flags, spl_stream_t stream);
+
+/*
+ * Per-peer statistics of the records a receiver accepted, for screening updates that look
+ * unlike the rest (The Sparse Frontier, "What the Blockchain Does (and Doesn't Do)": a crafted
+ * sparse update looks different from a naturally concentrated one).  Counted over the 64
+ * entries of every accepted record (a tail chunk's pads included).
+ */
+typedef struct {
+    uint32_t rejected;  /* records rejected (indices not strictly ascending, or a bad scale) */
+    uint32_t big;       /* entries with the magnitude bit set (|q| = 1.5 s) */
+    uint32_t negative;  /* entries with the sign bit set */
+    float max_scale;    /* largest scale among accepted records (0 if none) */
+    double sumsq;       /* sum of q^2 over the entries (relative error ~1e-7: fp32 per record,
+                           compensated sums; records summed in no fixed order) */
+} spl_peer_stats;       /* 24 bytes */
+
+/*
+ * spl_decode_aggregate, and in the same pass the statistics above for each peer.
+ * d_stats: device array of P entries (8-byte aligned), ACCUMULATED into: zero it before the
+ * first call (counts add up, max_scale takes the maximum, sumsq adds up across calls).
+ */
+spl_status spl_decode_aggregate_stats(const uint8_t* const* payloads, const float* const* scales,
+                                      int P, size_t n, float* mean_out, float* theta, float lr,
+                                      spl_peer_stats* d_stats, uint32_t* d_flags,
+                                      spl_stream_t stream);
 
 /*
  * Record layout helpers (per-chunk size equation): idx[C][64] and codes[C][64] to and from

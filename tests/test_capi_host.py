@@ -28,8 +28,9 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for fn in ("spl_ef_compress", "spl_ef_compress_multi", "spl_decode_aggregate", "spl_pack",
-               "spl_unpack", "spl_num_chunks", "spl_status_string", "spl_last_cuda_error"):
+    for fn in ("spl_ef_compress", "spl_ef_compress_multi", "spl_decode_aggregate",
+               "spl_decode_aggregate_stats", "spl_pack", "spl_unpack", "spl_num_chunks",
+               "spl_status_string", "spl_last_cuda_error"):
         assert fn in names
 
 
@@ -118,6 +119,18 @@ def test_decode_argument_errors(lib):
     assert f(pl_null, sc, P, n, Cp, None, 0.0, None, None) == INVALID
     pl_alias = (ctypes.c_void_p * P)(A, Cp + 4096)                          # record in mean
     assert f(pl_alias, sc, P, n, Cp, None, 0.0, None, None) == INVALID
+
+
+def test_decode_stats_argument_errors(lib):
+    f = lib.spl_decode_aggregate_stats
+    P = 2
+    pl = (ctypes.c_void_p * P)(A, A + 0x100000)
+    sc = (ctypes.c_void_p * P)(B, B + 0x100000)
+    n = 8192
+    assert f(pl, sc, P, n, Cp, None, 0.0, None, None, None) == INVALID      # NULL stats
+    assert f(pl, sc, P, n, Cp, None, 0.0, D + 4, None, None) == ALIGN       # stats 4-B
+    assert f(pl, sc, P, n, Cp, None, 0.0, Cp + 64, None, None) == INVALID   # stats in mean
+    assert f(pl, sc, 0, n, Cp, None, 0.0, D, None, None) == INVALID         # P = 0
 
 
 def test_pack_unpack_argument_errors(lib):

@@ -500,3 +500,56 @@ def test_memory_kinds_that_bulk_copies_cannot_read_are_rejected():
     assert lib.spl_decode_aggregate(parr, sarr, 1, n, mean.data_ptr(), pinned.data_ptr(), 0.7,
                                     None, st) == 1                    # theta in host memory
     torch.cuda.synchronize()
+
+
+# ---------------------------------------------------------------------------------------------
+# Per-peer statistics fused into the receive pass
+# ---------------------------------------------------------------------------------------------
+def test_peer_stats_match_oracle():
+    n = 1024 * 4096 + 333
+    P = 24
+    gen = synth.generator(81, DEV)
+    pls, scs = [], []
+    for p in range(P):
+        d = synth.laplace(n, 1e-4, synth.generator(100 + p, DEV), DEV)
+        pl, sc = gpu_round(d, torch.zeros(n, device=DEV), 0.95)
+        pls.append(pl)
+        scs.append(sc)
+    torch.cuda.synchronize()
+    h_pl = [host(p).copy() for p in pls]
+    h_sc = [host(s).copy() for s in scs]
+    idx, codes = oracle.unpack(h_pl[3])
+    idx[[5, 700], 9], idx[[5, 700], 10] = idx[[5, 700], 10], idx[[5, 700], 9]
+    h_pl[3] = oracle.pack(idx, codes)                       # two malformed records of peer 3
+    h_sc[7][11] = np.nan                                     # one bad scale of peer 7
+    for q, c, z in ((5, 20, 0.0), (6, 30, -0.0)):            # zero scales, codes all 3: both
+        idx, codes = oracle.unpack(h_pl[q])                  # levels decode to -0.0, yet the
+        codes[c, :] = 3                                      # code bits still count
+        h_pl[q] = oracle.pack(idx, codes)
+        h_sc[q][c] = z
+    pls = [torch.from_numpy(p).to(DEV) for p in h_pl]
+    scs = [torch.from_numpy(s).to(DEV) for s in h_sc]
+    theta = synth.theta(n, gen, DEV)
+    theta2 = theta.clone()
+    stats = spl.new_peer_stats(P, DEV)
+    mean = spl.decode_aggregate(pls, scs, n, theta=theta, lr=0.7, stats=stats)
+    mean_plain = spl.decode_aggregate(pls, scs, n, theta=theta2, lr=0.7)
+    torch.cuda.synchronize()
+    assert_bit_equal(host(mean), host(mean_plain), "mean with and without statistics")
+    assert_bit_equal(host(theta), host(theta2), "theta with and without statistics")
+    got = spl.read_peer_stats(stats)
+    ref = oracle.peer_stats(h_pl, h_sc, n)
+    for key in ("rejected", "big", "negative"):
+        assert np.array_equal(got[key], ref[key]), key
+    assert_bit_equal(got["max_scale"], ref["max_scale"], "max_scale")
+    assert np.allclose(got["sumsq"], ref["sumsq"], rtol=1e-6, atol=0)   # fp32 per record
+    assert ref["rejected"][3] == 2 and ref["rejected"][7] == 1
+    assert ref["rejected"][5] == 0 and ref["rejected"][6] == 0
+    # accumulated across calls
+    spl.decode_aggregate(pls, scs, n, stats=stats)
+    torch.cuda.synchronize()
+    again = spl.read_peer_stats(stats)
+    for key in ("rejected", "big", "negative"):
+        assert np.array_equal(again[key], 2 * ref[key]), key
+    assert_bit_equal(again["max_scale"], ref["max_scale"], "max_scale after two calls")
+    assert np.allclose(again["sumsq"], 2 * ref["sumsq"], rtol=1e-6, atol=0)
