@@ -36,6 +36,9 @@ TOPK = 64
 RECORD_BYTES = 112
 FLAG_NONFINITE = 1
 FLAG_BAD_RECORD = 2
+SCALE_MAX = 0        # s = max |a| / 1.5 (the default)
+SCALE_MEAN_ABS = 1   # s = pairwise sum of the chosen |a| / k (variant)
+DEFAULT_CODEC = (CHUNK, TOPK, SCALE_MAX)
 
 
 def build(force: bool = False) -> str:
@@ -71,6 +74,18 @@ def _load():
         lib.orc_decode_aggregate.restype = u32
         lib.orc_peer_stats.argtypes = [vp, vp, ctypes.c_int, i64, vp, vp, vp, vp, vp]
         lib.orc_peer_stats.restype = None
+        ci = ctypes.c_int
+        lib.orc_codec_record_bytes.argtypes, lib.orc_codec_record_bytes.restype = [ci, ci], ci
+        lib.orc_num_chunks_codec.argtypes, lib.orc_num_chunks_codec.restype = [ci, i64], i64
+        lib.orc_pairwise_sum.argtypes, lib.orc_pairwise_sum.restype = [vp, ci], f32
+        lib.orc_pack_codec.argtypes, lib.orc_pack_codec.restype = [ci, ci, vp, vp, i64, vp], ci
+        lib.orc_unpack_codec.argtypes, lib.orc_unpack_codec.restype = [ci, ci, vp, i64, vp, vp], ci
+        lib.orc_ef_compress_codec.argtypes = [ci, ci, ci, vp, ci, vp, i64, f32, vp, vp]
+        lib.orc_ef_compress_codec.restype = u32
+        lib.orc_decode_aggregate_codec.argtypes = [ci, ci, vp, vp, ci, i64, vp, vp, f32]
+        lib.orc_decode_aggregate_codec.restype = u32
+        lib.orc_peer_stats_codec.argtypes = [ci, ci, vp, vp, ci, i64, vp, vp, vp, vp, vp]
+        lib.orc_peer_stats_codec.restype = ci
         for name in ("orc_chunk", "orc_topk", "orc_record_bytes"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -89,8 +104,32 @@ def constants() -> dict:
             "record_bytes": lib.orc_record_bytes()}
 
 
-def num_chunks(n: int) -> int:
-    return int(_load().orc_num_chunks(n))
+def _codec(codec) -> tuple[int, int, int]:
+    """(L, k, rule) of a codec argument (None = the default 4096 / 64 / max-abs codec)."""
+    if codec is None:
+        return DEFAULT_CODEC
+    L, k, rule = (int(x) for x in codec)
+    if _load().orc_codec_record_bytes(L, k) < 0 or rule not in (SCALE_MAX, SCALE_MEAN_ABS):
+        raise ValueError(f"not a codec: {codec}")
+    return L, k, rule
+
+
+def record_bytes(codec=None) -> int:
+    """Bytes of one record: ceil(k * (2 + ceil(log2 L)) / 8)."""
+    L, k, _ = _codec(codec)
+    return int(_load().orc_codec_record_bytes(L, k))
+
+
+def num_chunks(n: int, codec=None) -> int:
+    L, _, _ = _codec(codec)
+    return int(_load().orc_num_chunks_codec(L, n))
+
+
+def pairwise_sum(x: np.ndarray) -> np.float32:
+    """Pairwise (recursive halving) fp32 sum, the mean-abs scale rule's summation."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    assert x.size >= 1
+    return np.float32(_load().orc_pairwise_sum(_ptr(x), x.size))
 
 
 def topk_select(a: np.ndarray, k: int) -> tuple[np.ndarray, int]:
@@ -116,82 +155,92 @@ def level(c: int, s: float) -> np.float32:
     return np.float32(_load().orc_level(c, s))
 
 
-def pack(idx: np.ndarray, codes: np.ndarray) -> np.ndarray:
-    """(idx[C,64] u16, codes[C,64] u8) -> payload[C,112] u8 (bit-at-a-time writer)."""
-    idx = np.ascontiguousarray(idx, dtype=np.uint16).reshape(-1, TOPK)
-    codes = np.ascontiguousarray(codes, dtype=np.uint8).reshape(-1, TOPK)
+def pack(idx: np.ndarray, codes: np.ndarray, codec=None) -> np.ndarray:
+    """(idx[C,k] u16, codes[C,k] u8) -> payload[C,record_bytes] u8 (bit-at-a-time writer)."""
+    L, k, _ = _codec(codec)
+    idx = np.ascontiguousarray(idx, dtype=np.uint16).reshape(-1, k)
+    codes = np.ascontiguousarray(codes, dtype=np.uint8).reshape(-1, k)
     C = idx.shape[0]
-    out = np.zeros((C, RECORD_BYTES), dtype=np.uint8)
-    _load().orc_pack(_ptr(idx), _ptr(codes), C, _ptr(out))
+    out = np.zeros((C, record_bytes(codec)), dtype=np.uint8)
+    assert _load().orc_pack_codec(L, k, _ptr(idx), _ptr(codes), C, _ptr(out))
     return out
 
 
-def unpack(payload: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
-    payload = np.ascontiguousarray(payload, dtype=np.uint8).reshape(-1, RECORD_BYTES)
+def unpack(payload: np.ndarray, codec=None) -> tuple[np.ndarray, np.ndarray]:
+    L, k, _ = _codec(codec)
+    payload = np.ascontiguousarray(payload, dtype=np.uint8).reshape(-1, record_bytes(codec))
     C = payload.shape[0]
-    idx = np.zeros((C, TOPK), dtype=np.uint16)
-    codes = np.zeros((C, TOPK), dtype=np.uint8)
-    _load().orc_unpack(_ptr(payload), C, _ptr(idx), _ptr(codes))
+    idx = np.zeros((C, k), dtype=np.uint16)
+    codes = np.zeros((C, k), dtype=np.uint8)
+    assert _load().orc_unpack_codec(L, k, _ptr(payload), C, _ptr(idx), _ptr(codes))
     return idx, codes
 
 
-def ef_compress(delta: np.ndarray, ef: np.ndarray, beta: float, *, bf16: bool = False):
+def ef_compress(delta: np.ndarray, ef: np.ndarray, beta: float, *, bf16: bool = False,
+                codec=None):
     """One sender round; ``ef`` (fp32) is updated in place.
 
-    ``delta`` is fp32, or with ``bf16=True`` a uint16 array of bf16 bit patterns.
-    Returns (payload[C,112] u8, scales[C] f32, flags).
+    ``delta`` is fp32, or with ``bf16=True`` a uint16 array of bf16 bit patterns.  ``codec``
+    is (L, k, rule) or None for the default codec.
+    Returns (payload[C,record_bytes] u8, scales[C] f32, flags).
     """
+    L, k, rule = _codec(codec)
     if bf16:
         delta = np.ascontiguousarray(delta, dtype=np.uint16)
     else:
         delta = np.ascontiguousarray(delta, dtype=np.float32)
     assert ef.dtype == np.float32 and ef.flags["C_CONTIGUOUS"] and ef.size == delta.size
     n = delta.size
-    C = num_chunks(n)
-    payload = np.zeros((C, RECORD_BYTES), dtype=np.uint8)
+    C = num_chunks(n, codec)
+    payload = np.zeros((C, record_bytes(codec)), dtype=np.uint8)
     scales = np.zeros(C, dtype=np.float32)
-    flags = _load().orc_ef_compress(_ptr(delta), 1 if bf16 else 0, _ptr(ef), n,
-                                    np.float32(beta), _ptr(payload), _ptr(scales))
+    flags = _load().orc_ef_compress_codec(L, k, rule, _ptr(delta), 1 if bf16 else 0, _ptr(ef),
+                                          n, np.float32(beta), _ptr(payload), _ptr(scales))
     return payload, scales, int(flags)
 
 
+def _peer_arrays(payloads, scales, n, codec):
+    P = len(payloads)
+    assert P == len(scales) and P >= 1
+    C = num_chunks(n, codec)
+    rb = record_bytes(codec)
+    pl = [np.ascontiguousarray(p, dtype=np.uint8).reshape(C, rb) for p in payloads]
+    sc = [np.ascontiguousarray(s, dtype=np.float32).reshape(C) for s in scales]
+    parr = (ctypes.c_void_p * P)(*[_ptr(p) for p in pl])
+    sarr = (ctypes.c_void_p * P)(*[_ptr(s) for s in sc])
+    return P, pl, sc, parr, sarr
+
+
 def decode_aggregate(payloads, scales, n: int, theta: np.ndarray | None = None,
-                     lr: float = 0.0):
+                     lr: float = 0.0, codec=None):
     """Mean of P peers' decoded records; with ``theta`` also theta -= lr * mean (in place).
 
     Returns (mean[n] f32, flags).
     """
-    P = len(payloads)
-    assert P == len(scales) and P >= 1
-    C = num_chunks(n)
-    pl = [np.ascontiguousarray(p, dtype=np.uint8).reshape(C, RECORD_BYTES) for p in payloads]
-    sc = [np.ascontiguousarray(s, dtype=np.float32).reshape(C) for s in scales]
-    parr = (ctypes.c_void_p * P)(*[_ptr(p) for p in pl])
-    sarr = (ctypes.c_void_p * P)(*[_ptr(s) for s in sc])
+    L, k, _ = _codec(codec)
+    P, pl, sc, parr, sarr = _peer_arrays(payloads, scales, n, codec)
     mean = np.zeros(n, dtype=np.float32)
     tptr = None
     if theta is not None:
         assert theta.dtype == np.float32 and theta.flags["C_CONTIGUOUS"] and theta.size == n
         tptr = _ptr(theta)
-    flags = _load().orc_decode_aggregate(parr, sarr, P, n, _ptr(mean), tptr, np.float32(lr))
+    flags = _load().orc_decode_aggregate_codec(L, k, parr, sarr, P, n, _ptr(mean), tptr,
+                                               np.float32(lr))
     return mean, int(flags)
 
 
-def peer_stats(payloads, scales, n: int) -> dict:
+def peer_stats(payloads, scales, n: int, codec=None) -> dict:
     """Per-peer statistics of the accepted records (rejected, big, negative, max_scale, sumsq).
 
     The Sparse Frontier, "What the Blockchain Does (and Doesn't Do)": crafted sparse updates
     look different from naturally concentrated ones.
     """
-    P = len(payloads)
-    C = num_chunks(n)
-    pl = [np.ascontiguousarray(p, dtype=np.uint8).reshape(C, RECORD_BYTES) for p in payloads]
-    sc = [np.ascontiguousarray(s, dtype=np.float32).reshape(C) for s in scales]
-    parr = (ctypes.c_void_p * P)(*[_ptr(p) for p in pl])
-    sarr = (ctypes.c_void_p * P)(*[_ptr(s) for s in sc])
+    L, k, _ = _codec(codec)
+    P, pl, sc, parr, sarr = _peer_arrays(payloads, scales, n, codec)
     out = {"rejected": np.zeros(P, np.uint32), "big": np.zeros(P, np.uint32),
            "negative": np.zeros(P, np.uint32), "max_scale": np.zeros(P, np.float32),
            "sumsq": np.zeros(P, np.float64)}
-    _load().orc_peer_stats(parr, sarr, P, n, _ptr(out["rejected"]), _ptr(out["big"]),
-                           _ptr(out["negative"]), _ptr(out["max_scale"]), _ptr(out["sumsq"]))
+    assert _load().orc_peer_stats_codec(L, k, parr, sarr, P, n, _ptr(out["rejected"]),
+                                        _ptr(out["big"]), _ptr(out["negative"]),
+                                        _ptr(out["max_scale"]), _ptr(out["sumsq"]))
     return out

@@ -40,6 +40,17 @@
  *     flag bit 1;
  *   - outer step: theta = fmaf(-lr, mean, theta).
  *
+ * Codec variants, for ablation (the pages fix L = 4096 and k = 64 and give the index width as
+ * ceil(log2 L); they leave the scale rule open):
+ *   - chunk length L (a power of two) and k <= L: every field is 2 + ceil(log2 L) bits, a record
+ *     is k such fields, packed as above, in ceil(k * (2 + log2 L) / 8) bytes; records follow one
+ *     another with no padding between them;
+ *   - scale rule 0 (the default): s = m / 1.5f as above;
+ *     scale rule 1 (mean-abs): s = (pairwise sum of |a| over the k chosen entries, in ascending
+ *     index order) / k, where the pairwise sum of x[0..n) is x[0] for n = 1 and otherwise the
+ *     sum of the first floor(n/2) entries plus the sum of the rest, each summed the same way;
+ *     the levels, the code rule, the residual and the decoder are those of rule 0.
+ *
  * Plain single-threaded C11.  Build with -O2 -ffp-contract=off and no fast-math: every
  * floating-point operation is one IEEE binary32 operation rounded to nearest-even, the
  * precision in which the codec's scale, residual and mean are defined.
@@ -59,11 +70,46 @@
 #define ORC_FLAG_NONFINITE 1u
 #define ORC_FLAG_BAD_RECORD 2u
 
+#define ORC_SCALE_MAX 0        /* s = max |a| / 1.5 */
+#define ORC_SCALE_MEAN_ABS 1   /* s = mean |a| over the chosen entries (variant) */
+
 int orc_chunk(void) { return ORC_CHUNK; }
 int orc_topk(void) { return ORC_TOPK; }
 int orc_record_bytes(void) { return ORC_RECORD_BYTES; }
 
 int64_t orc_num_chunks(int64_t n) { return (n + ORC_CHUNK - 1) / ORC_CHUNK; }
+
+/* A codec: chunk length L, k entries per record, scale rule, and the derived widths. */
+typedef struct {
+    int L, k, rule;
+    int idx_bits;      /* ceil(log2 L) ([SF] item 3) */
+    int field_bits;    /* 2 + idx_bits */
+    int record_bytes;  /* ceil(k * field_bits / 8) */
+} orc_codec;
+
+/* Fills cd; returns 0 when (L, k, rule) is not a codec: L a power of two in [2, 65536],
+ * 1 <= k <= L, rule 0 or 1. */
+static int orc_codec_init(orc_codec* cd, int L, int k, int rule) {
+    int b = 0;
+    if (L < 2 || L > 65536 || (L & (L - 1)) != 0) return 0;
+    if (k < 1 || k > L || (rule != ORC_SCALE_MAX && rule != ORC_SCALE_MEAN_ABS)) return 0;
+    while ((1 << b) < L) ++b;
+    cd->L = L;
+    cd->k = k;
+    cd->rule = rule;
+    cd->idx_bits = b;
+    cd->field_bits = ORC_VALUE_BITS + b;
+    cd->record_bytes = (k * cd->field_bits + 7) / 8;
+    return 1;
+}
+
+/* Record bytes of codec (L, k), or -1 when it is not one. */
+int orc_codec_record_bytes(int L, int k) {
+    orc_codec cd;
+    return orc_codec_init(&cd, L, k, ORC_SCALE_MAX) ? cd.record_bytes : -1;
+}
+
+int64_t orc_num_chunks_codec(int L, int64_t n) { return (n + L - 1) / L; }
 
 /* ------------------------------------------------------------------------------------------
  * Top-k selection ([SF] item 1), written for any chunk length L and any k <= L so that tiny
@@ -124,27 +170,39 @@ float orc_level(int code, float s) {
     return (code & 2) ? -q : q;
 }
 
+/* Pairwise (recursive halving) sum of x[0..n), n >= 1, in fp32: the mean-abs scale's sum. */
+float orc_pairwise_sum(const float* x, int n) {
+    int h;
+    if (n == 1) return x[0];
+    h = n / 2;
+    return orc_pairwise_sum(x, h) + orc_pairwise_sum(x + h, n - h);
+}
+
 /* ------------------------------------------------------------------------------------------
- * Record packing ([SF] per-chunk equation): 64 fields of 14 bits, written one bit at a time.
+ * Record packing ([SF] per-chunk equation): k fields of 2 + idx_bits bits (64 fields of 14
+ * bits for the default codec), written one bit at a time.
  * ---------------------------------------------------------------------------------------- */
-void orc_pack_record(const uint16_t* idx, const uint8_t* code, uint8_t* out) {
+static void orc_pack_record_cd(const orc_codec* cd, const uint16_t* idx, const uint8_t* code,
+                               uint8_t* out) {
     int r, b;
-    memset(out, 0, ORC_RECORD_BYTES);
-    for (r = 0; r < ORC_TOPK; ++r) {
-        uint32_t field = (uint32_t)(code[r] & 3u) | ((uint32_t)(idx[r] & 0xFFFu) << ORC_VALUE_BITS);
-        for (b = 0; b < ORC_FIELD_BITS; ++b) {
-            int bit = r * ORC_FIELD_BITS + b;
+    const uint32_t idx_mask = (1u << cd->idx_bits) - 1u;
+    memset(out, 0, (size_t)cd->record_bytes);
+    for (r = 0; r < cd->k; ++r) {
+        uint32_t field = (uint32_t)(code[r] & 3u) | (((uint32_t)idx[r] & idx_mask) << ORC_VALUE_BITS);
+        for (b = 0; b < cd->field_bits; ++b) {
+            int bit = r * cd->field_bits + b;
             if ((field >> b) & 1u) out[bit >> 3] |= (uint8_t)(1u << (bit & 7));
         }
     }
 }
 
-void orc_unpack_record(const uint8_t* rec, uint16_t* idx, uint8_t* code) {
+static void orc_unpack_record_cd(const orc_codec* cd, const uint8_t* rec, uint16_t* idx,
+                                 uint8_t* code) {
     int r, b;
-    for (r = 0; r < ORC_TOPK; ++r) {
+    for (r = 0; r < cd->k; ++r) {
         uint32_t field = 0;
-        for (b = 0; b < ORC_FIELD_BITS; ++b) {
-            int bit = r * ORC_FIELD_BITS + b;
+        for (b = 0; b < cd->field_bits; ++b) {
+            int bit = r * cd->field_bits + b;
             if ((rec[bit >> 3] >> (bit & 7)) & 1u) field |= 1u << b;
         }
         code[r] = (uint8_t)(field & 3u);
@@ -152,16 +210,50 @@ void orc_unpack_record(const uint8_t* rec, uint16_t* idx, uint8_t* code) {
     }
 }
 
-void orc_pack(const uint16_t* idx, const uint8_t* code, int64_t C, uint8_t* payload) {
+static orc_codec orc_default_codec(void) {
+    orc_codec cd;
+    orc_codec_init(&cd, ORC_CHUNK, ORC_TOPK, ORC_SCALE_MAX);
+    return cd;
+}
+
+void orc_pack_record(const uint16_t* idx, const uint8_t* code, uint8_t* out) {
+    orc_codec cd = orc_default_codec();
+    orc_pack_record_cd(&cd, idx, code, out);
+}
+
+void orc_unpack_record(const uint8_t* rec, uint16_t* idx, uint8_t* code) {
+    orc_codec cd = orc_default_codec();
+    orc_unpack_record_cd(&cd, rec, idx, code);
+}
+
+/* idx[C][k], code[C][k] <-> payload[C][record_bytes] for codec (L, k).  Returns 0 when (L, k)
+ * is not a codec (nothing written). */
+int orc_pack_codec(int L, int k, const uint16_t* idx, const uint8_t* code, int64_t C,
+                   uint8_t* payload) {
+    orc_codec cd;
     int64_t c;
+    if (!orc_codec_init(&cd, L, k, ORC_SCALE_MAX)) return 0;
     for (c = 0; c < C; ++c)
-        orc_pack_record(idx + c * ORC_TOPK, code + c * ORC_TOPK, payload + c * ORC_RECORD_BYTES);
+        orc_pack_record_cd(&cd, idx + c * k, code + c * k, payload + c * cd.record_bytes);
+    return 1;
+}
+
+int orc_unpack_codec(int L, int k, const uint8_t* payload, int64_t C, uint16_t* idx,
+                     uint8_t* code) {
+    orc_codec cd;
+    int64_t c;
+    if (!orc_codec_init(&cd, L, k, ORC_SCALE_MAX)) return 0;
+    for (c = 0; c < C; ++c)
+        orc_unpack_record_cd(&cd, payload + c * cd.record_bytes, idx + c * k, code + c * k);
+    return 1;
+}
+
+void orc_pack(const uint16_t* idx, const uint8_t* code, int64_t C, uint8_t* payload) {
+    orc_pack_codec(ORC_CHUNK, ORC_TOPK, idx, code, C, payload);
 }
 
 void orc_unpack(const uint8_t* payload, int64_t C, uint16_t* idx, uint8_t* code) {
-    int64_t c;
-    for (c = 0; c < C; ++c)
-        orc_unpack_record(payload + c * ORC_RECORD_BYTES, idx + c * ORC_TOPK, code + c * ORC_TOPK);
+    orc_unpack_codec(ORC_CHUNK, ORC_TOPK, payload, C, idx, code);
 }
 
 /* ------------------------------------------------------------------------------------------
@@ -179,23 +271,26 @@ static float orc_bf16_to_float(uint16_t h) {
     return f;
 }
 
-uint32_t orc_ef_compress(const void* delta, int delta_is_bf16, float* ef, int64_t n, float beta,
-                         uint8_t* payload, float* scales) {
-    int64_t C = orc_num_chunks(n);
+static uint32_t orc_ef_compress_cd(const orc_codec* cd, const void* delta, int delta_is_bf16,
+                                   float* ef, int64_t n, float beta, uint8_t* payload,
+                                   float* scales) {
+    const int L = cd->L, k = cd->k;
+    int64_t C = orc_num_chunks_codec(L, n);
     int64_t c;
     uint32_t flags = 0;
-    float a[ORC_CHUNK];
-    int sel[ORC_TOPK];
-    uint16_t idx[ORC_TOPK];
-    uint8_t code[ORC_TOPK];
+    float* a = (float*)malloc(sizeof(float) * (size_t)L);
+    float* mags = (float*)malloc(sizeof(float) * (size_t)k);
+    int* sel = (int*)malloc(sizeof(int) * (size_t)k);
+    uint16_t* idx = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)k);
+    uint8_t* code = (uint8_t*)malloc((size_t)k);
 
     for (c = 0; c < C; ++c) {
-        int64_t base = c * ORC_CHUNK;
+        int64_t base = c * L;
         int j, r, top;
-        float m, s;
+        float s;
 
         /* e <- beta * e + delta, on the zero-padded chunk */
-        for (j = 0; j < ORC_CHUNK; ++j) {
+        for (j = 0; j < L; ++j) {
             int64_t i = base + j;
             if (i < n) {
                 float d = delta_is_bf16 ? orc_bf16_to_float(((const uint16_t*)delta)[i])
@@ -207,24 +302,49 @@ uint32_t orc_ef_compress(const void* delta, int delta_is_bf16, float* ef, int64_
             }
         }
 
-        top = orc_topk_select(a, ORC_CHUNK, ORC_TOPK, sel);
-        m = fabsf(a[top]);
-        s = orc_scale(m);
+        top = orc_topk_select(a, L, k, sel);
+        if (cd->rule == ORC_SCALE_MAX) {
+            s = orc_scale(fabsf(a[top]));
+        } else {
+            for (r = 0; r < k; ++r) mags[r] = fabsf(a[sel[r]]);
+            s = orc_pairwise_sum(mags, k) / (float)k;
+        }
 
-        for (r = 0; r < ORC_TOPK; ++r) {
+        for (r = 0; r < k; ++r) {
             float v = a[sel[r]];
             code[r] = (uint8_t)orc_code(v, s);
             idx[r] = (uint16_t)sel[r];
             a[sel[r]] = v - orc_level(code[r], s); /* residual at a transmitted position */
         }
 
-        for (j = 0; j < ORC_CHUNK; ++j)
+        for (j = 0; j < L; ++j)
             if (base + j < n) ef[base + j] = a[j];
 
-        orc_pack_record(idx, code, payload + c * ORC_RECORD_BYTES);
+        orc_pack_record_cd(cd, idx, code, payload + c * cd->record_bytes);
         scales[c] = s;
     }
+    free(a);
+    free(mags);
+    free(sel);
+    free(idx);
+    free(code);
     return flags;
+}
+
+uint32_t orc_ef_compress(const void* delta, int delta_is_bf16, float* ef, int64_t n, float beta,
+                         uint8_t* payload, float* scales) {
+    orc_codec cd = orc_default_codec();
+    return orc_ef_compress_cd(&cd, delta, delta_is_bf16, ef, n, beta, payload, scales);
+}
+
+/* The sender for codec (L, k, rule); payload holds ceil(n / L) records of
+ * orc_codec_record_bytes(L, k) bytes.  Returns 0xffffffff when (L, k, rule) is not a codec. */
+uint32_t orc_ef_compress_codec(int L, int k, int rule, const void* delta, int delta_is_bf16,
+                               float* ef, int64_t n, float beta, uint8_t* payload,
+                               float* scales) {
+    orc_codec cd;
+    if (!orc_codec_init(&cd, L, k, rule)) return 0xffffffffu;
+    return orc_ef_compress_cd(&cd, delta, delta_is_bf16, ef, n, beta, payload, scales);
 }
 
 /* ------------------------------------------------------------------------------------------
@@ -235,64 +355,86 @@ uint32_t orc_ef_compress(const void* delta, int delta_is_bf16, float* ef, int64_
  * payloads[p]: C * 112 bytes; scales[p]: C floats; mean_out: n floats (overwritten);
  * theta: n floats or NULL.  Returns flag bit 1 when some record was rejected.
  * ---------------------------------------------------------------------------------------- */
-static int orc_record_ok(const uint16_t* idx, float s) {
+static int orc_record_ok(const uint16_t* idx, int k, float s) {
     int r;
     if (isnan(s) || isinf(s) || s < 0.0f) return 0;
-    for (r = 1; r < ORC_TOPK; ++r)
+    for (r = 1; r < k; ++r)
         if (!(idx[r - 1] < idx[r])) return 0;
     return 1;
 }
 
-uint32_t orc_decode_aggregate(const uint8_t* const* payloads, const float* const* scales, int P,
-                              int64_t n, float* mean_out, float* theta, float lr) {
-    int64_t C = orc_num_chunks(n);
+static uint32_t orc_decode_aggregate_cd(const orc_codec* cd, const uint8_t* const* payloads,
+                                        const float* const* scales, int P, int64_t n,
+                                        float* mean_out, float* theta, float lr) {
+    const int L = cd->L, k = cd->k;
+    int64_t C = orc_num_chunks_codec(L, n);
     int64_t c;
     uint32_t flags = 0;
-    float acc[ORC_CHUNK];
-    uint16_t idx[ORC_TOPK];
-    uint8_t code[ORC_TOPK];
+    float* acc = (float*)malloc(sizeof(float) * (size_t)L);
+    uint16_t* idx = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)k);
+    uint8_t* code = (uint8_t*)malloc((size_t)k);
 
     for (c = 0; c < C; ++c) {
-        int64_t base = c * ORC_CHUNK;
+        int64_t base = c * L;
         int p, r, j;
-        for (j = 0; j < ORC_CHUNK; ++j) acc[j] = 0.0f;
+        for (j = 0; j < L; ++j) acc[j] = 0.0f;
         for (p = 0; p < P; ++p) {
             float s = scales[p][c];
-            orc_unpack_record(payloads[p] + c * ORC_RECORD_BYTES, idx, code);
-            if (!orc_record_ok(idx, s)) {
+            orc_unpack_record_cd(cd, payloads[p] + c * cd->record_bytes, idx, code);
+            if (!orc_record_ok(idx, k, s)) {
                 flags |= ORC_FLAG_BAD_RECORD;
                 continue;
             }
-            for (r = 0; r < ORC_TOPK; ++r)
+            for (r = 0; r < k; ++r)
                 if (base + idx[r] < n) acc[idx[r]] += orc_level(code[r], s);
         }
-        for (j = 0; j < ORC_CHUNK; ++j) {
+        for (j = 0; j < L; ++j) {
             int64_t i = base + j;
             if (i >= n) break;
             mean_out[i] = acc[j] / (float)P;
             if (theta) theta[i] = fmaf(-lr, mean_out[i], theta[i]);
         }
     }
+    free(acc);
+    free(idx);
+    free(code);
     return flags;
+}
+
+uint32_t orc_decode_aggregate(const uint8_t* const* payloads, const float* const* scales, int P,
+                              int64_t n, float* mean_out, float* theta, float lr) {
+    orc_codec cd = orc_default_codec();
+    return orc_decode_aggregate_cd(&cd, payloads, scales, P, n, mean_out, theta, lr);
+}
+
+/* The receiver for codec (L, k); 0xffffffff when (L, k) is not a codec. */
+uint32_t orc_decode_aggregate_codec(int L, int k, const uint8_t* const* payloads,
+                                    const float* const* scales, int P, int64_t n,
+                                    float* mean_out, float* theta, float lr) {
+    orc_codec cd;
+    if (!orc_codec_init(&cd, L, k, ORC_SCALE_MAX)) return 0xffffffffu;
+    return orc_decode_aggregate_cd(&cd, payloads, scales, P, n, mean_out, theta, lr);
 }
 
 /* ------------------------------------------------------------------------------------------
  * Receiver statistics per peer, for screening updates that look unlike the rest ([SF] "What
  * the Blockchain Does (and Doesn't Do)": a crafted sparse update looks different from a
- * naturally concentrated one).  Over the 64 entries of every accepted record of peer p:
+ * naturally concentrated one).  Over the k entries of every accepted record of peer p:
  *   big[p]       entries with the magnitude bit set (|q| = 1.5 s)
  *   negative[p]  entries with the sign bit set
  *   max_scale[p] the largest scale among accepted records (0 if none)
  *   sumsq[p]     the sum of q^2 (fp64; q^2 is exact in fp64), records in chunk order
  * and rejected[p], the number of rejected records.  Arrays of P, overwritten.
  * ---------------------------------------------------------------------------------------- */
-void orc_peer_stats(const uint8_t* const* payloads, const float* const* scales, int P, int64_t n,
-                    uint32_t* rejected, uint32_t* big, uint32_t* negative, float* max_scale,
-                    double* sumsq) {
-    int64_t C = orc_num_chunks(n);
+static void orc_peer_stats_cd(const orc_codec* cd, const uint8_t* const* payloads,
+                              const float* const* scales, int P, int64_t n, uint32_t* rejected,
+                              uint32_t* big, uint32_t* negative, float* max_scale,
+                              double* sumsq) {
+    const int k = cd->k;
+    int64_t C = orc_num_chunks_codec(cd->L, n);
     int p;
-    uint16_t idx[ORC_TOPK];
-    uint8_t code[ORC_TOPK];
+    uint16_t* idx = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)k);
+    uint8_t* code = (uint8_t*)malloc((size_t)k);
     for (p = 0; p < P; ++p) {
         int64_t c;
         rejected[p] = big[p] = negative[p] = 0;
@@ -301,13 +443,13 @@ void orc_peer_stats(const uint8_t* const* payloads, const float* const* scales, 
         for (c = 0; c < C; ++c) {
             float s = scales[p][c];
             int r;
-            orc_unpack_record(payloads[p] + c * ORC_RECORD_BYTES, idx, code);
-            if (!orc_record_ok(idx, s)) {
+            orc_unpack_record_cd(cd, payloads[p] + c * cd->record_bytes, idx, code);
+            if (!orc_record_ok(idx, k, s)) {
                 rejected[p] += 1;
                 continue;
             }
             if (s > max_scale[p]) max_scale[p] = s;
-            for (r = 0; r < ORC_TOPK; ++r) {
+            for (r = 0; r < k; ++r) {
                 double q = (double)orc_level(code[r], s);
                 big[p] += code[r] & 1u;
                 negative[p] += (code[r] >> 1) & 1u;
@@ -315,4 +457,23 @@ void orc_peer_stats(const uint8_t* const* payloads, const float* const* scales, 
             }
         }
     }
+    free(idx);
+    free(code);
+}
+
+void orc_peer_stats(const uint8_t* const* payloads, const float* const* scales, int P, int64_t n,
+                    uint32_t* rejected, uint32_t* big, uint32_t* negative, float* max_scale,
+                    double* sumsq) {
+    orc_codec cd = orc_default_codec();
+    orc_peer_stats_cd(&cd, payloads, scales, P, n, rejected, big, negative, max_scale, sumsq);
+}
+
+/* Statistics for codec (L, k); returns 0 (nothing written) when (L, k) is not a codec. */
+int orc_peer_stats_codec(int L, int k, const uint8_t* const* payloads, const float* const* scales,
+                         int P, int64_t n, uint32_t* rejected, uint32_t* big, uint32_t* negative,
+                         float* max_scale, double* sumsq) {
+    orc_codec cd;
+    if (!orc_codec_init(&cd, L, k, ORC_SCALE_MAX)) return 0;
+    orc_peer_stats_cd(&cd, payloads, scales, P, n, rejected, big, negative, max_scale, sumsq);
+    return 1;
 }
