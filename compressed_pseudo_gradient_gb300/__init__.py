@@ -18,6 +18,8 @@ from ._binding import (  # noqa: F401
     FLAG_NONFINITE,
     MAX_PEERS,
     RECORD_BYTES,
+    SCALE_MAX_ABS,
+    SCALE_MEAN_ABS,
     TOPK,
     SplError,
     decode_aggregate,
@@ -29,5 +31,6 @@ from ._binding import (  # noqa: F401
     num_chunks,
     pack,
     read_peer_stats,
+    record_bytes,
     unpack,
 )

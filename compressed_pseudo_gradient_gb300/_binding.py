@@ -21,6 +21,8 @@ RECORD_BYTES = 112
 MAX_PEERS = 256
 FLAG_NONFINITE = 1
 FLAG_BAD_RECORD = 2
+SCALE_MAX_ABS = 0     # s = max |a| / 1.5 (the default)
+SCALE_MEAN_ABS = 1    # s = pairwise sum of the chosen |a| / k (codec variant)
 
 _F32, _BF16 = 0, 1
 _lock = threading.Lock()
@@ -43,6 +45,11 @@ class SplError(RuntimeError):
 
 class _Tensor(ctypes.Structure):
     _fields_ = [("delta", ctypes.c_void_p), ("ef", ctypes.c_void_p), ("n", ctypes.c_size_t)]
+
+
+class _Codec(ctypes.Structure):
+    _fields_ = [("chunk", ctypes.c_uint32), ("topk", ctypes.c_uint32),
+                ("scale_rule", ctypes.c_uint32)]
 
 
 def library_path() -> str:
@@ -75,6 +82,16 @@ def library():
         lib.spl_decode_aggregate_stats.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), ci,
                                                    sz, vp, vp, cf, vp, vp, vp]
         lib.spl_decode_aggregate_stats.restype = ci
+        cp = ctypes.POINTER(_Codec)
+        lib.spl_codec_record_bytes.argtypes = [cp]
+        lib.spl_codec_record_bytes.restype = ctypes.c_int64
+        lib.spl_codec_num_chunks.argtypes, lib.spl_codec_num_chunks.restype = [cp, sz], sz
+        lib.spl_ef_compress_codec.argtypes = [cp, ctypes.POINTER(_Tensor), ci, ci, cf, vp, vp,
+                                              vp, vp]
+        lib.spl_ef_compress_codec.restype = ci
+        lib.spl_decode_aggregate_codec.argtypes = [cp, ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                                   ci, sz, vp, vp, cf, vp, vp, vp]
+        lib.spl_decode_aggregate_codec.restype = ci
         lib.spl_pack.argtypes, lib.spl_pack.restype = [vp, vp, sz, vp, vp], ci
         lib.spl_unpack.argtypes, lib.spl_unpack.restype = [vp, sz, vp, vp, vp], ci
         _lib = lib
@@ -112,8 +129,26 @@ def _flags_ptr(flags, dev):
     return flags.data_ptr()
 
 
-def num_chunks(n: int) -> int:
-    return (int(n) + CHUNK - 1) // CHUNK
+def _codec(codec):
+    """ctypes codec of a (L, k, rule) tuple, or None for the default codec."""
+    if codec is None:
+        return None
+    L, k, rule = (int(x) for x in codec)
+    c = _Codec(L, k, rule)
+    if library().spl_codec_record_bytes(ctypes.byref(c)) < 0:
+        raise ValueError(f"codec {tuple(codec)} is not implemented by libspl")
+    return c
+
+
+def record_bytes(codec=None) -> int:
+    """Bytes of one record: 112 for the default codec, k * (2 + log2 L) / 8 for a variant."""
+    c = _codec(codec)
+    return RECORD_BYTES if c is None else int(library().spl_codec_record_bytes(ctypes.byref(c)))
+
+
+def num_chunks(n: int, codec=None) -> int:
+    L = CHUNK if codec is None else int(codec[0])
+    return (int(n) + L - 1) // L
 
 
 def _ef_tensor(ef: torch.Tensor, dev: torch.device) -> torch.Tensor:
@@ -131,13 +166,17 @@ def _ef_tensor(ef: torch.Tensor, dev: torch.device) -> torch.Tensor:
 
 
 def ef_compress(delta: torch.Tensor, ef: torch.Tensor, beta: float, *, payload=None,
-                scales=None, flags=None):
+                scales=None, flags=None, codec=None):
     """One sender round (spl_ef_compress); ``ef`` is updated in place.
 
     delta: fp32 or bf16 CUDA tensor of n values; ef: fp32 tensor of n values, on the same
-    GPU or in pinned host memory (then read and written over the host link).
-    Returns (payload uint8 [C, 112], scales fp32 [C]).
+    GPU or in pinned host memory (then read and written over the host link).  ``codec``:
+    (L, k, rule) of a codec variant (spl_ef_compress_codec), or None for the default codec.
+    Returns (payload uint8 [C, record_bytes], scales fp32 [C]).
     """
+    if codec is not None:
+        return ef_compress_multi([delta], [ef], beta, payload=payload, scales=scales,
+                                 flags=flags, codec=codec)
     lib = library()
     _cuda(delta, "delta", (torch.float32, torch.bfloat16))
     _ef_tensor(ef, delta.device)
@@ -162,12 +201,16 @@ def ef_compress(delta: torch.Tensor, ef: torch.Tensor, beta: float, *, payload=N
     return payload, scales
 
 
-def ef_compress_multi(deltas, efs, beta: float, *, payload=None, scales=None, flags=None):
-    """One sender round over a list of tensors, each chunked on its own (spl_ef_compress_multi).
+def ef_compress_multi(deltas, efs, beta: float, *, payload=None, scales=None, flags=None,
+                      codec=None):
+    """One sender round over a list of tensors, each chunked on its own (spl_ef_compress_multi,
+    or spl_ef_compress_codec for a codec variant (L, k, rule)).
 
-    Returns (payload uint8 [sum C_i, 112], scales fp32 [sum C_i]) in tensor order.
+    Returns (payload uint8 [sum C_i, record_bytes], scales fp32 [sum C_i]) in tensor order.
     """
     lib = library()
+    cd = _codec(codec)
+    rb = record_bytes(codec)
     if len(deltas) != len(efs) or not deltas:
         raise ValueError("deltas and efs must be non-empty lists of equal length")
     dtype = deltas[0].dtype
@@ -182,22 +225,24 @@ def ef_compress_multi(deltas, efs, beta: float, *, payload=None, scales=None, fl
         table[i].delta = d.data_ptr() if d.numel() else None
         table[i].ef = e.data_ptr() if e.numel() else None
         table[i].n = d.numel()
-        C += num_chunks(d.numel())
+        C += num_chunks(d.numel(), codec)
     if payload is None:
-        payload = torch.empty((C, RECORD_BYTES), dtype=torch.uint8, device=dev)
+        payload = torch.empty((C, rb), dtype=torch.uint8, device=dev)
     if scales is None:
         scales = torch.empty(C, dtype=torch.float32, device=dev)
     _cuda(payload, "payload", (torch.uint8,))
     _cuda(scales, "scales", (torch.float32,))
-    if payload.numel() < C * RECORD_BYTES or scales.numel() < C:
+    if payload.numel() < C * rb or scales.numel() < C:
         raise ValueError("payload/scales too small")
+    args = (table, len(deltas), _BF16 if dtype == torch.bfloat16 else _F32, float(beta),
+            payload.data_ptr() if C else None, scales.data_ptr() if C else None,
+            _flags_ptr(flags, dev), _stream(dev))
     with torch.cuda.device(dev):
-        st = lib.spl_ef_compress_multi(table, len(deltas),
-                                       _BF16 if dtype == torch.bfloat16 else _F32, float(beta),
-                                       payload.data_ptr() if C else None,
-                                       scales.data_ptr() if C else None,
-                                       _flags_ptr(flags, dev), _stream(dev))
-    _check("spl_ef_compress_multi", st)
+        if cd is None:
+            st = lib.spl_ef_compress_multi(*args)
+        else:
+            st = lib.spl_ef_compress_codec(ctypes.byref(cd), *args)
+    _check("spl_ef_compress_multi" if cd is None else "spl_ef_compress_codec", st)
     return payload, scales
 
 
@@ -221,20 +266,23 @@ def read_peer_stats(stats: torch.Tensor) -> dict:
 
 
 def decode_aggregate(payloads, scales, n: int, *, mean=None, theta=None, lr: float = 0.0,
-                     flags=None, stats=None):
+                     flags=None, stats=None, codec=None):
     """Mean of P peers' decoded records, optionally fused with theta -= lr * mean in place
     (spl_decode_aggregate).  With ``stats`` (from new_peer_stats, accumulated into), also the
-    per-peer statistics (spl_decode_aggregate_stats).  Returns mean (fp32 [n])."""
+    per-peer statistics (spl_decode_aggregate_stats).  ``codec``: (L, k, rule) of a codec
+    variant (spl_decode_aggregate_codec), or None.  Returns mean (fp32 [n])."""
     lib = library()
+    cd = _codec(codec)
+    rb = record_bytes(codec)
     P = len(payloads)
     if P != len(scales) or P < 1:
         raise ValueError("payloads and scales must be non-empty lists of equal length")
     dev = payloads[0].device
-    C = num_chunks(n)
+    C = num_chunks(n, codec)
     for i, (p, s) in enumerate(zip(payloads, scales)):
         _cuda(p, f"payloads[{i}]", (torch.uint8,))
         _cuda(s, f"scales[{i}]", (torch.float32,))
-        if p.device != dev or s.device != dev or p.numel() < C * RECORD_BYTES or s.numel() < C:
+        if p.device != dev or s.device != dev or p.numel() < C * rb or s.numel() < C:
             raise ValueError(f"peer {i}: device mismatch or arrays too small")
     if mean is None:
         mean = torch.empty(n, dtype=torch.float32, device=dev)
@@ -249,18 +297,28 @@ def decode_aggregate(payloads, scales, n: int, *, mean=None, theta=None, lr: flo
         tptr = theta.data_ptr()
     parr = (ctypes.c_void_p * P)(*[p.data_ptr() for p in payloads])
     sarr = (ctypes.c_void_p * P)(*[s.data_ptr() for s in scales])
+    sptr = None
+    if stats is not None:
+        _cuda(stats, "stats", (torch.uint8,))
+        if stats.numel() < P * PEER_STATS_BYTES or stats.device != dev:
+            raise ValueError("stats must hold P x 24 bytes on the inputs' device")
+        sptr = stats.data_ptr()
     with torch.cuda.device(dev):
-        if stats is None:
+        if cd is not None:
+            fn = "spl_decode_aggregate_codec"
+            st = lib.spl_decode_aggregate_codec(ctypes.byref(cd), parr, sarr, P, int(n),
+                                                mean.data_ptr(), tptr, float(lr), sptr,
+                                                _flags_ptr(flags, dev), _stream(dev))
+        elif stats is None:
+            fn = "spl_decode_aggregate"
             st = lib.spl_decode_aggregate(parr, sarr, P, int(n), mean.data_ptr(), tptr, float(lr),
                                           _flags_ptr(flags, dev), _stream(dev))
         else:
-            _cuda(stats, "stats", (torch.uint8,))
-            if stats.numel() < P * PEER_STATS_BYTES or stats.device != dev:
-                raise ValueError("stats must hold P x 24 bytes on the inputs' device")
+            fn = "spl_decode_aggregate_stats"
             st = lib.spl_decode_aggregate_stats(parr, sarr, P, int(n), mean.data_ptr(), tptr,
-                                                float(lr), stats.data_ptr(),
-                                                _flags_ptr(flags, dev), _stream(dev))
-    _check("spl_decode_aggregate_stats" if stats is not None else "spl_decode_aggregate", st)
+                                                float(lr), sptr, _flags_ptr(flags, dev),
+                                                _stream(dev))
+    _check(fn, st)
     return mean
 
 

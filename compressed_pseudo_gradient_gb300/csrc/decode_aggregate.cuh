@@ -1,0 +1,423 @@
+// Receiver kernel of the SparseLoCo codec: decode P peers' records, take their mean, and
+// optionally apply the outer step theta <- theta - lr * mean, in one pass over HBM.
+// Templated on the record geometry (chunk length L, k) and on the per-peer statistics; the
+// translation units that include this header instantiate it (the default codec in
+// decode_aggregate.cu, the variants in decode_aggregate_variants.cu).  The figures below are
+// the default codec's.
+//
+// Method: "The Sparse Frontier: SparseLoCo and the Compression Math Behind Permissionless
+// Pre-Training", "SparseLoCo: Three Compression Levers in One Pass" (item 3: the receiver
+// rebuilds positions from the 12-bit indices) and "Why Extreme Sparsity Doesn't Break
+// Convergence" ("Sparse aggregation can improve model quality": the peers' sparse updates
+// are aggregated); "Why DiLoCo Alone Isn't Enough" for the pseudo-gradient's sign.
+//
+// Design (HBM-bound: P x 116 B read per chunk, 16 KB of mean written, 32 KB of theta read and
+// written when the outer step is fused):
+//   - one 256-thread CTA per chunk, grid-stride over chunks with a persistent grid; while a
+//     chunk is worked on, the next chunk's theta (one 16 KB bulk copy, TMA) and its P records
+//     (16-byte cp.async copies spread over the threads) fly into a shared-memory stage, all
+//     completing on one mbarrier; the next chunk's P scales travel as plain loads into
+//     registers (lane l of warp w holds peer 8 l + w's);
+//   - each warp unpacks whole records (one peer at a time): the 64 14-bit fields, a check that
+//     the indices ascend strictly and the scale is finite and non-negative, and the decoded
+//     value of every entry, stored as (position, value) pairs (with statistics, the warp also
+//     counts the record's magnitude and sign bits and keeps them beside its scale);
+//   - then one warp adds the peers into a 16 KB shared accumulator in order p = 0..P-1, two
+//     entries per lane (distinct positions within a valid record), so every position is summed
+//     in fp32 in peer order from +0.0, as a plain sequential loop over peers would, with no
+//     atomics; a single warp keeps every lane busy and the instruction count minimal, while
+//     the other resident CTAs keep the SM fed;
+//   - the dense pass divides by P (correctly rounded, with a precomputed reciprocal), stores
+//     the mean and the updated theta with streaming stores and clears the accumulator.  Peers
+//     are unpacked in groups of up to 64, so shared memory stays bounded for any P.
+#pragma once
+
+#include <cfloat>
+
+#include "spl_device.cuh"
+#include "spl_kernels.h"
+
+namespace spl {
+namespace {
+
+#ifndef SPL_DECODE_STAGES
+#define SPL_DECODE_STAGES 1
+#endif
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kStages = SPL_DECODE_STAGES;
+
+// Per-codec sizes of the receiver (default: 512 positions and 4 vectors per thread of each
+// warp, groups of 64 peers, two entries per lane, seven 16-byte pieces per record).
+template <class Geo>
+struct RecvShape {
+    static constexpr int kChunk = Geo::kChunk;
+    static constexpr int kTopK = Geo::kTopK;
+    static constexpr int kSlice = kChunk / kWarps;          // positions per warp
+    static constexpr int kVec = kSlice / 128;               // vectors of 4 per thread
+    static constexpr int kGroup = kTopK <= 64 ? 64 : 32;    // peers unpacked per pass
+    static constexpr int kPerLane = kTopK / 32;             // entries per lane of a record
+    static constexpr int kPieceBytes = Geo::kVecRecords ? 16 : 4;
+    static constexpr int kPieces = Geo::kRecordBytes / kPieceBytes;   // copies per record
+    static constexpr int kMinBlocks = kChunk <= 4096 ? 4 : 2;
+};
+
+__host__ __device__ constexpr size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+
+// Dynamic shared memory for P peers (offsets 16-byte aligned), G = min(P, group):
+//   bar[2] | theta stage [S][4096] f32 | record stage [S][P][112] (+16) | acc [4096] f32 |
+//   entries [G][64] (position, value) | validity [G] u32 |
+//   with statistics only: (scale, magnitude | sign << 8 bit counts) [G] | per-peer totals of
+//   this CTA: sum of squares and its Kahan compensation [2][P] f32 | rejected, big, negative
+//   [3][P] u32 | max scale [P] f32
+template <class Geo>
+struct Layout {
+    size_t bar, theta, rec, acc, ent, ok, sgrp, st_sq, st_cnt, st_max, total;
+    __host__ __device__ Layout(int P, bool stats) {
+        using S = RecvShape<Geo>;
+        const size_t G = static_cast<size_t>(P < S::kGroup ? P : S::kGroup);
+        bar = 0;
+        theta = 16;
+        rec = theta + kStages * S::kChunk * 4;
+        acc = rec + align16(kStages * static_cast<size_t>(P) * Geo::kRecordBytes) + 16;
+        ent = acc + S::kChunk * 4;
+        ok = ent + G * S::kTopK * 8;
+        sgrp = ok + align16(G * 4);
+        st_sq = sgrp + align16(G * 8);
+        st_cnt = st_sq + align16(static_cast<size_t>(P) * 8);
+        st_max = st_cnt + align16(3 * static_cast<size_t>(P) * 4);
+        total = stats ? st_max + align16(static_cast<size_t>(P) * 4) : sgrp;
+    }
+};
+
+// All threads: start chunk c's copies into one stage.  Thread 0 arrives with the expected
+// theta bytes (a full chunk when the outer step is fused) and starts its bulk copy; the
+// record pieces (7 x 16 B per peer; 4-byte pieces for a variant whose records are not 16-byte
+// aligned) are spread over the threads, each of which arrives once its own copies have
+// landed.  Arrivals per phase: min(pieces, 256) + 1.
+template <class Geo>
+__device__ __forceinline__ void prefetch(const DecodeTable& tab, int P, int64_t c, bool full,
+                                         const float* theta, uint64_t* bar, uint8_t* st_rec,
+                                         float* st_theta, int tid) {
+    using S = RecvShape<Geo>;
+    constexpr int kChunk = S::kChunk;
+    constexpr int kRecordBytes = Geo::kRecordBytes;
+    constexpr int kPieces = S::kPieces;
+    constexpr int kPieceBytes = S::kPieceBytes;
+    if (tid == 0) {
+        if (theta != nullptr && full) {
+            fence_async_smem();
+            mbar_expect_tx(bar, kChunk * 4);
+            bulk_load(st_theta, theta + c * kChunk, kChunk * 4, bar);
+        } else {
+            mbar_arrive(bar);
+        }
+    }
+    const int pieces = P * kPieces;
+    if (tid < pieces) {
+        for (int i = tid; i < pieces; i += kThreads) {
+            const int p = i / kPieces;
+            const int w = i - p * kPieces;
+            if constexpr (kPieceBytes == 16)
+                cp_async16(st_rec + i * 16, tab.payload[p] + c * kRecordBytes + w * 16);
+            else
+                cp_async4(st_rec + i * 4, tab.payload[p] + c * kRecordBytes + w * 4);
+        }
+        cp_async_arrive(bar);
+    }
+}
+
+template <class Geo, bool kStats>
+__global__ void __launch_bounds__(kThreads, RecvShape<Geo>::kMinBlocks)
+k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __restrict__ mean,
+                   float* __restrict__ theta, float neg_lr, PeerStats* __restrict__ stats,
+                   uint32_t* __restrict__ flags) {
+    using S = RecvShape<Geo>;
+    constexpr int kChunk = S::kChunk;
+    constexpr int kTopK = S::kTopK;
+    constexpr int kSlice = S::kSlice;
+    constexpr int kVec = S::kVec;
+    constexpr int kGroup = S::kGroup;
+    constexpr int kPerLane = S::kPerLane;
+    constexpr int kRecordBytes = Geo::kRecordBytes;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const Layout<Geo> L(P, kStats);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + L.bar);
+    float* st_theta = reinterpret_cast<float*>(smem_raw + L.theta);
+    uint8_t* st_rec = smem_raw + L.rec;
+    float* acc = reinterpret_cast<float*>(smem_raw + L.acc);
+    uint2* ent = reinterpret_cast<uint2*>(smem_raw + L.ent);
+    uint32_t* okp = reinterpret_cast<uint32_t*>(smem_raw + L.ok);
+    uint2* sgrp = reinterpret_cast<uint2*>(smem_raw + L.sgrp);
+    float* st_sum = reinterpret_cast<float*>(smem_raw + L.st_sq);        // [P]
+    float* st_comp = st_sum + P;                                           // [P]
+    uint32_t* st_cnt = reinterpret_cast<uint32_t*>(smem_raw + L.st_cnt);   // [3][P]
+    float* st_max = reinterpret_cast<float*>(smem_raw + L.st_max);
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int64_t C = (n + kChunk - 1) / kChunk;
+    const int64_t G = gridDim.x;
+    if (static_cast<int64_t>(blockIdx.x) >= C) return;
+    const float pf = static_cast<float>(P);
+    const int slice0 = kSlice * warp;    // this warp's positions: slice0 + 128 v + 4 lane + u
+    const int my_peer = 8 * lane + warp; // the peer whose scale this lane carries
+
+#pragma unroll
+    for (int v = 0; v < kVec; ++v)
+        *reinterpret_cast<float4*>(&acc[slice0 + 128 * v + 4 * lane]) = make_float4(0.f, 0.f, 0.f, 0.f);
+    if constexpr (kStats) {
+        for (int p = tid; p < P; p += kThreads) {
+            st_sum[p] = st_comp[p] = 0.0f;
+            st_cnt[p] = st_cnt[P + p] = st_cnt[2 * P + p] = 0u;
+            st_max[p] = 0.0f;
+        }
+    }
+    if (tid == 0) {
+        const uint32_t arrivals = static_cast<uint32_t>(min(P * S::kPieces, kThreads) + 1);
+        for (int st = 0; st < kStages; ++st) mbar_init(&bars[st], arrivals);
+    }
+    __syncthreads();
+    for (int st = 0; st < kStages; ++st) {
+        const int64_t c = blockIdx.x + st * G;
+        if (c < C)
+            prefetch<Geo>(tab, P, c, (c + 1) * kChunk <= n, theta, &bars[st],
+                     st_rec + st * P * kRecordBytes, st_theta + st * kChunk, tid);
+    }
+    float sc_cur = my_peer < P ? __ldcs(tab.scale[my_peer] + blockIdx.x) : 0.0f;
+
+    bool bad = false;
+    bool aborted = false;
+    int it = 0;
+    int64_t c = blockIdx.x;
+    for (; c < C; c += G, ++it) {
+        const int st = it % kStages;
+        const uint32_t parity = static_cast<uint32_t>(it / kStages) & 1u;
+        const uint8_t* rec = st_rec + st * P * kRecordBytes;
+        const int64_t base = c * kChunk;
+        const bool full = base + kChunk <= n;
+        const int valid = full ? kChunk : static_cast<int>(n - base);
+
+        const bool timed_out = !mbar_wait(&bars[st], parity);
+        float4 th[kVec];
+        if (theta != nullptr && full) {
+#pragma unroll
+            for (int v = 0; v < kVec; ++v)
+                th[v] = *reinterpret_cast<const float4*>(
+                    &st_theta[st * kChunk + slice0 + 128 * v + 4 * lane]);
+        }
+        float sc_next = 0.0f;
+
+        for (int g0 = 0; g0 < P; g0 += kGroup) {
+            const int gn = P - g0 < kGroup ? P - g0 : kGroup;
+            // ---- unpack: one warp per peer --------------------------------------------
+            for (int g = warp; g < gn; g += kWarps) {
+                const int p = g0 + g;
+                const uint32_t* words = reinterpret_cast<const uint32_t*>(rec + p * kRecordBytes);
+                // entry lane + 32 m of the record, m = 0 .. k/32 - 1
+                uint32_t f[kPerLane], ix[kPerLane];
+#pragma unroll
+                for (int m = 0; m < kPerLane; ++m) {
+                    f[m] = record_field_fs<Geo::kFieldBits>(words, lane + 32 * m);
+                    ix[m] = f[m] >> 2;
+                }
+                // indices strictly ascending: each entry below the next one
+                bool asc = true;
+#pragma unroll
+                for (int m = 0; m < kPerLane; ++m) {
+                    uint32_t next = __shfl_down_sync(0xffffffffu, ix[m], 1);
+                    if (m + 1 < kPerLane) {
+                        const uint32_t first = __shfl_sync(0xffffffffu, ix[m + 1 < kPerLane ? m + 1 : m], 0);
+                        if (lane == 31) next = first;
+                        asc = asc && ix[m] < next;
+                    } else {
+                        asc = asc && (lane == 31 || ix[m] < next);
+                    }
+                }
+                const float s = __shfl_sync(0xffffffffu, sc_cur, p >> 3);
+                const bool ok = __all_sync(0xffffffffu, asc) && s >= 0.0f && s <= FLT_MAX;
+                if (ok) {
+                    uint2* eg = ent + g * kTopK;
+#pragma unroll
+                    for (int m = 0; m < kPerLane; ++m)
+                        eg[lane + 32 * m] = make_uint2(ix[m], __float_as_uint(level_value(f[m] & 3u, s)));
+                    if (kStats) {
+                        uint32_t nbig = 0, nneg = 0;
+#pragma unroll
+                        for (int m = 0; m < kPerLane; ++m) {
+                            nbig += __popc(__ballot_sync(0xffffffffu, f[m] & 1u));
+                            nneg += __popc(__ballot_sync(0xffffffffu, f[m] & 2u));
+                        }
+                        if (lane == 0) sgrp[g] = make_uint2(__float_as_uint(s), nbig | nneg << 8);
+                    }
+                } else {
+                    bad = true;
+                }
+                if (lane == 0) okp[g] = ok ? 1u : 0u;
+            }
+            const bool last = g0 + kGroup >= P;
+            if (last) {
+                if (__syncthreads_or(timed_out)) {
+                    aborted = true;
+                    break;
+                }
+                // the stage has been read: start chunk c + S G's copies, and c + G's scales
+                const int64_t c2 = c + kStages * G;
+                if (c2 < C)
+                    prefetch<Geo>(tab, P, c2, (c2 + 1) * kChunk <= n, theta, &bars[st],
+                             st_rec + st * P * kRecordBytes, st_theta + st * kChunk, tid);
+                if (my_peer < P && c + G < C) sc_next = __ldcs(tab.scale[my_peer] + c + G);
+            } else {
+                __syncthreads();
+            }
+            // ---- the other warps, meanwhile: per-peer statistics, one record per thread ----
+            // (a group holds at most 64 peers; peer p is always thread 32 + p mod 64)
+            if (kStats && tid >= 32 && tid - 32 < gn) {
+                const int g = tid - 32;
+                const int p = g0 + g;
+                if (okp[g] == 0u) {
+                    st_cnt[p] += 1u;
+                } else {
+                    const uint2 sg = sgrp[g];
+                    const float s = __uint_as_float(sg.x);
+                    const uint32_t nbig = sg.y & 0xffu;
+                    const uint32_t nneg = sg.y >> 8;
+                    const float lo = level_value(0u, s);
+                    const float hi = level_value(1u, s);
+                    // every entry decodes to +-RN(0.5 s) or +-RN(1.5 s): the record's sum of
+                    // squares from the two counts, in fp32 (fp64 is scarce on this GPU), added
+                    // to the CTA's total with Kahan compensation
+                    const float t = __fmaf_rn(__fmul_rn(hi, hi), static_cast<float>(nbig),
+                                              __fmul_rn(__fmul_rn(lo, lo),
+                                                        static_cast<float>(kTopK - nbig)));
+                    const float y = __fsub_rn(t, st_comp[p]);
+                    const float z = __fadd_rn(st_sum[p], y);
+                    st_comp[p] = __fsub_rn(__fsub_rn(z, st_sum[p]), y);
+                    st_sum[p] = z;
+                    st_cnt[P + p] += nbig;
+                    st_cnt[2 * P + p] += nneg;
+                    st_max[p] = fmaxf(st_max[p], s);
+                }
+            }
+            // ---- one warp: add the peers in order, k/32 entries per lane ------------------
+            if (warp == 0) {
+                uint2 en[kPerLane];
+#pragma unroll
+                for (int m = 0; m < kPerLane; ++m) en[m] = ent[lane + 32 * m];
+                uint32_t okn = okp[0];
+                for (int g = 0; g < gn; ++g) {
+                    uint2 e[kPerLane];
+#pragma unroll
+                    for (int m = 0; m < kPerLane; ++m) e[m] = en[m];
+                    const uint32_t ok = okn;
+                    if (g + 1 < gn) {
+#pragma unroll
+                        for (int m = 0; m < kPerLane; ++m) en[m] = ent[(g + 1) * kTopK + lane + 32 * m];
+                        okn = okp[g + 1];
+                    }
+                    if (ok != 0u) {
+#pragma unroll
+                        for (int m = 0; m < kPerLane; ++m)
+                            acc[e[m].x] = __fadd_rn(acc[e[m].x], __uint_as_float(e[m].y));
+                    }
+                    __syncwarp();
+                }
+            }
+            __syncthreads();   // the accumulator is complete; entries are rewritten next pass
+        }
+        if (aborted) break;
+        sc_cur = sc_next;
+
+        // ---- dense pass: mean, outer step --------------------------------------------------
+#pragma unroll
+        for (int v = 0; v < kVec; ++v) {
+            const int j0 = slice0 + 128 * v + 4 * lane;
+            float4 m4 = *reinterpret_cast<const float4*>(&acc[j0]);
+            *reinterpret_cast<float4*>(&acc[j0]) = make_float4(0.f, 0.f, 0.f, 0.f);
+            m4.x = div_rn(m4.x, pf, rp);
+            m4.y = div_rn(m4.y, pf, rp);
+            m4.z = div_rn(m4.z, pf, rp);
+            m4.w = div_rn(m4.w, pf, rp);
+            if (full) {
+                st_stream_f4(mean + base + j0, m4);
+                if (theta != nullptr) {
+                    float4 t4 = th[v];
+                    t4.x = __fmaf_rn(neg_lr, m4.x, t4.x);
+                    t4.y = __fmaf_rn(neg_lr, m4.y, t4.y);
+                    t4.z = __fmaf_rn(neg_lr, m4.z, t4.z);
+                    t4.w = __fmaf_rn(neg_lr, m4.w, t4.w);
+                    st_stream_f4(theta + base + j0, t4);
+                }
+            } else {
+                const float m[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int j = j0 + u;
+                    if (j < valid) {
+                        mean[base + j] = m[u];
+                        if (theta != nullptr)
+                            theta[base + j] = __fmaf_rn(neg_lr, m[u], theta[base + j]);
+                    }
+                }
+            }
+        }
+    }
+    if (aborted && tid == 0) {
+        // copies still in flight may land late: wait for them (bounded) before the CTA's
+        // shared memory is released: the stage that timed out and any armed after it
+        for (int k = 0; k < kStages; ++k) {
+            const int it2 = it + k;
+            if (c + k * G < C) mbar_wait(&bars[it2 % kStages], static_cast<uint32_t>(it2 / kStages) & 1u);
+        }
+    }
+    if constexpr (kStats) {
+        __syncthreads();
+        for (int p = tid; p < P; p += kThreads) {
+            PeerStats* o = stats + p;
+            if (st_cnt[p]) atomicAdd(&o->rejected, st_cnt[p]);
+            if (st_cnt[P + p]) atomicAdd(&o->big, st_cnt[P + p]);
+            if (st_cnt[2 * P + p]) atomicAdd(&o->negative, st_cnt[2 * P + p]);
+            if (st_max[p] > 0.0f)   // non-negative floats order like their bit patterns
+                atomicMax(reinterpret_cast<unsigned int*>(&o->max_scale), __float_as_uint(st_max[p]));
+            if (st_sum[p] != 0.0f)
+                atomicAdd(&o->sumsq, static_cast<double>(st_sum[p]) - static_cast<double>(st_comp[p]));
+        }
+    }
+    if (flags != nullptr) {
+        if (bad && lane == 0) atomicOr(flags, kFlagBadRecord);
+        if (aborted && tid == 0) atomicOr(flags, kFlagTimeout);
+    }
+}
+
+template <class Geo, bool kStats>
+cudaError_t launch_decode(const DecodeTable& tab, int P, int64_t n, float* mean, float* theta,
+                          float lr, PeerStats* stats, uint32_t* flags, cudaStream_t stream) {
+    const int64_t C = (n + Geo::kChunk - 1) / Geo::kChunk;
+    if (C == 0) return cudaSuccess;
+    const size_t smem = Layout<Geo>(P, kStats).total;
+    const void* kern = reinterpret_cast<const void*>(&k_decode_aggregate<Geo, kStats>);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const int resident = persistent_grid(kern, kThreads, smem);
+    if (resident <= 0) return cudaErrorInvalidConfiguration;
+    const int grid = static_cast<int>(C < resident ? C : resident);
+    const float rp = 1.0f / static_cast<float>(P);   // correctly rounded on the host
+    k_decode_aggregate<Geo, kStats><<<grid, kThreads, smem, stream>>>(tab, P, rp, n, mean, theta,
+                                                                      -lr, stats, flags);
+    return cudaGetLastError();
+}
+
+// Launch for one record geometry, with or without statistics.
+template <class Geo>
+cudaError_t launch_geometry(const DecodeTable& tab, int P, int64_t n, float* mean, float* theta,
+                            float lr, PeerStats* stats, uint32_t* flags, cudaStream_t stream) {
+    return stats != nullptr
+               ? launch_decode<Geo, true>(tab, P, n, mean, theta, lr, stats, flags, stream)
+               : launch_decode<Geo, false>(tab, P, n, mean, theta, lr, stats, flags, stream);
+}
+
+}  // namespace
+}  // namespace spl

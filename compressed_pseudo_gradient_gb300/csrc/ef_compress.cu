@@ -1,545 +1,16 @@
-// Fused sender kernel of the SparseLoCo codec: error feedback, chunk top-64, 2-bit quantise,
-// 14-bit field packing and the error-feedback residual, in one pass over HBM.
-//
-// Method: "The Sparse Frontier: SparseLoCo and the Compression Math Behind Permissionless
-// Pre-Training", "SparseLoCo: Three Compression Levers in One Pass" (items 1-3, per-chunk
-// equation) and "Why Extreme Sparsity Doesn't Break Convergence" ("Error feedback
-// accumulation": what is not sent stays in the buffer for the next round).
-//
-// Design (HBM-bound: 8 B read + 4 B written per fp32 value, 116 B written per chunk):
-//   - one 256-thread CTA per 4096-value chunk, grid-stride over chunks with a persistent grid
-//     (SMs x resident CTAs); while a chunk is worked on, the next chunk's error buffer and
-//     delta fly into a shared-memory stage as two 1-D bulk copies (TMA, no multicast, no
-//     cluster) completing on an mbarrier, whose wait is bounded in time;
-//   - each thread takes 16 values from the stage into registers (four 16-byte vectors at
-//     chunk offsets v*1024 + 4*tid), forms a = fma(beta, e, delta) and the 31-bit magnitude
-//     keys, and keeps them there for the whole chunk; the error buffer is written back once,
-//     from registers, with streaming stores;
-//   - the 64th-largest key is found by a radix select: shared-memory histograms of key bits
-//     [30:20], then [19:9] and [8:0] restricted to the keys matching the digits found so far,
-//     stopping as soon as the boundary bin is taken whole; ties at the final threshold go to
-//     the lowest indices; the chosen positions end up in a 4096-bit shared bitmap;
-//   - one warp turns the bitmap into per-word prefix counts, from which every thread that
-//     owns a chosen value knows its rank in ascending index order; it computes the code and
-//     the residual in registers and writes its 14-bit field to shared memory; one warp then
-//     assembles the 112-byte record (28 words) and stores it as seven 16-byte vectors.
-#include "spl_device.cuh"
-#include "spl_kernels.h"
+// Sender launches for the default codec (4096-value chunks, k = 64, max-abs scale), and the
+// dispatch of every other codec to ef_compress_variants.cu.
+#include "ef_compress.cuh"
 
 namespace spl {
-namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kPer = kChunk / kThreads;    // 16 values per thread
-constexpr int kVec = kPer / 4;             // 4 vectors of 4 per thread
-constexpr int kBitmapWords = kChunk / 32;  // 128
-constexpr uint32_t kWindow = (2048u << 16) - 1u;   // 16 octaves of magnitude keys: 2048 bins
-constexpr uint32_t kNotFound = 0xffffffffu;
-
-struct Smem {
-    float stage_e[kChunk];          // prefetched error-buffer chunk (bulk copy)
-    uint32_t stage_d[kChunk];       // prefetched delta chunk: fp32, or bf16 in the first half
-    uint32_t hist[2048];            // histogram bins (one select pass at a time)
-    uint32_t sel_bm[kBitmapWords];  // chosen positions (complete once the select is done)
-    uint32_t eq_bm[kBitmapWords];   // ties at the final threshold (many-candidate path)
-    uint32_t warp_tot[kWarps];
-    uint32_t warp_max[kWarps];
-    uint32_t bcast[3];              // digit, count above the digit's bin, count in the bin
-    uint2 cand[32];                 // (key, index) of the keys in the boundary bin
-    uint32_t ncand;
-    uint16_t fields[kTopK];         // the record's 64 fields, in ascending index order
-    alignas(16) uint16_t pre[kBitmapWords];   // chosen positions before each bitmap word
-    uint64_t bar;                   // completes when the stage's bulk copies have landed
-};
-
-// Block-wide search of the bin holding the need-th largest key (counting from the top bin).
-// Thread t owns bins [kBinsPer*t, kBinsPer*t + kBinsPer).  Writes sm.bcast; the caller
-// synchronises before reading it.
-template <int kBins>
-__device__ __forceinline__ void find_digit(Smem& sm, const uint32_t* hist, uint32_t need,
-                                           int tid, int lane, int warp) {
-    constexpr int kBinsPer = kBins / kThreads;
-    uint32_t h[kBinsPer];
-    uint32_t sum = 0;
-#pragma unroll
-    for (int i = 0; i < kBinsPer; ++i) {
-        h[i] = hist[kBinsPer * tid + i];
-        sum += h[i];
-    }
-    uint32_t incl = sum;   // suffix sum over lanes >= lane
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_down_sync(0xffffffffu, incl, o);
-        if (lane + o < 32) incl += y;
-    }
-    if (lane == 0) sm.warp_tot[warp] = incl;
-    __syncthreads();
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w)
-        if (w > warp) incl += sm.warp_tot[w];
-    const uint32_t excl = incl - sum;
-    if (excl < need && incl >= need) {
-        uint32_t run = excl;
-#pragma unroll
-        for (int i = kBinsPer - 1; i >= 0; --i) {
-            if (run + h[i] >= need) {
-                sm.bcast[0] = kBinsPer * tid + i;
-                sm.bcast[1] = run;
-                sm.bcast[2] = h[i];
-                break;
-            }
-            run += h[i];
-        }
-    }
-}
-
-// The chunk a CTA works on: its tensor's pointers advanced to the chunk, and its extent.
-struct ChunkRef {
-    const void* delta;
-    float* ef;
-    int valid;
-    bool full;
-};
-
-template <bool kBf16>
-__device__ __forceinline__ ChunkRef locate(const CompressTable& tab, int64_t c) {
-    int t = 0;
-    int hi = tab.num;
-    while (hi - t > 1) {
-        const int mid = (t + hi) >> 1;
-        if (tab.chunk_begin[mid] <= c) t = mid; else hi = mid;
-    }
-    const int64_t base = (c - tab.chunk_begin[t]) * kChunk;
-    const int64_t n = tab.n[t];
-    ChunkRef r;
-    r.ef = tab.ef[t] + base;
-    r.delta = kBf16
-        ? static_cast<const void*>(static_cast<const uint16_t*>(tab.delta[t]) + base)
-        : static_cast<const void*>(static_cast<const float*>(tab.delta[t]) + base);
-    r.full = base + kChunk <= n;
-    r.valid = r.full ? kChunk : static_cast<int>(n - base);
-    return r;
-}
-
-// One thread: start the bulk copies of a full chunk's error buffer and delta into the stage.
-// With the error buffer in host memory (kEfHost) only delta is staged: the buffer is read and
-// written over the host link with plain 16-byte accesses.
-template <bool kBf16, bool kEfHost>
-__device__ __forceinline__ void prefetch(Smem& sm, const ChunkRef& r) {
-    constexpr uint32_t kDeltaBytes = kChunk * (kBf16 ? 2 : 4);
-    fence_async_smem();
-    mbar_expect_tx(&sm.bar, (kEfHost ? 0u : kChunk * 4u) + kDeltaBytes);
-    if constexpr (!kEfHost) bulk_load(sm.stage_e, r.ef, kChunk * 4, &sm.bar);
-    bulk_load(sm.stage_d, r.delta, kDeltaBytes, &sm.bar);
-}
-
-// a = fmaf(beta, e, delta) for this thread's 16 values, from the stage (full chunks); with
-// the error buffer in host memory, e comes straight from there.
-template <bool kBf16, bool kEfHost>
-__device__ __forceinline__ void accumulate_from_stage(const Smem& sm, const ChunkRef& r,
-                                                      float beta, int tid, float (&a)[kPer]) {
-    float4 eh[kVec];
-    if constexpr (kEfHost) {
-#pragma unroll
-        for (int v = 0; v < kVec; ++v) eh[v] = ld_stream_f4(r.ef + v * 1024 + 4 * tid);
-    }
-#pragma unroll
-    for (int v = 0; v < kVec; ++v) {
-        const int j0 = v * 1024 + 4 * tid;
-        const float4 e4 = kEfHost ? eh[v] : *reinterpret_cast<const float4*>(&sm.stage_e[j0]);
-        float d[4];
-        if constexpr (kBf16) {
-            const uint2 d2 = *reinterpret_cast<const uint2*>(
-                reinterpret_cast<const uint16_t*>(sm.stage_d) + j0);
-            d[0] = bf16_bits_to_float(d2.x & 0xffffu);
-            d[1] = bf16_bits_to_float(d2.x >> 16);
-            d[2] = bf16_bits_to_float(d2.y & 0xffffu);
-            d[3] = bf16_bits_to_float(d2.y >> 16);
-        } else {
-            const float4 d4 = *reinterpret_cast<const float4*>(&sm.stage_d[j0]);
-            d[0] = d4.x; d[1] = d4.y; d[2] = d4.z; d[3] = d4.w;
-        }
-        a[4 * v + 0] = __fmaf_rn(beta, e4.x, d[0]);
-        a[4 * v + 1] = __fmaf_rn(beta, e4.y, d[1]);
-        a[4 * v + 2] = __fmaf_rn(beta, e4.z, d[2]);
-        a[4 * v + 3] = __fmaf_rn(beta, e4.w, d[3]);
-    }
-}
-
-// The same for a tail chunk, straight from global memory; pads are +0.
-template <bool kBf16>
-__device__ __forceinline__ void accumulate_tail(const ChunkRef& r, float beta, int tid,
-                                                float (&a)[kPer]) {
-#pragma unroll
-    for (int v = 0; v < kVec; ++v)
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int j = v * 1024 + 4 * tid + u;
-            float d = 0.0f, e = 0.0f;
-            if (j < r.valid) {
-                e = r.ef[j];
-                d = kBf16 ? bf16_bits_to_float(static_cast<const uint16_t*>(r.delta)[j])
-                          : static_cast<const float*>(r.delta)[j];
-            }
-            a[4 * v + u] = j < r.valid ? __fmaf_rn(beta, e, d) : 0.0f;
-        }
-}
-
-// Generic select (any data): radix passes on key bits [30:20], [19:9] and [8:0], each over
-// the keys matching the digits found so far, stopping once the boundary bin is taken whole;
-// ties at the final threshold go to the lowest indices.  Marks the 64 chosen positions in
-// sm.sel_bm.  Entered by all threads with sm.sel_bm/eq_bm cleared; clears hist itself.
-__device__ __noinline__ void generic_select(Smem& sm, const uint32_t (&key)[kPer], int tid,
-                                               int lane, int warp) {
-    {
-        uint4* h4 = reinterpret_cast<uint4*>(&sm.hist[0]);
-        h4[tid] = make_uint4(0, 0, 0, 0);
-        h4[tid + kThreads] = make_uint4(0, 0, 0, 0);
-    }
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) atomicAdd(&sm.hist[key[i] >> 20], 1u);
-    __syncthreads();
-    find_digit<2048>(sm, sm.hist, kTopK, tid, lane, warp);
-    __syncthreads();
-    uint32_t need = kTopK - sm.bcast[1];      // keys still to take from bin D
-    const uint32_t dig = sm.bcast[0];
-    const uint32_t in_bin = sm.bcast[2];
-
-    if (in_bin == need) {
-        // ---- bin D is taken whole: every key at or above it is in -------------------
-#pragma unroll
-        for (int v = 0; v < kVec; ++v)
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int j = v * 1024 + 4 * tid + u;
-                if ((key[4 * v + u] >> 20) >= dig) atomicOr(&sm.sel_bm[j >> 5], 1u << (j & 31));
-            }
-        __syncthreads();
-    } else {
-        // ---- resolve bin D: radix passes on key bits [19:9] and [8:0] ---------------
-        uint32_t prefix = dig << 20;
-        uint32_t pmask = 0x7ffu << 20;
-        {   // the first pass's bins have been read: clear them for the second pass
-            uint4* h4 = reinterpret_cast<uint4*>(&sm.hist[0]);
-            h4[tid] = make_uint4(0, 0, 0, 0);
-            h4[tid + kThreads] = make_uint4(0, 0, 0, 0);
-        }
-        __syncthreads();
-#pragma unroll
-        for (int i = 0; i < kPer; ++i)
-            if ((key[i] & pmask) == prefix) atomicAdd(&sm.hist[(key[i] >> 9) & 0x7ffu], 1u);
-        __syncthreads();
-        find_digit<2048>(sm, sm.hist, need, tid, lane, warp);
-        __syncthreads();
-        need -= sm.bcast[1];
-        prefix |= sm.bcast[0] << 9;
-        pmask |= 0x7ffu << 9;
-        if (sm.bcast[2] != need) {
-            sm.hist[tid] = 0;                 // the second pass's bins have been read
-            sm.hist[tid + kThreads] = 0;
-            __syncthreads();
-#pragma unroll
-            for (int i = 0; i < kPer; ++i)
-                if ((key[i] & pmask) == prefix) atomicAdd(&sm.hist[key[i] & 0x1ffu], 1u);
-            __syncthreads();
-            find_digit<512>(sm, sm.hist, need, tid, lane, warp);
-            __syncthreads();
-            need -= sm.bcast[1];
-            prefix |= sm.bcast[0];
-            pmask = 0x7fffffffu;
-        }
-        // keys above the final prefix are in; ties at it go by index, lowest first
-#pragma unroll
-        for (int v = 0; v < kVec; ++v)
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const uint32_t mk = key[4 * v + u] & pmask;
-                const int j = v * 1024 + 4 * tid + u;
-                if (mk > prefix) atomicOr(&sm.sel_bm[j >> 5], 1u << (j & 31));
-                else if (mk == prefix) atomicOr(&sm.eq_bm[j >> 5], 1u << (j & 31));
-            }
-        __syncthreads();
-        if (warp == 0) {
-            uint32_t eqw[4];
-            uint32_t cnt = 0;
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-                eqw[qq] = sm.eq_bm[4 * lane + qq];
-                cnt += __popc(eqw[qq]);
-            }
-            uint32_t incl = cnt;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            const uint32_t before = incl - cnt;
-            uint32_t take = need > before ? min(need - before, cnt) : 0u;
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-                uint32_t w = eqw[qq];
-                uint32_t kept = 0;
-                while (take != 0u && w != 0u) {
-                    const uint32_t low = w & (0u - w);
-                    kept |= low;
-                    w ^= low;
-                    --take;
-                }
-                sm.sel_bm[4 * lane + qq] |= kept;
-            }
-        }
-        __syncthreads();
-    }
-}
-
-#ifndef SPL_COMPRESS_MIN_BLOCKS
-#define SPL_COMPRESS_MIN_BLOCKS 4
-#endif
-
-template <bool kBf16, bool kEfHost>
-__global__ void __launch_bounds__(kThreads, SPL_COMPRESS_MIN_BLOCKS)
-k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload,
-              float* __restrict__ scales, uint32_t* __restrict__ flags) {
-    extern __shared__ __align__(128) unsigned char smem_raw[];
-    Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
-    const int tid = threadIdx.x;
-    const int lane = tid & 31;
-    const int warp = tid >> 5;
-    const int64_t total = tab.chunk_begin[tab.num];
-    if (static_cast<int64_t>(blockIdx.x) >= total) return;
-
-    if (tid == 0) {
-        mbar_init(&sm.bar, 1);
-        const ChunkRef r0 = locate<kBf16>(tab, blockIdx.x);
-        if (r0.full) prefetch<kBf16, kEfHost>(sm, r0);
-    }
-    __syncthreads();
-
-    uint32_t parity = 0;
-    bool nonfinite = false;
-    bool aborted = false;
-
-    for (int64_t c = blockIdx.x; c < total; c += gridDim.x) {
-        const ChunkRef r = locate<kBf16>(tab, c);
-
-        // ---- a = beta * e + delta (from the prefetched stage), and the magnitude keys -----
-        float a[kPer];
-        bool timed_out = false;
-        if (r.full) {
-            timed_out = !mbar_wait(&sm.bar, parity);
-            parity ^= 1u;
-            accumulate_from_stage<kBf16, kEfHost>(sm, r, beta, tid, a);
-        } else {
-            accumulate_tail<kBf16>(r, beta, tid, a);
-        }
-        uint32_t key[kPer];
-        uint32_t kmax = 0;
-#pragma unroll
-        for (int i = 0; i < kPer; ++i) {
-            key[i] = mag_key(a[i]);
-            kmax = max(kmax, key[i]);
-        }
-        nonfinite |= kmax >= kKeyInf;
-
-        // ---- clear the histograms and bitmaps; chunk max --------------------------------
-        {
-            uint4* h4 = reinterpret_cast<uint4*>(&sm.hist[0]);
-            const uint4 z = make_uint4(0, 0, 0, 0);
-            h4[tid] = z;                      // 2048 words
-            h4[tid + kThreads] = z;
-            if (tid < kBitmapWords) sm.sel_bm[tid] = 0;
-            else sm.eq_bm[tid - kBitmapWords] = 0;
-            if (tid == 0) {
-                sm.ncand = 0;
-                sm.bcast[0] = kNotFound;
-            }
-            kmax = __reduce_max_sync(0xffffffffu, kmax);
-            if (lane == 0) sm.warp_max[warp] = kmax;
-        }
-        if (__syncthreads_or(timed_out)) {
-            aborted = true;
-            break;
-        }
-        // the stage has been read by every thread: start the next chunk's copies
-        if (tid == 0 && c + gridDim.x < total) {
-            const ChunkRef rn = locate<kBf16>(tab, c + gridDim.x);
-            if (rn.full) prefetch<kBf16, kEfHost>(sm, rn);
-        }
-        uint32_t mkey = 0;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) mkey = max(mkey, sm.warp_max[w]);
-
-        // ---- select, fast path: 2048 bins of 1/128 octave over the 16 octaves below the
-        //      largest key; the 64th key almost always falls inside, and its bin holds only a
-        //      few keys, which warp 0 ranks directly.  Otherwise: the generic radix select.
-        //      (A narrower first window does not pay: with ~10 % of the keys inside it, nearly
-        //      every warp still has a lane that takes the in-window path.)
-        // lo_key puts the largest key exactly in the top bin, so no key needs clamping
-        const bool windowed = mkey < kKeyInf;
-        const uint32_t lo_key = mkey > kWindow ? mkey - kWindow : 0u;
-        if (windowed) {
-#pragma unroll
-            for (int i = 0; i < kPer; ++i)
-                if (key[i] >= lo_key) atomicAdd(&sm.hist[(key[i] - lo_key) >> 16], 1u);
-        }
-        __syncthreads();
-        if (windowed) find_digit<2048>(sm, sm.hist, kTopK, tid, lane, warp);
-        __syncthreads();
-        bool selected = false;
-        if (windowed && sm.bcast[0] != kNotFound) {
-            const uint32_t need = kTopK - sm.bcast[1];
-            const uint32_t dig = sm.bcast[0];
-            const uint32_t in_bin = sm.bcast[2];
-            if (in_bin == need || in_bin <= 32u) {
-                const bool rank_bin = in_bin != need;
-                // bin D as a key range [k_lo, k_hi): keys at or above k_hi are in, keys in the
-                // range are in when the bin is taken whole, else they are the candidates
-                const uint32_t k_lo = lo_key + (dig << 16);
-                const uint32_t k_hi = k_lo + (1u << 16);
-                const uint32_t k_in = rank_bin ? k_hi : k_lo;
-#pragma unroll
-                for (int v = 0; v < kVec; ++v)
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const uint32_t kk = key[4 * v + u];
-                        const int j = v * 1024 + 4 * tid + u;
-                        if (kk >= k_in) {
-                            atomicOr(&sm.sel_bm[j >> 5], 1u << (j & 31));
-                        } else if (kk >= k_lo) {
-                            const uint32_t slot = atomicAdd(&sm.ncand, 1u);
-                            if (slot < 32u) sm.cand[slot] = make_uint2(kk, static_cast<uint32_t>(j));
-                        }
-                    }
-                __syncthreads();
-                if (rank_bin && warp == 0) {
-                    const uint2 me = static_cast<uint32_t>(lane) < in_bin ? sm.cand[lane] : make_uint2(0u, 0u);
-                    uint32_t rank = 0;
-                    for (uint32_t o = 0; o < in_bin; ++o) {
-                        const uint32_t ok = __shfl_sync(0xffffffffu, me.x, o);
-                        const uint32_t oj = __shfl_sync(0xffffffffu, me.y, o);
-                        rank += (ok > me.x || (ok == me.x && oj < me.y)) ? 1u : 0u;
-                    }
-                    if (static_cast<uint32_t>(lane) < in_bin && rank < need)
-                        atomicOr(&sm.sel_bm[me.y >> 5], 1u << (me.y & 31));
-                    __syncwarp();
-                }
-                selected = true;
-            }
-        }
-        if (!selected) generic_select(sm, key, tid, lane, warp);
-
-        // ---- warp 0: chosen positions before each bitmap word ----------------------------
-        if (warp == 0) {
-            const uint4 w4 = *reinterpret_cast<const uint4*>(&sm.sel_bm[4 * lane]);
-            const uint32_t c0 = __popc(w4.x), c1 = __popc(w4.y), c2 = __popc(w4.z);
-            const uint32_t mine = c0 + c1 + c2 + __popc(w4.w);
-            uint32_t incl = mine;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            const uint32_t p0 = incl - mine;
-            *reinterpret_cast<uint2*>(&sm.pre[4 * lane]) =
-                make_uint2(p0 | ((p0 + c0) << 16), (p0 + c0 + c1) | ((p0 + c0 + c1 + c2) << 16));
-        }
-        __syncthreads();
-
-        // ---- owners: rank, code and residual of each chosen value ------------------------
-        const float s = __fdiv_rn(__uint_as_float(mkey), 1.5f);
-#pragma unroll
-        for (int v = 0; v < kVec; ++v) {
-            const int j0 = v * 1024 + 4 * tid;
-            const uint32_t word = sm.sel_bm[j0 >> 5];
-            const int sh = j0 & 31;
-            if (((word >> sh) & 0xfu) == 0u) continue;
-            const uint32_t base_rank = sm.pre[j0 >> 5];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                if ((word >> (sh + u)) & 1u) {
-                    const uint32_t rank = base_rank + __popc(word & ((1u << (sh + u)) - 1u));
-                    const uint32_t code = quant_code(a[4 * v + u], s);
-                    a[4 * v + u] = __fsub_rn(a[4 * v + u], level_value(code, s));
-                    if (rank < kTopK)
-                        sm.fields[rank] = static_cast<uint16_t>(code | (static_cast<uint32_t>(j0 + u) << 2));
-                }
-            }
-        }
-        if (r.full) {
-#pragma unroll
-            for (int v = 0; v < kVec; ++v)
-                st_stream_f4(r.ef + v * 1024 + 4 * tid,
-                             make_float4(a[4 * v], a[4 * v + 1], a[4 * v + 2], a[4 * v + 3]));
-        } else {
-#pragma unroll
-            for (int v = 0; v < kVec; ++v)
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int j = v * 1024 + 4 * tid + u;
-                    if (j < r.valid) r.ef[j] = a[4 * v + u];
-                }
-        }
-        __syncthreads();
-
-        // ---- one warp: pack the record and write the scale ------------------------------
-        if (warp == 0) {
-            const int w = lane < kRecordWords ? lane : kRecordWords - 1;
-            const int r_first = (32 * w) / kFieldBits;
-            const int r_last = (32 * w + 31) / kFieldBits;
-            uint32_t word = 0;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int r = r_first + k;
-                if (r <= r_last) {
-                    const uint32_t f = sm.fields[r];
-                    const int off = kFieldBits * r - 32 * w;
-                    word |= off >= 0 ? (f << off) : (f >> (-off));
-                }
-            }
-            store_record(payload + c * kRecordBytes, word, lane);
-            if (lane == 0) scales[c] = s;
-        }
-    }
-    if (aborted && tid == 0) {
-        // the copy that did not complete may still land: wait once more (bounded) before
-        // the CTA's shared memory is released
-        mbar_wait(&sm.bar, parity ^ 1u);
-    }
-    if (flags != nullptr) {
-        if (nonfinite) atomicOr(flags, kFlagNonFinite);
-        if (aborted && tid == 0) atomicOr(flags, kFlagTimeout);
-    }
-}
-
-template <bool kBf16, bool kEfHost>
-cudaError_t launch_variant(const CompressTable& tab, int64_t total, float beta, uint8_t* payload,
-                           float* scales, uint32_t* flags, cudaStream_t stream) {
-    const void* kern = reinterpret_cast<const void*>(&k_ef_compress<kBf16, kEfHost>);
-    const size_t smem = sizeof(Smem);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    const int resident = persistent_grid(kern, kThreads, smem);
-    if (resident <= 0) return cudaErrorInvalidConfiguration;
-    const int grid = static_cast<int>(total < resident ? total : resident);
-    k_ef_compress<kBf16, kEfHost><<<grid, kThreads, smem, stream>>>(tab, beta, payload, scales, flags);
-    return cudaGetLastError();
-}
-
-}  // namespace
-
-cudaError_t launch_ef_compress(const CompressTable& tab, bool bf16, bool ef_host, float beta,
-                               uint8_t* payload, float* scales, uint32_t* flags,
+cudaError_t launch_ef_compress(const CompressTable& tab, const Codec& cd, bool bf16, bool ef_host,
+                               float beta, uint8_t* payload, float* scales, uint32_t* flags,
                                cudaStream_t stream) {
-    const int64_t total = tab.chunk_begin[tab.num];
-    if (total == 0) return cudaSuccess;
-    if (bf16)
-        return ef_host ? launch_variant<true, true>(tab, total, beta, payload, scales, flags, stream)
-                       : launch_variant<true, false>(tab, total, beta, payload, scales, flags, stream);
-    return ef_host ? launch_variant<false, true>(tab, total, beta, payload, scales, flags, stream)
-                   : launch_variant<false, false>(tab, total, beta, payload, scales, flags, stream);
+    if (is_default_codec(cd))
+        return launch_codec<DefaultGeometry, kScaleMax>(tab, bf16, ef_host, beta, payload, scales,
+                                                        flags, stream);
+    return launch_ef_compress_variant(tab, cd, bf16, ef_host, beta, payload, scales, flags, stream);
 }
 
 }  // namespace spl

@@ -84,11 +84,27 @@ const char* spl_status_string(int status) {
 
 int spl_last_cuda_error(void) { return g_last_cuda_error; }
 
-static spl_status check_tensor(const void* delta, spl_dtype dt, const float* ef, size_t n) {
+// The codec a call names (NULL: the default one).  Returns false for a codec the library has
+// no kernels for.
+static bool resolve_codec(const spl_codec* c, spl::Codec* out) {
+    if (c == nullptr) {
+        *out = spl::Codec{SPL_CHUNK, SPL_TOPK, SPL_SCALE_MAX_ABS};
+        return true;
+    }
+    if (c->chunk > 65536u || c->topk > 65536u || c->scale_rule > 1u) return false;
+    *out = spl::Codec{static_cast<int>(c->chunk), static_cast<int>(c->topk),
+                      static_cast<int>(c->scale_rule)};
+    return spl::codec_record_bytes(*out) != 0;
+}
+
+static size_t chunks_of(size_t n, size_t L) { return n / L + (n % L != 0); }
+
+static spl_status check_tensor(const void* delta, spl_dtype dt, const float* ef, size_t n,
+                               size_t L) {
     if (n == 0) return SPL_OK;
     if (delta == nullptr || ef == nullptr) return SPL_ERR_INVALID_ARG;
     if (dt != SPL_F32 && dt != SPL_BF16) return SPL_ERR_INVALID_ARG;
-    if (spl_num_chunks(n) > kMaxChunks) return SPL_ERR_INVALID_ARG;
+    if (chunks_of(n, L) > kMaxChunks) return SPL_ERR_INVALID_ARG;
     if (!aligned(delta, 16) || !aligned(ef, 16)) return SPL_ERR_ALIGNMENT;
     const size_t esz = dt == SPL_F32 ? 4 : 2;
     if (overlap(delta, n * esz, ef, n * 4)) return SPL_ERR_INVALID_ARG;
@@ -96,17 +112,17 @@ static spl_status check_tensor(const void* delta, spl_dtype dt, const float* ef,
 }
 
 static spl_status check_outputs(const spl_tensor* t, int num, spl_dtype dt, const uint8_t* payload,
-                                const float* scales, const uint32_t* flags, size_t C) {
+                                const float* scales, const uint32_t* flags, size_t C, size_t rb) {
     if (C == 0) return SPL_OK;
     if (payload == nullptr || scales == nullptr) return SPL_ERR_INVALID_ARG;
     if (!aligned(payload, 16) || !aligned(scales, 4) || !aligned(flags, 4))
         return SPL_ERR_ALIGNMENT;
     const size_t esz = dt == SPL_F32 ? 4 : 2;
-    if (overlap(payload, C * SPL_RECORD_BYTES, scales, C * 4)) return SPL_ERR_INVALID_ARG;
+    if (overlap(payload, C * rb, scales, C * 4)) return SPL_ERR_INVALID_ARG;
     for (int i = 0; i < num; ++i) {
         const size_t n = t[i].n;
-        if (overlap(payload, C * SPL_RECORD_BYTES, t[i].delta, n * esz) ||
-            overlap(payload, C * SPL_RECORD_BYTES, t[i].ef, n * 4) ||
+        if (overlap(payload, C * rb, t[i].delta, n * esz) ||
+            overlap(payload, C * rb, t[i].ef, n * 4) ||
             overlap(scales, C * 4, t[i].delta, n * esz) || overlap(scales, C * 4, t[i].ef, n * 4) ||
             overlap(flags, 4, t[i].ef, n * 4) || overlap(flags, 4, t[i].delta, n * esz))
             return SPL_ERR_INVALID_ARG;
@@ -119,20 +135,24 @@ static spl_status check_outputs(const spl_tensor* t, int num, spl_dtype dt, cons
     return SPL_OK;
 }
 
-spl_status spl_ef_compress_multi(const spl_tensor* tensors, int num_tensors, spl_dtype delta_dtype,
-                                 float beta, uint8_t* payload, float* scales, uint32_t* d_flags,
-                                 spl_stream_t stream) {
+static spl_status compress_impl(const spl::Codec& cd, const spl_tensor* tensors, int num_tensors,
+                                spl_dtype delta_dtype, float beta, uint8_t* payload, float* scales,
+                                uint32_t* d_flags, spl_stream_t stream) {
     if (tensors == nullptr || num_tensors < 1) return SPL_ERR_INVALID_ARG;
     if (delta_dtype != SPL_F32 && delta_dtype != SPL_BF16) return SPL_ERR_INVALID_ARG;
     if (!std::isfinite(beta)) return SPL_ERR_INVALID_ARG;
+    const size_t L = static_cast<size_t>(cd.chunk);
+    const size_t rb = static_cast<size_t>(spl::codec_record_bytes(cd));
     size_t C = 0;
     for (int i = 0; i < num_tensors; ++i) {
-        const spl_status st = check_tensor(tensors[i].delta, delta_dtype, tensors[i].ef, tensors[i].n);
+        const spl_status st =
+            check_tensor(tensors[i].delta, delta_dtype, tensors[i].ef, tensors[i].n, L);
         if (st != SPL_OK) return st;
-        C += spl_num_chunks(tensors[i].n);
+        C += chunks_of(tensors[i].n, L);
         if (C > kMaxChunks) return SPL_ERR_INVALID_ARG;
     }
-    const spl_status st = check_outputs(tensors, num_tensors, delta_dtype, payload, scales, d_flags, C);
+    const spl_status st =
+        check_outputs(tensors, num_tensors, delta_dtype, payload, scales, d_flags, C, rb);
     if (st != SPL_OK) return st;
     if (C == 0) return SPL_OK;
     // delta (and a device-resident error buffer) arrive by bulk copies (TMA) into shared
@@ -148,6 +168,7 @@ spl_status spl_ef_compress_multi(const spl_tensor* tensors, int num_tensors, spl
         ef_kind = k;
     }
     const bool ef_host = ef_kind == cudaMemoryTypeHost;
+    if (ef_host && !spl::is_default_codec(cd)) return SPL_ERR_INVALID_ARG;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     size_t chunk0 = 0;
@@ -162,17 +183,46 @@ spl_status spl_ef_compress_multi(const spl_tensor* tensors, int num_tensors, spl
             tab.ef[i] = tensors[first + i].ef;
             tab.n[i] = static_cast<int64_t>(tensors[first + i].n);
             tab.chunk_begin[i] = chunks;
-            chunks += static_cast<int64_t>(spl_num_chunks(tensors[first + i].n));
+            chunks += static_cast<int64_t>(chunks_of(tensors[first + i].n, L));
         }
         tab.chunk_begin[count] = chunks;
         tab.num = count;
         const spl_status ls = cuda_status(spl::launch_ef_compress(
-            tab, delta_dtype == SPL_BF16, ef_host, beta, payload + chunk0 * SPL_RECORD_BYTES,
+            tab, cd, delta_dtype == SPL_BF16, ef_host, beta, payload + chunk0 * rb,
             scales + chunk0, d_flags, s));
         if (ls != SPL_OK) return ls;
         chunk0 += static_cast<size_t>(chunks);
     }
     return SPL_OK;
+}
+
+spl_status spl_ef_compress_multi(const spl_tensor* tensors, int num_tensors, spl_dtype delta_dtype,
+                                 float beta, uint8_t* payload, float* scales, uint32_t* d_flags,
+                                 spl_stream_t stream) {
+    spl::Codec cd;
+    resolve_codec(nullptr, &cd);
+    return compress_impl(cd, tensors, num_tensors, delta_dtype, beta, payload, scales, d_flags,
+                         stream);
+}
+
+spl_status spl_ef_compress_codec(const spl_codec* codec, const spl_tensor* tensors,
+                                 int num_tensors, spl_dtype delta_dtype, float beta,
+                                 uint8_t* payload, float* scales, uint32_t* d_flags,
+                                 spl_stream_t stream) {
+    spl::Codec cd;
+    if (!resolve_codec(codec, &cd)) return SPL_ERR_INVALID_ARG;
+    return compress_impl(cd, tensors, num_tensors, delta_dtype, beta, payload, scales, d_flags,
+                         stream);
+}
+
+int64_t spl_codec_record_bytes(const spl_codec* codec) {
+    spl::Codec cd;
+    return resolve_codec(codec, &cd) ? spl::codec_record_bytes(cd) : -1;
+}
+
+size_t spl_codec_num_chunks(const spl_codec* codec, size_t n) {
+    spl::Codec cd;
+    return resolve_codec(codec, &cd) ? chunks_of(n, static_cast<size_t>(cd.chunk)) : 0;
 }
 
 spl_status spl_ef_compress(const void* delta, spl_dtype delta_dtype, float* ef, size_t n,
@@ -188,14 +238,16 @@ spl_status spl_ef_compress(const void* delta, spl_dtype delta_dtype, float* ef, 
 
 static_assert(sizeof(spl_peer_stats) == sizeof(spl::PeerStats), "spl_peer_stats layout");
 
-static spl_status decode_impl(const uint8_t* const* payloads, const float* const* scales, int P,
-                              size_t n, float* mean_out, float* theta, float lr,
-                              spl_peer_stats* d_stats, uint32_t* d_flags, spl_stream_t stream) {
+static spl_status decode_impl(const spl::Codec& cd, const uint8_t* const* payloads,
+                              const float* const* scales, int P, size_t n, float* mean_out,
+                              float* theta, float lr, spl_peer_stats* d_stats, uint32_t* d_flags,
+                              spl_stream_t stream) {
     if (P < 1 || P > SPL_MAX_PEERS) return SPL_ERR_INVALID_ARG;
     if (theta != nullptr && !std::isfinite(lr)) return SPL_ERR_INVALID_ARG;
     if (n == 0) return SPL_OK;
     if (payloads == nullptr || scales == nullptr || mean_out == nullptr) return SPL_ERR_INVALID_ARG;
-    const size_t C = spl_num_chunks(n);
+    const size_t rb = static_cast<size_t>(spl::codec_record_bytes(cd));
+    const size_t C = chunks_of(n, static_cast<size_t>(cd.chunk));
     if (C > kMaxChunks) return SPL_ERR_INVALID_ARG;
     if (!aligned(mean_out, 16) || !aligned(theta, 16) || !aligned(d_flags, 4))
         return SPL_ERR_ALIGNMENT;
@@ -207,8 +259,8 @@ static spl_status decode_impl(const uint8_t* const* payloads, const float* const
     for (int p = 0; p < P; ++p) {
         if (payloads[p] == nullptr || scales[p] == nullptr) return SPL_ERR_INVALID_ARG;
         if (!aligned(payloads[p], 16) || !aligned(scales[p], 4)) return SPL_ERR_ALIGNMENT;
-        if (overlap(payloads[p], C * SPL_RECORD_BYTES, mean_out, n * 4) ||
-            overlap(payloads[p], C * SPL_RECORD_BYTES, theta, n * 4) ||
+        if (overlap(payloads[p], C * rb, mean_out, n * 4) ||
+            overlap(payloads[p], C * rb, theta, n * 4) ||
             overlap(scales[p], C * 4, mean_out, n * 4) || overlap(scales[p], C * 4, theta, n * 4))
             return SPL_ERR_INVALID_ARG;
         tab.payload[p] = payloads[p];
@@ -219,14 +271,42 @@ static spl_status decode_impl(const uint8_t* const* payloads, const float* const
     // plain stores; those take any memory the device can address)
     if (theta != nullptr && memory_type(theta) != cudaMemoryTypeDevice) return SPL_ERR_INVALID_ARG;
     return cuda_status(spl::launch_decode_aggregate(
-        tab, P, static_cast<int64_t>(n), mean_out, theta, lr,
+        tab, cd, P, static_cast<int64_t>(n), mean_out, theta, lr,
         reinterpret_cast<spl::PeerStats*>(d_stats), d_flags, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 spl_status spl_decode_aggregate(const uint8_t* const* payloads, const float* const* scales, int P,
                                 size_t n, float* mean_out, float* theta, float lr,
                                 uint32_t* d_flags, spl_stream_t stream) {
-    return decode_impl(payloads, scales, P, n, mean_out, theta, lr, nullptr, d_flags, stream);
+    spl::Codec cd;
+    resolve_codec(nullptr, &cd);
+    return decode_impl(cd, payloads, scales, P, n, mean_out, theta, lr, nullptr, d_flags, stream);
+}
+
+// Checks of a statistics array (P entries, 8-byte aligned, apart from the outputs).
+static spl_status check_stats(const spl_peer_stats* d_stats, int P, size_t n,
+                              const float* mean_out, const float* theta, const uint32_t* d_flags) {
+    if (!aligned(d_stats, 8)) return SPL_ERR_ALIGNMENT;
+    const size_t sb = static_cast<size_t>(P) * sizeof(spl_peer_stats);
+    if (overlap(d_stats, sb, mean_out, n * 4) || overlap(d_stats, sb, theta, n * 4) ||
+        overlap(d_stats, sb, d_flags, 4))
+        return SPL_ERR_INVALID_ARG;
+    return SPL_OK;
+}
+
+spl_status spl_decode_aggregate_codec(const spl_codec* codec, const uint8_t* const* payloads,
+                                      const float* const* scales, int P, size_t n,
+                                      float* mean_out, float* theta, float lr,
+                                      spl_peer_stats* d_stats, uint32_t* d_flags,
+                                      spl_stream_t stream) {
+    spl::Codec cd;
+    if (!resolve_codec(codec, &cd)) return SPL_ERR_INVALID_ARG;
+    if (P < 1 || P > SPL_MAX_PEERS) return SPL_ERR_INVALID_ARG;
+    if (d_stats != nullptr) {
+        const spl_status st = check_stats(d_stats, P, n, mean_out, theta, d_flags);
+        if (st != SPL_OK) return st;
+    }
+    return decode_impl(cd, payloads, scales, P, n, mean_out, theta, lr, d_stats, d_flags, stream);
 }
 
 spl_status spl_decode_aggregate_stats(const uint8_t* const* payloads, const float* const* scales,
@@ -234,12 +314,11 @@ spl_status spl_decode_aggregate_stats(const uint8_t* const* payloads, const floa
                                       spl_peer_stats* d_stats, uint32_t* d_flags,
                                       spl_stream_t stream) {
     if (P < 1 || P > SPL_MAX_PEERS || d_stats == nullptr) return SPL_ERR_INVALID_ARG;
-    if (!aligned(d_stats, 8)) return SPL_ERR_ALIGNMENT;
-    const size_t sb = static_cast<size_t>(P) * sizeof(spl_peer_stats);
-    if (overlap(d_stats, sb, mean_out, n * 4) || overlap(d_stats, sb, theta, n * 4) ||
-        overlap(d_stats, sb, d_flags, 4))
-        return SPL_ERR_INVALID_ARG;
-    return decode_impl(payloads, scales, P, n, mean_out, theta, lr, d_stats, d_flags, stream);
+    const spl_status st = check_stats(d_stats, P, n, mean_out, theta, d_flags);
+    if (st != SPL_OK) return st;
+    spl::Codec cd;
+    resolve_codec(nullptr, &cd);
+    return decode_impl(cd, payloads, scales, P, n, mean_out, theta, lr, d_stats, d_flags, stream);
 }
 
 spl_status spl_pack(const uint16_t* idx, const uint8_t* codes, size_t num_chunks, uint8_t* payload,

@@ -3,6 +3,8 @@
 // Format: "The Sparse Frontier: SparseLoCo and the Compression Math Behind Permissionless
 // Pre-Training", section "SparseLoCo: Three Compression Levers in One Pass": chunks of 4096,
 // top-64 by |value|, 2-bit values, 12-bit indices, 64 x 14 bits = 112 bytes per chunk.
+// Codec variants keep the layout with another chunk length L or k: fields of
+// 2 + log2(L) bits, k of them per record.
 #pragma once
 
 #include <cstdint>
@@ -16,6 +18,30 @@ constexpr int kFieldBits = 14;
 constexpr int kRecordBytes = 112;
 constexpr int kRecordWords = kRecordBytes / 4;   // 28
 constexpr int kRecordVec = kRecordBytes / 16;    // 7 x 16 bytes
+
+// Scale rules: s = max |a| / 1.5 (the default), or the pairwise sum of the k chosen |a| in
+// ascending index order divided by k (mean-abs, a variant).
+constexpr int kScaleMax = 0;
+constexpr int kScaleMeanAbs = 1;
+
+constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x >> 1); }
+
+// A codec's record geometry: chunk length L (a power of two), k entries per record, each a
+// field of 2 + log2(L) bits; the supported geometries fill whole 32-bit words.
+template <int L, int K>
+struct Geometry {
+    static constexpr int kChunk = L;
+    static constexpr int kTopK = K;
+    static constexpr int kFieldBits = 2 + ilog2(L);
+    static constexpr int kRecordWords = K * kFieldBits / 32;
+    static constexpr int kRecordBytes = 4 * kRecordWords;
+    static constexpr bool kVecRecords = kRecordBytes % 16 == 0;   // records stay 16-B aligned
+    static_assert((L & (L - 1)) == 0 && L >= 2048 && L <= 8192, "chunk length");
+    static_assert(K % 32 == 0 && K >= 32 && K <= 128, "entries per record");
+    static_assert(K * kFieldBits % 32 == 0, "records fill whole words");
+};
+using DefaultGeometry = Geometry<kChunk, kTopK>;
+static_assert(DefaultGeometry::kRecordBytes == kRecordBytes, "default record size");
 
 constexpr uint32_t kFlagNonFinite = 1u;
 constexpr uint32_t kFlagBadRecord = 2u;
@@ -127,6 +153,12 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
                  : "memory");
 }
 
+// The same for 4 bytes (both addresses 4-byte aligned).
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src)
+                 : "memory");
+}
+
 // One arrival on the mbarrier once all of this thread's earlier cp.async copies have landed
 // (counted against the barrier's expected arrivals).
 __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
@@ -206,13 +238,14 @@ __device__ __forceinline__ uint32_t record_field(const uint32_t* words, int r) {
     return v & ((1u << kFieldBits) - 1u);
 }
 
-// The same with one funnel shift.  Reads words[w + 1] even when the field ends inside
-// words[w] (its bits are masked off), so the word after the record must be readable shared
-// memory.
+// The same with one funnel shift, for fields of kBits bits.  Reads words[w + 1] even when
+// the field ends inside words[w] (its bits are masked off), so the word after the record must
+// be readable shared memory.
+template <int kBits = kFieldBits>
 __device__ __forceinline__ uint32_t record_field_fs(const uint32_t* words, int r) {
-    const int bit = kFieldBits * r;
+    const int bit = kBits * r;
     const int w = bit >> 5;
-    return __funnelshift_r(words[w], words[w + 1], bit & 31) & ((1u << kFieldBits) - 1u);
+    return __funnelshift_r(words[w], words[w + 1], bit & 31) & ((1u << kBits) - 1u);
 }
 
 }  // namespace spl

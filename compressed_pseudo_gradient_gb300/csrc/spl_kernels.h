@@ -9,6 +9,36 @@ namespace spl {
 constexpr int kMaxTensorsPerLaunch = 64;
 constexpr int kMaxPeers = 256;
 
+// A codec: chunk length L, entries per record k, scale rule (0: max |a| / 1.5, the default;
+// 1: mean-abs).
+struct Codec {
+    int chunk;
+    int topk;
+    int rule;
+};
+
+// The record geometries (L, k) with kernels in this library; the first is the default.
+constexpr int kNumGeometries = 5;
+constexpr int kGeometries[kNumGeometries][2] = {
+    {4096, 64}, {4096, 32}, {4096, 128}, {2048, 32}, {8192, 128}};
+
+inline bool is_default_codec(const Codec& cd) {
+    return cd.chunk == 4096 && cd.topk == 64 && cd.rule == 0;
+}
+
+// Bytes of one record of a supported codec (k x (2 + log2 L) bits), or 0 when the library
+// has no kernels for it.
+inline int64_t codec_record_bytes(const Codec& cd) {
+    if (cd.rule != 0 && cd.rule != 1) return 0;
+    for (int i = 0; i < kNumGeometries; ++i) {
+        if (kGeometries[i][0] != cd.chunk || kGeometries[i][1] != cd.topk) continue;
+        int bits = 0;
+        while ((1 << bits) < cd.chunk) ++bits;
+        return static_cast<int64_t>(cd.topk) * (2 + bits) / 8;
+    }
+    return 0;
+}
+
 // A table of tensors compressed in one launch; chunk_begin holds prefix sums of the
 // per-tensor chunk counts (chunk_begin[num] = chunks in this launch).
 struct CompressTable {
@@ -25,10 +55,15 @@ struct DecodeTable {
 };
 
 // ef_host: the tensors' error buffers are pinned host memory, read and written over the host
-// link with plain accesses (delta stays in device memory).
-cudaError_t launch_ef_compress(const CompressTable& tab, bool bf16, bool ef_host, float beta,
-                               uint8_t* payload, float* scales, uint32_t* flags,
+// link with plain accesses (delta stays in device memory; default codec only).  The table's
+// chunk_begin counts chunks of the codec's length.
+cudaError_t launch_ef_compress(const CompressTable& tab, const Codec& cd, bool bf16, bool ef_host,
+                               float beta, uint8_t* payload, float* scales, uint32_t* flags,
                                cudaStream_t stream);
+// The same for a codec other than the default (cudaErrorNotSupported for an unknown one).
+cudaError_t launch_ef_compress_variant(const CompressTable& tab, const Codec& cd, bool bf16,
+                                       bool ef_host, float beta, uint8_t* payload, float* scales,
+                                       uint32_t* flags, cudaStream_t stream);
 
 // Per-peer statistics (same layout as spl_peer_stats in spl.h), accumulated by the kernel.
 struct PeerStats {
@@ -39,9 +74,15 @@ struct PeerStats {
     double sumsq;
 };
 
-cudaError_t launch_decode_aggregate(const DecodeTable& tab, int P, int64_t n, float* mean,
-                                    float* theta, float lr, PeerStats* stats, uint32_t* flags,
-                                    cudaStream_t stream);
+cudaError_t launch_decode_aggregate(const DecodeTable& tab, const Codec& cd, int P, int64_t n,
+                                    float* mean, float* theta, float lr, PeerStats* stats,
+                                    uint32_t* flags, cudaStream_t stream);
+// The same for a record geometry other than the default (the scale rule does not matter to
+// the receiver).
+cudaError_t launch_decode_aggregate_variant(const DecodeTable& tab, const Codec& cd, int P,
+                                            int64_t n, float* mean, float* theta, float lr,
+                                            PeerStats* stats, uint32_t* flags,
+                                            cudaStream_t stream);
 
 cudaError_t launch_pack(const uint16_t* idx, const uint8_t* codes, int64_t C,
                         uint8_t* payload, cudaStream_t stream);

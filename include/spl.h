@@ -174,6 +174,59 @@ spl_status spl_decode_aggregate_stats(const uint8_t* const* payloads, const floa
                                       spl_stream_t stream);
 
 /*
+ * Codec variants, for ablation.  The pages fix L = 4096 and k = 64 ("SparseLoCo: Three
+ * Compression Levers in One Pass", item 1), give the index width as ceil(log2 L) (item 3) and
+ * leave the scale rule open (item 2: "a per-chunk scale factor").  A variant keeps the
+ * record layout with fields of 2 + log2 L bits, k per record, in k x (2 + log2 L) / 8 bytes;
+ * records follow one another with no padding (payload base 16-byte aligned; records of 52
+ * or 56 bytes are then 4-byte aligned).  Scale rules:
+ *   SPL_SCALE_MAX_ABS   s = max |a| / 1.5f (the default, above);
+ *   SPL_SCALE_MEAN_ABS  s = (pairwise sum of the k chosen |a| in ascending index order) / k,
+ *                       where the pairwise sum of x[0..m) is x[0] for m = 1 and otherwise the
+ *                       sum of its first floor(m/2) entries plus the sum of the rest, each
+ *                       summed the same way, in fp32 (round to nearest); codes, levels, the
+ *                       residual and the decoder are those of the default rule.
+ * Supported (L, k): (4096, 64) (the default), (4096, 32), (4096, 128), (2048, 32),
+ * (8192, 128), each with either rule.  A NULL codec pointer means the default codec.
+ */
+typedef enum { SPL_SCALE_MAX_ABS = 0, SPL_SCALE_MEAN_ABS = 1 } spl_scale_rule;
+
+typedef struct {
+    uint32_t chunk;      /* L: values per chunk */
+    uint32_t topk;       /* k: entries per record */
+    uint32_t scale_rule; /* an spl_scale_rule */
+} spl_codec;
+
+/* Bytes of one record of the codec, or -1 when the library does not implement it. */
+int64_t spl_codec_record_bytes(const spl_codec* codec);
+
+/* ceil(n / L) for the codec's chunk length L (0 for a codec the library does not implement). */
+size_t spl_codec_num_chunks(const spl_codec* codec, size_t n);
+
+/*
+ * spl_ef_compress_multi with the given codec: payload holds spl_codec_num_chunks(n_i) records
+ * of spl_codec_record_bytes bytes per tensor, in table order.  Error buffers must be device
+ * memory unless the codec is the default one.  SPL_ERR_INVALID_ARG for a codec the library
+ * does not implement.
+ */
+spl_status spl_ef_compress_codec(const spl_codec* codec, const spl_tensor* tensors,
+                                 int num_tensors, spl_dtype delta_dtype, float beta,
+                                 uint8_t* payload, float* scales, uint32_t* d_flags,
+                                 spl_stream_t stream);
+
+/*
+ * spl_decode_aggregate (d_stats NULL) or spl_decode_aggregate_stats (d_stats given) for
+ * records of the given codec (only its L and k matter to the receiver): each payloads[p] holds
+ * spl_codec_num_chunks(n) records of spl_codec_record_bytes bytes, 16-byte aligned at its
+ * start; the statistics count over the k entries of each accepted record.
+ */
+spl_status spl_decode_aggregate_codec(const spl_codec* codec, const uint8_t* const* payloads,
+                                      const float* const* scales, int P, size_t n,
+                                      float* mean_out, float* theta, float lr,
+                                      spl_peer_stats* d_stats, uint32_t* d_flags,
+                                      spl_stream_t stream);
+
+/*
  * Record layout helpers (per-chunk size equation): idx[C][64] and codes[C][64] to and from
  * payload[C][112].  Only the low 12 bits of an index and the low 2 bits of a code are used;
  * pack does not check ordering.  All pointers are device memory.

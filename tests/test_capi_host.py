@@ -29,7 +29,9 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for fn in ("spl_ef_compress", "spl_ef_compress_multi", "spl_decode_aggregate",
-               "spl_decode_aggregate_stats", "spl_pack", "spl_unpack", "spl_num_chunks",
+               "spl_decode_aggregate_stats", "spl_ef_compress_codec",
+               "spl_decode_aggregate_codec", "spl_codec_record_bytes", "spl_codec_num_chunks",
+               "spl_pack", "spl_unpack", "spl_num_chunks",
                "spl_status_string", "spl_last_cuda_error"):
         assert fn in names
 
@@ -131,6 +133,43 @@ def test_decode_stats_argument_errors(lib):
     assert f(pl, sc, P, n, Cp, None, 0.0, D + 4, None, None) == ALIGN       # stats 4-B
     assert f(pl, sc, P, n, Cp, None, 0.0, Cp + 64, None, None) == INVALID   # stats in mean
     assert f(pl, sc, 0, n, Cp, None, 0.0, D, None, None) == INVALID         # P = 0
+
+
+def test_codec_sizes_and_argument_errors(lib):
+    Codec = spl._binding._Codec
+    sizes = {(2048, 32): 52, (4096, 32): 56, (4096, 64): 112, (4096, 128): 224, (8192, 128): 240}
+    for (L, k), rb in sizes.items():
+        for rule in (0, 1):
+            c = Codec(L, k, rule)
+            assert lib.spl_codec_record_bytes(ctypes.byref(c)) == rb
+            assert lib.spl_codec_num_chunks(ctypes.byref(c), 3 * L + 1) == 4
+    assert lib.spl_codec_record_bytes(None) == 112
+    assert lib.spl_codec_num_chunks(None, 4097) == 2
+    for bad in [(1024, 16, 0), (4096, 64, 2), (4096, 48, 0), (0, 0, 0), (2048, 64, 0)]:
+        c = Codec(*bad)
+        assert lib.spl_codec_record_bytes(ctypes.byref(c)) == -1
+        assert lib.spl_codec_num_chunks(ctypes.byref(c), 100) == 0
+    T = spl._binding._Tensor
+    tab = (T * 1)()
+    tab[0].delta, tab[0].ef, tab[0].n = A, B, 8192
+    f = lib.spl_ef_compress_codec
+    bad = Codec(1024, 16, 0)
+    good = Codec(2048, 32, 1)
+    assert f(ctypes.byref(bad), tab, 1, 0, 1.0, Cp, D, None, None) == INVALID
+    assert f(ctypes.byref(good), tab, 1, 0, float("nan"), Cp, D, None, None) == INVALID
+    assert f(ctypes.byref(good), tab, 1, 0, 1.0, Cp + 4, D, None, None) == ALIGN
+    # 4 chunks of 52 bytes: scales placed inside the payload overlap it
+    assert f(ctypes.byref(good), tab, 1, 0, 1.0, Cp, Cp + 200, None, None) == INVALID
+    g = lib.spl_decode_aggregate_codec
+    P = 2
+    pl = (ctypes.c_void_p * P)(A, A + 0x100000)
+    sc = (ctypes.c_void_p * P)(B, B + 0x100000)
+    assert g(ctypes.byref(bad), pl, sc, P, 8192, Cp, None, 0.0, None, None, None) == INVALID
+    assert g(ctypes.byref(good), pl, sc, 0, 8192, Cp, None, 0.0, None, None, None) == INVALID
+    assert g(ctypes.byref(good), pl, sc, P, 8192, Cp, None, 0.0, D + 4, None, None) == ALIGN
+    assert g(ctypes.byref(good), pl, sc, P, 0, Cp, None, 0.0, None, None, None) == OK
+    pl_alias = (ctypes.c_void_p * P)(A, Cp + 4096)                           # record in mean
+    assert g(ctypes.byref(good), pl_alias, sc, P, 8192, Cp, None, 0.0, None, None, None) == INVALID
 
 
 def test_pack_unpack_argument_errors(lib):

@@ -1,0 +1,172 @@
+"""GPU parity of the codec variants (other chunk length L and k, the mean-abs scale rule)
+against the oracle's variants, on the same seeded inputs.
+
+Bar, as for the default codec: payload bytes, scales and the error buffer bit-exact; the mean
+and theta bit-exact (fixed peer order, one rounding each); statistics counts exact.  Every
+case spans several chunks and a ragged tail; the edge cases cover the generic select (ties,
+zeros, few nonzeros) at each geometry, 4-byte-aligned records (52 and 56 bytes) and
+malformed records whose fault lies past the 64th entry.
+"""
+import numpy as np
+import pytest
+import torch
+
+import compressed_pseudo_gradient_gb300 as spl
+import oracle
+from compressed_pseudo_gradient_gb300 import synth
+from parity_util import assert_bit_equal, host
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+MAX, MEAN = spl.SCALE_MAX_ABS, spl.SCALE_MEAN_ABS
+GEOMETRIES = [(4096, 32), (4096, 128), (2048, 32), (8192, 128)]
+CODECS = [(4096, 64, MEAN)] + [(L, k, r) for (L, k) in GEOMETRIES for r in (MAX, MEAN)]
+
+
+@pytest.fixture(autouse=True)
+def _free():
+    yield
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def compare_round(delta, ef, beta, codec, what):
+    d_h, e_h = host(delta), host(ef)
+    flags = torch.zeros(1, dtype=torch.int32, device=DEV)
+    payload, scales = spl.ef_compress(delta, ef, beta, codec=codec, flags=flags)
+    torch.cuda.synchronize()
+    o_pl, o_sc, o_flags = oracle.ef_compress(d_h, e_h, beta, bf16=delta.dtype == torch.bfloat16,
+                                             codec=codec)
+    assert payload.shape == (oracle.num_chunks(delta.numel(), codec), oracle.record_bytes(codec))
+    assert_bit_equal(host(payload), o_pl, f"{what}: payload")
+    assert_bit_equal(host(scales), o_sc, f"{what}: scales")
+    assert_bit_equal(host(ef), e_h, f"{what}: error buffer")
+    assert int(flags.item()) == o_flags
+    return payload, scales, o_pl, o_sc
+
+
+@pytest.mark.parametrize("codec", CODECS)
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_variant_rounds_match_oracle(codec, dtype):
+    L = codec[0]
+    n = 37 * L + 123
+    gen = synth.generator(7 + L + codec[1] + codec[2], DEV)
+    ef = torch.zeros(n, device=DEV)
+    for r in range(3):
+        if dtype == torch.bfloat16:
+            delta = synth.heavy_tail_bf16(n, gen, DEV)
+        else:
+            delta = synth.laplace(n, 1e-3, gen, DEV)
+        compare_round(delta, ef, 0.95, codec, f"{codec} {dtype} round {r}")
+
+
+@pytest.mark.parametrize("codec", CODECS)
+def test_variant_edge_chunks(codec):
+    """Chunks that take the generic select (zeros, constants, heavy ties, fewer nonzeros than
+    k) and tiny tensors, at each geometry."""
+    L, k, _ = codec
+    rng = np.random.default_rng(L + k)
+    few = np.zeros(L, np.float32)
+    few[rng.choice(L, k // 2, replace=False)] = rng.standard_normal(k // 2)
+    ties = np.round(rng.standard_normal(L) * 2).astype(np.float32)
+    coarse = (rng.integers(-3, 4, L) * 0.25).astype(np.float32)
+    spikes = (rng.standard_normal(L) * 1e-3).astype(np.float32)
+    spikes[rng.choice(L, k, replace=False)] = rng.choice([-1.0, 1.0], k) * (1 + rng.random(k))
+    blocks = [np.zeros(L), np.full(L, -2.5), np.arange(L) * -1.0, few, ties, coarse, spikes,
+              np.full(L, 1.4e-45)]
+    delta = torch.cat([torch.as_tensor(b, dtype=torch.float32) for b in blocks]).to(DEV)
+    ef = torch.zeros_like(delta)
+    compare_round(delta, ef, 1.0, codec, f"{codec} edge round 1")
+    compare_round(torch.zeros_like(delta), ef, 1.0, codec, f"{codec} edge round 2")
+    for n in (1, k - 1, k, k + 1, L - 1, L + 1):
+        d = synth.laplace(n, 1.0, synth.generator(n, DEV), DEV)
+        compare_round(d, torch.zeros(n, device=DEV), 0.5, codec, f"{codec} n={n}")
+
+
+@pytest.mark.parametrize("codec", [(L, k, MAX) for (L, k) in GEOMETRIES])
+def test_variant_decode_matches_oracle(codec):
+    L, k, _ = codec
+    n = 21 * L + 77
+    P = 5
+    pls, scs, o_pls, o_scs = [], [], [], []
+    for p in range(P):
+        d = synth.laplace(n, 1e-3, synth.generator(50 + p, DEV), DEV)
+        pl, sc, opl, osc = compare_round(d, torch.zeros(n, device=DEV), 1.0, codec, f"peer {p}")
+        pls.append(pl), scs.append(sc), o_pls.append(opl), o_scs.append(osc)
+    theta = synth.theta(n, synth.generator(3, DEV), DEV)
+    th_h = host(theta).copy()
+    flags = torch.zeros(1, dtype=torch.int32, device=DEV)
+    stats = spl.new_peer_stats(P, DEV)
+    mean = spl.decode_aggregate(pls, scs, n, theta=theta, lr=0.7, flags=flags, stats=stats,
+                                codec=codec)
+    mean_plain = spl.decode_aggregate(pls, scs, n, codec=codec)
+    torch.cuda.synchronize()
+    o_mean, o_flags = oracle.decode_aggregate(o_pls, o_scs, n, theta=th_h, lr=0.7, codec=codec)
+    assert int(flags.item()) == o_flags == 0
+    assert_bit_equal(host(mean), o_mean, f"{codec}: mean")
+    assert_bit_equal(host(mean_plain), o_mean, f"{codec}: mean without theta or statistics")
+    assert_bit_equal(host(theta), th_h, f"{codec}: theta")
+    got = spl.read_peer_stats(stats)
+    ref = oracle.peer_stats(o_pls, o_scs, n, codec=codec)
+    for key in ("rejected", "big", "negative"):
+        assert np.array_equal(got[key], ref[key]), key
+    assert_bit_equal(got["max_scale"], ref["max_scale"], "max_scale")
+    assert np.allclose(got["sumsq"], ref["sumsq"], rtol=1e-6, atol=0)
+
+
+@pytest.mark.parametrize("codec", [(4096, 128, MAX), (2048, 32, MAX), (8192, 128, MAX)])
+def test_variant_malformed_records_rejected_like_oracle(codec):
+    L, k, _ = codec
+    n = 6 * L
+    pls, scs = [], []
+    for p in range(3):
+        d = synth.laplace(n, 1e-4, synth.generator(90 + p, DEV), DEV)
+        pl, sc = spl.ef_compress(d, torch.zeros(n, device=DEV), 1.0, codec=codec)
+        pls.append(host(pl).copy()), scs.append(host(sc).copy())
+    idx, codes = oracle.unpack(pls[1], codec)
+    idx[0, [k - 3, k - 2]] = idx[0, [k - 2, k - 3]]   # chunk 0: not ascending near the end
+    idx[2, 20] = idx[2, 19]                            # chunk 2: duplicate
+    pls[1] = oracle.pack(idx, codes, codec)
+    scs[2][1] = np.nan
+    scs[2][4] = -1.0
+    flags = torch.zeros(1, dtype=torch.int32, device=DEV)
+    stats = spl.new_peer_stats(3, DEV)
+    mean = spl.decode_aggregate([torch.from_numpy(p).to(DEV) for p in pls],
+                                [torch.from_numpy(s).to(DEV) for s in scs], n, flags=flags,
+                                stats=stats, codec=codec)
+    torch.cuda.synchronize()
+    o_mean, o_flags = oracle.decode_aggregate(pls, scs, n, codec=codec)
+    assert int(flags.item()) == o_flags == oracle.FLAG_BAD_RECORD
+    assert_bit_equal(host(mean), o_mean, f"{codec}: mean with rejected records")
+    got = spl.read_peer_stats(stats)
+    assert list(got["rejected"]) == list(oracle.peer_stats(pls, scs, n, codec=codec)["rejected"])
+    assert list(got["rejected"]) == [0, 2, 2]
+
+
+def test_variant_multi_tensor_matches_single_calls():
+    codec = (2048, 32, MEAN)
+    sizes = [2048 * 3, 100, 2048 * 5 + 7, 0, 1]
+    gen = synth.generator(4, DEV)
+    deltas = [synth.laplace(m, 1e-3, gen, DEV) for m in sizes]
+    efs = [synth.laplace(m, 1e-4, gen, DEV) for m in sizes]
+    efs2 = [e.clone() for e in efs]
+    payload, scales = spl.ef_compress_multi(deltas, efs, 0.9, codec=codec)
+    parts_p, parts_s = [], []
+    for d, e in zip(deltas, efs2):
+        if d.numel():
+            p, s = spl.ef_compress(d, e, 0.9, codec=codec)
+            parts_p.append(p), parts_s.append(s)
+    torch.cuda.synchronize()
+    assert_bit_equal(host(payload), host(torch.cat(parts_p)), "multi-tensor payload")
+    assert_bit_equal(host(scales), host(torch.cat(parts_s)), "multi-tensor scales")
+    for e, e2 in zip(efs, efs2):
+        assert_bit_equal(host(e), host(e2), "multi-tensor error buffers")
+
+
+def test_variant_host_error_buffer_rejected():
+    n = 3 * 4096
+    delta = torch.zeros(n, device=DEV)
+    ef = torch.zeros(n).pin_memory()
+    with pytest.raises(spl.SplError):
+        spl.ef_compress(delta, ef, 1.0, codec=(4096, 32, MAX))
+    spl.ef_compress(delta, ef, 1.0, codec=(4096, 64, MAX))   # the default codec takes it
