@@ -50,12 +50,18 @@ WORKLOAD = ("EF-compress of 2^30 fp32 Laplace(0,1e-4) values (beta 0.95, fp32 er
 FALLBACK_HBM_GBS = 6800.0
 
 
-def compress_bytes(n: int, C: int) -> int:
-    return 12 * n + (RECORD + 4) * C
+def compress_bytes(n: int, C: int, record: int = RECORD) -> int:
+    return 12 * n + (record + 4) * C
 
 
-def decode_bytes(n: int, C: int, P: int, theta: bool = True) -> int:
-    return P * (RECORD + 4) * C + 4 * n + (8 * n if theta else 0)
+def decode_bytes(n: int, C: int, P: int, theta: bool = True, record: int = RECORD) -> int:
+    return P * (record + 4) * C + 4 * n + (8 * n if theta else 0)
+
+
+# The codec variants timed by --workload codecs: (chunk length, k, scale rule), the default
+# codec first.
+CODECS = [(4096, 64, 0), (4096, 64, 1), (4096, 32, 0), (4096, 32, 1), (4096, 128, 0),
+          (4096, 128, 1), (2048, 32, 0), (2048, 32, 1), (8192, 128, 0), (8192, 128, 1)]
 
 
 STEP_BYTES = compress_bytes(N_ELEMS, N_CHUNKS) + decode_bytes(N_ELEMS, N_CHUNKS, PEERS)
@@ -126,9 +132,10 @@ def read_peaks():
 
 
 def kernel_source_hash(name: str) -> str:
+    """Hash of a kernel's sources: its launch unit, its template header and the device helpers."""
     src = os.path.join(ROOT, "compressed_pseudo_gradient_gb300", "csrc")
     h = hashlib.sha256()
-    for f in (f"{name}.cu", "spl_device.cuh"):
+    for f in (f"{name}.cu", f"{name}.cuh", "spl_device.cuh"):
         with open(os.path.join(src, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -400,6 +407,84 @@ def run_other_workload(args, dev):
     return 0
 
 
+def run_codecs(args, dev):
+    """Times the receive step (compress of n fp32 Laplace(0,1e-4) values with beta 0.95, then
+    the 24-peer decode fused with the outer step) for the default codec and each variant;
+    one JSON line with a per-codec breakdown.  The value is all codecs' bytes over their
+    total time."""
+    import torch
+    import compressed_pseudo_gradient_gb300 as spl
+    from compressed_pseudo_gradient_gb300 import synth
+
+    n = args.elements
+    delta = synth.laplace(n, 1e-4, synth.generator(1, dev), dev)
+    ef = torch.zeros(n, dtype=torch.float32, device=dev)
+    theta = synth.theta(n, synth.generator(5000, dev), dev)
+    mean = torch.empty(n, dtype=torch.float32, device=dev)
+    tmp = torch.empty(n, dtype=torch.float32, device=dev)
+    peak, kind = read_peaks()
+    rows, total_bytes, total_s, launches = [], 0, 0.0, 0
+    for codec in CODECS:
+        L = codec[0]
+        C = (n + L - 1) // L
+        rb = spl.record_bytes(codec)
+        payload = torch.empty((C, rb), dtype=torch.uint8, device=dev)
+        scales = torch.empty(C, dtype=torch.float32, device=dev)
+        pls, scs = [], []
+        for p in range(PEERS):
+            d = synth.laplace(n, 1e-4, synth.generator(2 + p, dev), dev)
+            tmp.zero_()
+            pl, sc = spl.ef_compress(d, tmp, BETA, codec=codec)
+            pls.append(pl)
+            scs.append(sc)
+            del d
+        ef.zero_()
+
+        def step(ev=None):
+            if ev:
+                ev[0].record()
+            spl.ef_compress(delta, ef, BETA, payload=payload, scales=scales, codec=codec)
+            if ev:
+                ev[1].record()
+            spl.decode_aggregate(pls, scs, n, mean=mean, theta=theta, lr=LR, codec=codec)
+            if ev:
+                ev[2].record()
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize(dev)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        for k in range(args.steps):
+            step(evs[k])
+            launches += 2
+        torch.cuda.synchronize(dev)
+        c_s = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) / 1e3
+        d_s = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) / 1e3
+        cb, db = compress_bytes(n, C, rb), decode_bytes(n, C, PEERS, record=rb)
+        total_bytes += (cb + db) * args.steps
+        total_s += (c_s + d_s) * args.steps
+        rows.append({"codec": {"chunk": codec[0], "topk": codec[1],
+                               "scale": "mean_abs" if codec[2] else "max_abs"},
+                     "record_bytes": rb,
+                     "ef_compress": {"ms": round(1e3 * c_s, 4), "GB/s": round(cb / c_s / 1e9, 1),
+                                     "frac_of_hbm": round(cb / c_s / 1e9 / peak, 4)},
+                     "decode_aggregate": {"ms": round(1e3 * d_s, 4),
+                                          "GB/s": round(db / d_s / 1e9, 1),
+                                          "frac_of_hbm": round(db / d_s / 1e9 / peak, 4)}})
+        del pls, scs, payload, scales
+        torch.cuda.empty_cache()
+    value = total_bytes / total_s / 1e9
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * total_s / args.steps / len(CODECS), 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": f"codec variants: receive step at {n} values, 24 peers",
+                       "n": n, "peak_gbs": peak, "peak_kind": kind, "codecs": rows},
+            "gpu_launches": launches}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_gpu(args, dev, rank, world):
     import torch
 
@@ -608,7 +693,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="receive",
-                    choices=["receive", "heavy_tail_bf16", "decoder_layer", "tiny", "offload"],
+                    choices=["receive", "heavy_tail_bf16", "decoder_layer", "tiny", "offload",
+                             "codecs"],
                     help="receive (default): the headline step; the others time one round of "
                          "another workload on one GPU")
     ap.add_argument("--decode-stats", action="store_true",
@@ -633,6 +719,8 @@ def main(argv=None):
             raise SystemExit("--workload other than receive runs on one GPU")
         if args.workload == "offload":
             return run_offload(args, dev)
+        if args.workload == "codecs":
+            return run_codecs(args, dev)
         return run_other_workload(args, dev)
     dist_init("nccl")
     r = run_gpu(args, dev, rank, world)
