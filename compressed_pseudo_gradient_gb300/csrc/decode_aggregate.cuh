@@ -44,23 +44,29 @@ namespace {
 #define SPL_DECODE_STAGES 1
 #endif
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
 constexpr int kStages = SPL_DECODE_STAGES;
 
-// Per-codec sizes of the receiver (default: 512 positions and 4 vectors per thread of each
-// warp, groups of 64 peers, two entries per lane, seven 16-byte pieces per record).
+#ifndef SPL_DECODE_THREADS_8192
+#define SPL_DECODE_THREADS_8192 512
+#endif
+
+// Per-codec sizes of the receiver (default: 256 threads, 512 positions and 4 vectors per
+// thread of each warp, groups of 64 peers, two entries per lane, seven 16-byte pieces per
+// record).
 template <class Geo>
 struct RecvShape {
     static constexpr int kChunk = Geo::kChunk;
     static constexpr int kTopK = Geo::kTopK;
+    static constexpr int kThreads = kChunk == 8192 ? SPL_DECODE_THREADS_8192 : 256;
+    static constexpr int kWarps = kThreads / 32;
     static constexpr int kSlice = kChunk / kWarps;          // positions per warp
     static constexpr int kVec = kSlice / 128;               // vectors of 4 per thread
     static constexpr int kGroup = kTopK <= 64 ? 64 : 32;    // peers unpacked per pass
     static constexpr int kPerLane = kTopK / 32;             // entries per lane of a record
     static constexpr int kPieceBytes = Geo::kVecRecords ? 16 : 4;
     static constexpr int kPieces = Geo::kRecordBytes / kPieceBytes;   // copies per record
-    static constexpr int kMinBlocks = kChunk <= 4096 ? 4 : 2;
+    static constexpr int kMinBlocks = kThreads == 256 && kChunk > 4096 ? 2 : 1024 / kThreads;
+    static_assert(32 * kWarps >= kMaxPeers, "one scale per lane for up to 256 peers");
 };
 
 __host__ __device__ constexpr size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
@@ -101,6 +107,7 @@ __device__ __forceinline__ void prefetch(const DecodeTable& tab, int P, int64_t 
                                          const float* theta, uint64_t* bar, uint8_t* st_rec,
                                          float* st_theta, int tid) {
     using S = RecvShape<Geo>;
+    constexpr int kThreads = S::kThreads;
     constexpr int kChunk = S::kChunk;
     constexpr int kRecordBytes = Geo::kRecordBytes;
     constexpr int kPieces = S::kPieces;
@@ -129,11 +136,13 @@ __device__ __forceinline__ void prefetch(const DecodeTable& tab, int P, int64_t 
 }
 
 template <class Geo, bool kStats>
-__global__ void __launch_bounds__(kThreads, RecvShape<Geo>::kMinBlocks)
+__global__ void __launch_bounds__(RecvShape<Geo>::kThreads, RecvShape<Geo>::kMinBlocks)
 k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __restrict__ mean,
                    float* __restrict__ theta, float neg_lr, PeerStats* __restrict__ stats,
                    uint32_t* __restrict__ flags) {
     using S = RecvShape<Geo>;
+    constexpr int kThreads = S::kThreads;
+    constexpr int kWarps = S::kWarps;
     constexpr int kChunk = S::kChunk;
     constexpr int kTopK = S::kTopK;
     constexpr int kSlice = S::kSlice;
@@ -163,7 +172,7 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
     if (static_cast<int64_t>(blockIdx.x) >= C) return;
     const float pf = static_cast<float>(P);
     const int slice0 = kSlice * warp;    // this warp's positions: slice0 + 128 v + 4 lane + u
-    const int my_peer = 8 * lane + warp; // the peer whose scale this lane carries
+    const int my_peer = kWarps * lane + warp;   // the peer whose scale this lane carries
 
 #pragma unroll
     for (int v = 0; v < kVec; ++v)
@@ -236,7 +245,7 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
                         asc = asc && (lane == 31 || ix[m] < next);
                     }
                 }
-                const float s = __shfl_sync(0xffffffffu, sc_cur, p >> 3);
+                const float s = __shfl_sync(0xffffffffu, sc_cur, p / kWarps);
                 const bool ok = __all_sync(0xffffffffu, asc) && s >= 0.0f && s <= FLT_MAX;
                 if (ok) {
                     uint2* eg = ent + g * kTopK;
@@ -401,6 +410,7 @@ cudaError_t launch_decode(const DecodeTable& tab, int P, int64_t n, float* mean,
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
+    constexpr int kThreads = RecvShape<Geo>::kThreads;
     const int resident = persistent_grid(kern, kThreads, smem);
     if (resident <= 0) return cudaErrorInvalidConfiguration;
     const int grid = static_cast<int>(C < resident ? C : resident);

@@ -39,22 +39,32 @@
 namespace spl {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
 constexpr uint32_t kWindow = (2048u << 16) - 1u;   // 16 octaves of magnitude keys: 2048 bins
 constexpr uint32_t kNotFound = 0xffffffffu;
 
-// Per-codec sizes of the sender (default: 16 values and 4 vectors per thread, 128 bitmap
-// words, 4 per lane of warp 0).
+#ifndef SPL_COMPRESS_THREADS_4096
+#define SPL_COMPRESS_THREADS_4096 256
+#endif
+#ifndef SPL_COMPRESS_MIN_BLOCKS_4096
+#define SPL_COMPRESS_MIN_BLOCKS_4096 4
+#endif
+
+// Per-codec sizes of the sender.  A CTA of L / 16 threads works on one chunk, 16 values per
+// thread (default: 256 threads, 4 vectors per thread, 128 bitmap words, 4 per lane of warp 0),
+// and 1024 / threads CTAs share an SM (64 registers per thread, 32 warps per SM).
 template <class Geo>
 struct SendShape {
     static constexpr int kChunk = Geo::kChunk;
     static constexpr int kTopK = Geo::kTopK;
+    static constexpr int kThreads = kChunk == 4096 ? SPL_COMPRESS_THREADS_4096 : kChunk / 16;
+    static constexpr int kWarps = kThreads / 32;
     static constexpr int kPer = kChunk / kThreads;       // values per thread
     static constexpr int kVec = kPer / 4;                // vectors of 4 per thread
+    static constexpr int kStride = 4 * kThreads;         // between a thread's vectors
     static constexpr int kBitmapWords = kChunk / 32;
     static constexpr int kWordsPerLane = kBitmapWords / 32;
-    static constexpr int kMinBlocks = kChunk <= 4096 ? 4 : 2;   // 64 or 128 registers
+    static constexpr int kMinBlocks = kChunk == 4096 ? SPL_COMPRESS_MIN_BLOCKS_4096 : 1024 / kThreads;
+    static_assert(kPer % 4 == 0 && kThreads % 32 == 0 && 2048 % kThreads == 0, "sender shape");
 };
 
 template <class Geo, int kRule>
@@ -65,8 +75,8 @@ struct Smem {
     uint32_t hist[2048];               // histogram bins (one select pass at a time)
     uint32_t sel_bm[S::kBitmapWords];  // chosen positions (complete once the select is done)
     uint32_t eq_bm[S::kBitmapWords];   // ties at the final threshold (many-candidate path)
-    uint32_t warp_tot[kWarps];
-    uint32_t warp_max[kWarps];
+    uint32_t warp_tot[S::kWarps];
+    uint32_t warp_max[S::kWarps];
     uint32_t bcast[3];                 // digit, count above the digit's bin, count in the bin
     uint2 cand[32];                    // (key, index) of the keys in the boundary bin
     uint32_t ncand;
@@ -80,10 +90,11 @@ struct Smem {
 // Block-wide search of the bin holding the need-th largest key (counting from the top bin).
 // Thread t owns bins [kBinsPer*t, kBinsPer*t + kBinsPer).  Writes sm.bcast; the caller
 // synchronises before reading it.
-template <int kBins, class Sm>
+template <int kBins, class S, class Sm>
 __device__ __forceinline__ void find_digit(Sm& sm, const uint32_t* hist, uint32_t need,
                                            int tid, int lane, int warp) {
-    constexpr int kBinsPer = kBins / kThreads;
+    constexpr int kWarps = S::kWarps;
+    constexpr int kBinsPer = kBins / S::kThreads;
     uint32_t h[kBinsPer];
     uint32_t sum = 0;
 #pragma unroll
@@ -160,17 +171,18 @@ __device__ __forceinline__ void prefetch(Sm& sm, const ChunkRef& r) {
 
 // a = fmaf(beta, e, delta) for this thread's 16 values, from the stage (full chunks); with
 // the error buffer in host memory, e comes straight from there.
-template <int kVec, bool kBf16, bool kEfHost, class Sm>
+template <class S, bool kBf16, bool kEfHost, class Sm>
 __device__ __forceinline__ void accumulate_from_stage(const Sm& sm, const ChunkRef& r,
-                                                      float beta, int tid, float (&a)[4 * kVec]) {
+                                                      float beta, int tid, float (&a)[S::kPer]) {
+    constexpr int kVec = S::kVec;
     float4 eh[kVec];
     if constexpr (kEfHost) {
 #pragma unroll
-        for (int v = 0; v < kVec; ++v) eh[v] = ld_stream_f4(r.ef + v * 1024 + 4 * tid);
+        for (int v = 0; v < kVec; ++v) eh[v] = ld_stream_f4(r.ef + v * S::kStride + 4 * tid);
     }
 #pragma unroll
     for (int v = 0; v < kVec; ++v) {
-        const int j0 = v * 1024 + 4 * tid;
+        const int j0 = v * S::kStride + 4 * tid;
         const float4 e4 = kEfHost ? eh[v] : *reinterpret_cast<const float4*>(&sm.stage_e[j0]);
         float d[4];
         if constexpr (kBf16) {
@@ -192,14 +204,14 @@ __device__ __forceinline__ void accumulate_from_stage(const Sm& sm, const ChunkR
 }
 
 // The same for a tail chunk, straight from global memory; pads are +0.
-template <int kVec, bool kBf16>
+template <class S, bool kBf16>
 __device__ __forceinline__ void accumulate_tail(const ChunkRef& r, float beta, int tid,
-                                                float (&a)[4 * kVec]) {
+                                                float (&a)[S::kPer]) {
 #pragma unroll
-    for (int v = 0; v < kVec; ++v)
+    for (int v = 0; v < S::kVec; ++v)
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const int j = v * 1024 + 4 * tid + u;
+            const int j = v * S::kStride + 4 * tid + u;
             float d = 0.0f, e = 0.0f;
             if (j < r.valid) {
                 e = r.ef[j];
@@ -220,17 +232,19 @@ __device__ __noinline__ void generic_select(Sm& sm, const uint32_t (&key)[SendSh
     using S = SendShape<Geo>;
     constexpr int kPer = S::kPer;
     constexpr int kVec = S::kVec;
+    constexpr int kThreads = S::kThreads;
+    constexpr int kStride = S::kStride;
     constexpr uint32_t kTopK = S::kTopK;
     {
         uint4* h4 = reinterpret_cast<uint4*>(&sm.hist[0]);
-        h4[tid] = make_uint4(0, 0, 0, 0);
-        h4[tid + kThreads] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int i = 0; i < 512 / kThreads; ++i) h4[tid + i * kThreads] = make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < kPer; ++i) atomicAdd(&sm.hist[key[i] >> 20], 1u);
     __syncthreads();
-    find_digit<2048>(sm, sm.hist, kTopK, tid, lane, warp);
+    find_digit<2048, S>(sm, sm.hist, kTopK, tid, lane, warp);
     __syncthreads();
     uint32_t need = kTopK - sm.bcast[1];      // keys still to take from bin D
     const uint32_t dig = sm.bcast[0];
@@ -242,7 +256,7 @@ __device__ __noinline__ void generic_select(Sm& sm, const uint32_t (&key)[SendSh
         for (int v = 0; v < kVec; ++v)
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int j = v * 1024 + 4 * tid + u;
+                const int j = v * kStride + 4 * tid + u;
                 if ((key[4 * v + u] >> 20) >= dig) atomicOr(&sm.sel_bm[j >> 5], 1u << (j & 31));
             }
         __syncthreads();
@@ -252,28 +266,29 @@ __device__ __noinline__ void generic_select(Sm& sm, const uint32_t (&key)[SendSh
         uint32_t pmask = 0x7ffu << 20;
         {   // the first pass's bins have been read: clear them for the second pass
             uint4* h4 = reinterpret_cast<uint4*>(&sm.hist[0]);
-            h4[tid] = make_uint4(0, 0, 0, 0);
-            h4[tid + kThreads] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int i = 0; i < 512 / kThreads; ++i) h4[tid + i * kThreads] = make_uint4(0, 0, 0, 0);
         }
         __syncthreads();
 #pragma unroll
         for (int i = 0; i < kPer; ++i)
             if ((key[i] & pmask) == prefix) atomicAdd(&sm.hist[(key[i] >> 9) & 0x7ffu], 1u);
         __syncthreads();
-        find_digit<2048>(sm, sm.hist, need, tid, lane, warp);
+        find_digit<2048, S>(sm, sm.hist, need, tid, lane, warp);
         __syncthreads();
         need -= sm.bcast[1];
         prefix |= sm.bcast[0] << 9;
         pmask |= 0x7ffu << 9;
         if (sm.bcast[2] != need) {
-            sm.hist[tid] = 0;                 // the second pass's bins have been read
-            sm.hist[tid + kThreads] = 0;
+#pragma unroll
+            for (int i = 0; i < 512 / kThreads; ++i)   // the second pass's bins have been read
+                sm.hist[tid + i * kThreads] = 0;
             __syncthreads();
 #pragma unroll
             for (int i = 0; i < kPer; ++i)
                 if ((key[i] & pmask) == prefix) atomicAdd(&sm.hist[key[i] & 0x1ffu], 1u);
             __syncthreads();
-            find_digit<512>(sm, sm.hist, need, tid, lane, warp);
+            find_digit<512, S>(sm, sm.hist, need, tid, lane, warp);
             __syncthreads();
             need -= sm.bcast[1];
             prefix |= sm.bcast[0];
@@ -285,7 +300,7 @@ __device__ __noinline__ void generic_select(Sm& sm, const uint32_t (&key)[SendSh
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const uint32_t mk = key[4 * v + u] & pmask;
-                const int j = v * 1024 + 4 * tid + u;
+                const int j = v * kStride + 4 * tid + u;
                 if (mk > prefix) atomicOr(&sm.sel_bm[j >> 5], 1u << (j & 31));
                 else if (mk == prefix) atomicOr(&sm.eq_bm[j >> 5], 1u << (j & 31));
             }
@@ -344,14 +359,17 @@ __device__ __forceinline__ void store_words(uint8_t* rec, int w0, uint32_t word,
 }
 
 template <class Geo, int kRule, bool kBf16, bool kEfHost>
-__global__ void __launch_bounds__(kThreads, SendShape<Geo>::kMinBlocks)
+__global__ void __launch_bounds__(SendShape<Geo>::kThreads, SendShape<Geo>::kMinBlocks)
 k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload,
               float* __restrict__ scales, uint32_t* __restrict__ flags) {
     using S = SendShape<Geo>;
     constexpr int kChunk = S::kChunk;
     constexpr int kTopK = S::kTopK;
+    constexpr int kThreads = S::kThreads;
+    constexpr int kWarps = S::kWarps;
     constexpr int kPer = S::kPer;
     constexpr int kVec = S::kVec;
+    constexpr int kStride = S::kStride;
     constexpr int kBitmapWords = S::kBitmapWords;
     constexpr int kFieldBits = Geo::kFieldBits;
     constexpr int kRecordWords = Geo::kRecordWords;
@@ -385,9 +403,9 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
         if (r.full) {
             timed_out = !mbar_wait(&sm.bar, parity);
             parity ^= 1u;
-            accumulate_from_stage<kVec, kBf16, kEfHost>(sm, r, beta, tid, a);
+            accumulate_from_stage<S, kBf16, kEfHost>(sm, r, beta, tid, a);
         } else {
-            accumulate_tail<kVec, kBf16>(r, beta, tid, a);
+            accumulate_tail<S, kBf16>(r, beta, tid, a);
         }
         uint32_t key[kPer];
         uint32_t kmax = 0;
@@ -402,8 +420,8 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
         {
             uint4* h4 = reinterpret_cast<uint4*>(&sm.hist[0]);
             const uint4 z = make_uint4(0, 0, 0, 0);
-            h4[tid] = z;                      // 2048 words
-            h4[tid + kThreads] = z;
+#pragma unroll
+            for (int i = 0; i < 512 / kThreads; ++i) h4[tid + i * kThreads] = z;   // 2048 words
             if constexpr (2 * kBitmapWords == kThreads) {
                 if (tid < kBitmapWords) sm.sel_bm[tid] = 0;
                 else sm.eq_bm[tid - kBitmapWords] = 0;
@@ -447,7 +465,7 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
                 if (key[i] >= lo_key) atomicAdd(&sm.hist[(key[i] - lo_key) >> 16], 1u);
         }
         __syncthreads();
-        if (windowed) find_digit<2048>(sm, sm.hist, kTopK, tid, lane, warp);
+        if (windowed) find_digit<2048, S>(sm, sm.hist, kTopK, tid, lane, warp);
         __syncthreads();
         bool selected = false;
         if (windowed && sm.bcast[0] != kNotFound) {
@@ -466,7 +484,7 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const uint32_t kk = key[4 * v + u];
-                        const int j = v * 1024 + 4 * tid + u;
+                        const int j = v * kStride + 4 * tid + u;
                         if (kk >= k_in) {
                             atomicOr(&sm.sel_bm[j >> 5], 1u << (j & 31));
                         } else if (kk >= k_lo) {
@@ -540,7 +558,7 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
             // owners: each chosen |a| at its rank (ascending index order)
 #pragma unroll
             for (int v = 0; v < kVec; ++v) {
-                const int j0 = v * 1024 + 4 * tid;
+                const int j0 = v * kStride + 4 * tid;
                 const uint32_t word = sm.sel_bm[j0 >> 5];
                 const int sh = j0 & 31;
                 if (((word >> sh) & 0xfu) == 0u) continue;
@@ -577,7 +595,7 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
         // ---- owners: rank, code and residual of each chosen value ------------------------
 #pragma unroll
         for (int v = 0; v < kVec; ++v) {
-            const int j0 = v * 1024 + 4 * tid;
+            const int j0 = v * kStride + 4 * tid;
             const uint32_t word = sm.sel_bm[j0 >> 5];
             const int sh = j0 & 31;
             if (((word >> sh) & 0xfu) == 0u) continue;
@@ -596,14 +614,14 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
         if (r.full) {
 #pragma unroll
             for (int v = 0; v < kVec; ++v)
-                st_stream_f4(r.ef + v * 1024 + 4 * tid,
+                st_stream_f4(r.ef + v * kStride + 4 * tid,
                              make_float4(a[4 * v], a[4 * v + 1], a[4 * v + 2], a[4 * v + 3]));
         } else {
 #pragma unroll
             for (int v = 0; v < kVec; ++v)
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const int j = v * 1024 + 4 * tid + u;
+                    const int j = v * kStride + 4 * tid + u;
                     if (j < r.valid) r.ef[j] = a[4 * v + u];
                 }
         }
@@ -651,6 +669,7 @@ cudaError_t launch_compress(const CompressTable& tab, int64_t total, float beta,
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
+    constexpr int kThreads = SendShape<Geo>::kThreads;
     const int resident = persistent_grid(kern, kThreads, smem);
     if (resident <= 0) return cudaErrorInvalidConfiguration;
     const int grid = static_cast<int>(total < resident ? total : resident);
