@@ -82,7 +82,7 @@ struct Smem {
     uint32_t ncand;
     uint16_t fields[S::kTopK];         // the record's fields, in ascending index order
     float absval[kRule == kScaleMeanAbs ? S::kTopK : 1];   // mean-abs: chosen |a| by rank
-    float scale;                       // mean-abs: the chunk's scale
+    uint32_t full_scan;                // the k-th key lies below the top 512 bins
     alignas(16) uint16_t pre[S::kBitmapWords];   // chosen positions before each bitmap word
     uint64_t bar;                      // completes when the stage's bulk copies have landed
 };
@@ -127,6 +127,51 @@ __device__ __forceinline__ void find_digit(Sm& sm, const uint32_t* hist, uint32_
             run += h[i];
         }
     }
+}
+
+// Warp 0: the bin holding the need-th largest key, searched among the top 512 of the 2048
+// bins (the 4 octaves below the largest key), where it lies for all but very heavy-tailed
+// chunks.  Writes sm.bcast and returns true, or returns false (for the whole warp) when those
+// bins hold fewer than need keys.  Spares the block-wide search and its two barriers.
+template <class Sm>
+__device__ __forceinline__ bool top_digit(Sm& sm, uint32_t need, int lane) {
+    constexpr int kTop = 512;
+    constexpr int kBase = 2048 - kTop;
+    constexpr int kPerLane = kTop / 32;
+    uint32_t h[kPerLane];
+    uint32_t sum = 0;
+    const uint4* h4 = reinterpret_cast<const uint4*>(&sm.hist[kBase + kPerLane * lane]);
+#pragma unroll
+    for (int q = 0; q < kPerLane / 4; ++q) {
+        const uint4 v = h4[q];
+        h[4 * q + 0] = v.x;
+        h[4 * q + 1] = v.y;
+        h[4 * q + 2] = v.z;
+        h[4 * q + 3] = v.w;
+        sum += v.x + v.y + v.z + v.w;
+    }
+    uint32_t incl = sum;   // suffix sum over lanes >= lane
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_down_sync(0xffffffffu, incl, o);
+        if (lane + o < 32) incl += y;
+    }
+    if (__shfl_sync(0xffffffffu, incl, 0) < need) return false;
+    const uint32_t excl = incl - sum;
+    if (excl < need && incl >= need) {
+        uint32_t run = excl;
+#pragma unroll
+        for (int i = kPerLane - 1; i >= 0; --i) {
+            if (run + h[i] >= need) {
+                sm.bcast[0] = kBase + kPerLane * lane + i;
+                sm.bcast[1] = run;
+                sm.bcast[2] = h[i];
+                break;
+            }
+            run += h[i];
+        }
+    }
+    return true;
 }
 
 // The chunk a CTA works on: its tensor's pointers advanced to the chunk, and its extent.
@@ -358,6 +403,34 @@ __device__ __forceinline__ void store_words(uint8_t* rec, int w0, uint32_t word,
     }
 }
 
+// One warp: assemble a record from the fields in shared memory and store it with its scale.
+template <class Geo, class Sm>
+__device__ __forceinline__ void pack_record(const Sm& sm, uint8_t* __restrict__ payload,
+                                            float* __restrict__ scales, int64_t c, float s,
+                                            int lane) {
+    constexpr int kFieldBits = Geo::kFieldBits;
+    constexpr int kRecordWords = Geo::kRecordWords;
+#pragma unroll
+    for (int w0 = 0; w0 < kRecordWords; w0 += 32) {
+        const int w = w0 + lane < kRecordWords ? w0 + lane : kRecordWords - 1;
+        const int r_first = (32 * w) / kFieldBits;
+        const int r_last = (32 * w + 31) / kFieldBits;
+        uint32_t word = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {   // a word touches at most 4 fields of >= 13 bits
+            const int r = r_first + k;
+            if (r <= r_last) {
+                const uint32_t f = sm.fields[r];
+                const int off = kFieldBits * r - 32 * w;
+                word |= off >= 0 ? (f << off) : (f >> (-off));
+            }
+        }
+        store_words<kRecordWords, Geo::kVecRecords>(payload + c * Geo::kRecordBytes, w0, word,
+                                                     lane);
+    }
+    if (lane == 0) scales[c] = s;
+}
+
 template <class Geo, int kRule, bool kBf16, bool kEfHost>
 __global__ void __launch_bounds__(SendShape<Geo>::kThreads, SendShape<Geo>::kMinBlocks)
 k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload,
@@ -393,6 +466,8 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
     uint32_t parity = 0;
     bool nonfinite = false;
     bool aborted = false;
+    int64_t pend_c = -1;     // the chunk whose record the last warp still has to pack
+    float pend_s = 0.0f;
 
     for (int64_t c = blockIdx.x; c < total; c += gridDim.x) {
         const ChunkRef r = locate<kChunk, kBf16>(tab, c);
@@ -416,21 +491,13 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
         }
         nonfinite |= kmax >= kKeyInf;
 
-        // ---- clear the histograms and bitmaps; chunk max --------------------------------
+        // ---- clear the histogram; chunk max ----------------------------------------------
+        // (the previous chunk's select is done, and nothing reads the histogram after it)
         {
             uint4* h4 = reinterpret_cast<uint4*>(&sm.hist[0]);
             const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
             for (int i = 0; i < 512 / kThreads; ++i) h4[tid + i * kThreads] = z;   // 2048 words
-            if constexpr (2 * kBitmapWords == kThreads) {
-                if (tid < kBitmapWords) sm.sel_bm[tid] = 0;
-                else sm.eq_bm[tid - kBitmapWords] = 0;
-            } else {
-                for (int i = tid; i < 2 * kBitmapWords; i += kThreads) {
-                    if (i < kBitmapWords) sm.sel_bm[i] = 0;
-                    else sm.eq_bm[i - kBitmapWords] = 0;
-                }
-            }
             if (tid == 0) {
                 sm.ncand = 0;
                 sm.bcast[0] = kNotFound;
@@ -447,6 +514,21 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
             const ChunkRef rn = locate<kChunk, kBf16>(tab, c + gridDim.x);
             if (rn.full) prefetch<kChunk, kBf16, kEfHost>(sm, rn);
         }
+        // the previous chunk's owners have read the bitmaps (the barrier above follows their
+        // step): clear them for this chunk's select, which first writes them two barriers on
+        if constexpr (2 * kBitmapWords == kThreads) {
+            if (tid < kBitmapWords) sm.sel_bm[tid] = 0;
+            else sm.eq_bm[tid - kBitmapWords] = 0;
+        } else {
+            for (int i = tid; i < 2 * kBitmapWords; i += kThreads) {
+                if (i < kBitmapWords) sm.sel_bm[i] = 0;
+                else sm.eq_bm[i - kBitmapWords] = 0;
+            }
+        }
+        // the last warp packs the previous chunk's record: its fields are complete (the
+        // barrier above follows that chunk's owner step) and are next written after this
+        // chunk's select
+        if (warp == kWarps - 1 && pend_c >= 0) pack_record<Geo>(sm, payload, scales, pend_c, pend_s, lane);
         uint32_t mkey = 0;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) mkey = max(mkey, sm.warp_max[w]);
@@ -465,8 +547,15 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
                 if (key[i] >= lo_key) atomicAdd(&sm.hist[(key[i] - lo_key) >> 16], 1u);
         }
         __syncthreads();
-        if (windowed) find_digit<2048, S>(sm, sm.hist, kTopK, tid, lane, warp);
+        if (windowed && warp == 0) {
+            const bool found = top_digit(sm, kTopK, lane);
+            if (lane == 0) sm.full_scan = found ? 0u : 1u;
+        }
         __syncthreads();
+        if (windowed && sm.full_scan != 0u) {   // uniform: every thread read the same flag
+            find_digit<2048, S>(sm, sm.hist, kTopK, tid, lane, warp);
+            __syncthreads();
+        }
         bool selected = false;
         if (windowed && sm.bcast[0] != kNotFound) {
             const uint32_t need = kTopK - sm.bcast[1];
@@ -572,24 +661,21 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
                 }
             }
             __syncthreads();
-            // warp 0: pairwise sum (recursive halving) over ranks 0..k-1: lane l first sums
-            // its k/32 consecutive entries the same way, then the lanes combine as a tree
-            if (warp == 0) {
-                constexpr int kPerLane = kTopK / 32;
-                float x[kPerLane];
+            // every warp forms the same pairwise sum (recursive halving) over ranks 0..k-1:
+            // lane l first sums its k/32 consecutive entries the same way, then the lanes
+            // combine as a tree; so each warp holds the scale without another barrier
+            constexpr int kPerLane = kTopK / 32;
+            float x[kPerLane];
 #pragma unroll
-                for (int i = 0; i < kPerLane; ++i) x[i] = sm.absval[kPerLane * lane + i];
+            for (int i = 0; i < kPerLane; ++i) x[i] = sm.absval[kPerLane * lane + i];
 #pragma unroll
-                for (int w = 1; w < kPerLane; w <<= 1)
+            for (int w = 1; w < kPerLane; w <<= 1)
 #pragma unroll
-                    for (int i = 0; i + w < kPerLane; i += 2 * w) x[i] = __fadd_rn(x[i], x[i + w]);
-                float t = x[0];
+                for (int i = 0; i + w < kPerLane; i += 2 * w) x[i] = __fadd_rn(x[i], x[i + w]);
+            float t = x[0];
 #pragma unroll
-                for (int o = 1; o < 32; o <<= 1) t = __fadd_rn(t, __shfl_down_sync(0xffffffffu, t, o));
-                if (lane == 0) sm.scale = __fdiv_rn(t, static_cast<float>(kTopK));
-            }
-            __syncthreads();
-            s = sm.scale;
+            for (int o = 1; o < 32; o <<= 1) t = __fadd_rn(t, __shfl_down_sync(0xffffffffu, t, o));
+            s = __fdiv_rn(__shfl_sync(0xffffffffu, t, 0), static_cast<float>(kTopK));
         }
 
         // ---- owners: rank, code and residual of each chosen value ------------------------
@@ -625,31 +711,13 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
                     if (j < r.valid) r.ef[j] = a[4 * v + u];
                 }
         }
-        __syncthreads();
 
-        // ---- one warp: pack the record and write the scale ------------------------------
-        if (warp == 0) {
-#pragma unroll
-            for (int w0 = 0; w0 < kRecordWords; w0 += 32) {
-                const int w = w0 + lane < kRecordWords ? w0 + lane : kRecordWords - 1;
-                const int r_first = (32 * w) / kFieldBits;
-                const int r_last = (32 * w + 31) / kFieldBits;
-                uint32_t word = 0;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {   // a word touches at most 4 fields of >= 13 bits
-                    const int r = r_first + k;
-                    if (r <= r_last) {
-                        const uint32_t f = sm.fields[r];
-                        const int off = kFieldBits * r - 32 * w;
-                        word |= off >= 0 ? (f << off) : (f >> (-off));
-                    }
-                }
-                store_words<kRecordWords, Geo::kVecRecords>(payload + c * kRecordBytes, w0, word,
-                                                             lane);
-            }
-            if (lane == 0) scales[c] = s;
-        }
+        // ---- the record is packed by the last warp at the top of the next iteration ------
+        pend_c = c;
+        pend_s = s;
     }
+    __syncthreads();   // the last chunk's fields are complete
+    if (warp == kWarps - 1 && pend_c >= 0) pack_record<Geo>(sm, payload, scales, pend_c, pend_s, lane);
     if (aborted && tid == 0) {
         // the copy that did not complete may still land: wait once more (bounded) before
         // the CTA's shared memory is released
