@@ -61,7 +61,9 @@ struct RecvShape {
     static constexpr int kWarps = kThreads / 32;
     static constexpr int kSlice = kChunk / kWarps;          // positions per warp
     static constexpr int kVec = kSlice / 128;               // vectors of 4 per thread
-    static constexpr int kGroup = kTopK <= 64 ? 64 : 32;    // peers unpacked per pass
+    // peers unpacked per pass: with k = 128, 16 at 256 threads keeps the entries at 16 KB, so
+    // four CTAs fit an SM; a multiple of the warp count (peer p is unpacked by warp p mod W)
+    static constexpr int kGroup = kTopK <= 64 ? 64 : (kThreads == 256 ? 16 : 32);
     static constexpr int kPerLane = kTopK / 32;             // entries per lane of a record
     static constexpr int kPieceBytes = Geo::kVecRecords ? 16 : 4;
     static constexpr int kPieces = Geo::kRecordBytes / kPieceBytes;   // copies per record
