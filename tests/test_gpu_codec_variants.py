@@ -170,3 +170,40 @@ def test_variant_host_error_buffer_rejected():
     with pytest.raises(spl.SplError):
         spl.ef_compress(delta, ef, 1.0, codec=(4096, 32, MAX))
     spl.ef_compress(delta, ef, 1.0, codec=(4096, 64, MAX))   # the default codec takes it
+
+
+@pytest.mark.parametrize("codec", [(L, k, MAX) for (L, k) in GEOMETRIES])
+@pytest.mark.parametrize("P", [24, 70])
+def test_variant_many_peers_span_several_groups(codec, P):
+    """Peers are unpacked in groups (16 or 32 for k = 128, 64 otherwise); 24 and 70 peers
+    span one to five groups."""
+    L, k, _ = codec
+    n = 5 * L + 9
+    C = 6
+    rng = np.random.default_rng(P + L + k)
+    pls, scs = [], []
+    for p in range(P):
+        idx = np.sort(np.stack([rng.choice(L, k, replace=False) for _ in range(C)]), axis=1)
+        idx = idx.astype(np.uint16)
+        codes = rng.integers(0, 4, size=(C, k)).astype(np.uint8)
+        if p % 11 == 3:
+            idx[p % C, [k - 2, k - 1]] = idx[p % C, [k - 1, k - 2]]   # a malformed record
+        pls.append(oracle.pack(idx, codes, codec))
+        scs.append((rng.random(C) * 1e-3).astype(np.float32))
+    theta = synth.theta(n, synth.generator(P, DEV), DEV)
+    th_h = host(theta).copy()
+    flags = torch.zeros(1, dtype=torch.int32, device=DEV)
+    stats = spl.new_peer_stats(P, DEV)
+    mean = spl.decode_aggregate([torch.from_numpy(p).to(DEV) for p in pls],
+                                [torch.from_numpy(s).to(DEV) for s in scs], n, theta=theta,
+                                lr=0.7, flags=flags, stats=stats, codec=codec)
+    torch.cuda.synchronize()
+    o_mean, o_flags = oracle.decode_aggregate(pls, scs, n, theta=th_h, lr=0.7, codec=codec)
+    assert int(flags.item()) == o_flags == oracle.FLAG_BAD_RECORD
+    assert_bit_equal(host(mean), o_mean, f"{codec} P={P}: mean")
+    assert_bit_equal(host(theta), th_h, f"{codec} P={P}: theta")
+    got = spl.read_peer_stats(stats)
+    ref = oracle.peer_stats(pls, scs, n, codec=codec)
+    for key in ("rejected", "big", "negative"):
+        assert np.array_equal(got[key], ref[key]), key
+    assert np.allclose(got["sumsq"], ref["sumsq"], rtol=1e-6, atol=0)

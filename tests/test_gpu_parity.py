@@ -553,3 +553,44 @@ def test_peer_stats_match_oracle():
         assert np.array_equal(again[key], 2 * ref[key]), key
     assert_bit_equal(again["max_scale"], ref["max_scale"], "max_scale after two calls")
     assert np.allclose(again["sumsq"], 2 * ref["sumsq"], rtol=1e-6, atol=0)
+
+
+# ---------------------------------------------------------------------------------------------
+# Many peers: the decode unpacks peers in groups of 64, so these span several groups
+# ---------------------------------------------------------------------------------------------
+def random_records(rng, C: int, L: int = 4096, k: int = 64):
+    """C records with random strictly ascending indices and random codes, as (idx, codes)."""
+    idx = np.sort(np.stack([rng.choice(L, k, replace=False) for _ in range(C)]), axis=1)
+    return idx.astype(np.uint16), rng.integers(0, 4, size=(C, k)).astype(np.uint8)
+
+
+@pytest.mark.parametrize("P", [65, 130, 256])
+def test_many_peers_span_several_groups(P):
+    n = 9 * 4096 + 11
+    C = 10
+    rng = np.random.default_rng(P)
+    pls, scs = [], []
+    for p in range(P):
+        idx, codes = random_records(rng, C)
+        if p % 37 == 5:
+            idx[p % C, [7, 8]] = idx[p % C, [8, 7]]          # a malformed record
+        pls.append(oracle.pack(idx, codes))
+        scs.append((rng.random(C) * 1e-3).astype(np.float32))
+    theta = synth.theta(n, synth.generator(P, DEV), DEV)
+    th_h = host(theta).copy()
+    flags = torch.zeros(1, dtype=torch.int32, device=DEV)
+    stats = spl.new_peer_stats(P, DEV)
+    mean = spl.decode_aggregate([torch.from_numpy(p).to(DEV) for p in pls],
+                                [torch.from_numpy(s).to(DEV) for s in scs], n, theta=theta,
+                                lr=0.7, flags=flags, stats=stats)
+    torch.cuda.synchronize()
+    o_mean, o_flags = oracle.decode_aggregate(pls, scs, n, theta=th_h, lr=0.7)
+    assert int(flags.item()) == o_flags == oracle.FLAG_BAD_RECORD
+    assert_bit_equal(host(mean), o_mean, f"P={P}: mean")
+    assert_bit_equal(host(theta), th_h, f"P={P}: theta")
+    got = spl.read_peer_stats(stats)
+    ref = oracle.peer_stats(pls, scs, n)
+    for key in ("rejected", "big", "negative"):
+        assert np.array_equal(got[key], ref[key]), key
+    assert_bit_equal(got["max_scale"], ref["max_scale"], "max_scale")
+    assert np.allclose(got["sumsq"], ref["sumsq"], rtol=1e-6, atol=0)
