@@ -78,7 +78,7 @@ struct Smem {
     uint32_t warp_tot[S::kWarps];
     uint32_t warp_max[S::kWarps];
     uint32_t bcast[3];                 // digit, count above the digit's bin, count in the bin
-    uint2 cand[32];                    // (key, index) of the keys in the boundary bin
+    uint2 cand[64];                    // (key, index) of the keys in the boundary bin
     uint32_t ncand;
     uint16_t fields[S::kTopK];         // the record's fields, in ascending index order
     float absval[kRule == kScaleMeanAbs ? S::kTopK : 1];   // mean-abs: chosen |a| by rank
@@ -561,7 +561,7 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
             const uint32_t need = kTopK - sm.bcast[1];
             const uint32_t dig = sm.bcast[0];
             const uint32_t in_bin = sm.bcast[2];
-            if (in_bin == need || in_bin <= 32u) {
+            if (in_bin == need || in_bin <= 64u) {
                 const bool rank_bin = in_bin != need;
                 // bin D as a key range [k_lo, k_hi): keys at or above k_hi are in, keys in the
                 // range are in when the bin is taken whole, else they are the candidates
@@ -578,20 +578,41 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
                             atomicOr(&sm.sel_bm[j >> 5], 1u << (j & 31));
                         } else if (kk >= k_lo) {
                             const uint32_t slot = atomicAdd(&sm.ncand, 1u);
-                            if (slot < 32u) sm.cand[slot] = make_uint2(kk, static_cast<uint32_t>(j));
+                            if (slot < 64u) sm.cand[slot] = make_uint2(kk, static_cast<uint32_t>(j));
                         }
                     }
                 __syncthreads();
                 if (rank_bin && warp == 0) {
-                    const uint2 me = static_cast<uint32_t>(lane) < in_bin ? sm.cand[lane] : make_uint2(0u, 0u);
-                    uint32_t rank = 0;
-                    for (uint32_t o = 0; o < in_bin; ++o) {
-                        const uint32_t ok = __shfl_sync(0xffffffffu, me.x, o);
-                        const uint32_t oj = __shfl_sync(0xffffffffu, me.y, o);
-                        rank += (ok > me.x || (ok == me.x && oj < me.y)) ? 1u : 0u;
+                    // rank each candidate among the bin's keys (magnitude, then index)
+                    if (in_bin <= 32u) {
+                        const uint2 me = static_cast<uint32_t>(lane) < in_bin ? sm.cand[lane] : make_uint2(0u, 0u);
+                        uint32_t rank = 0;
+                        for (uint32_t o = 0; o < in_bin; ++o) {
+                            const uint32_t ok = __shfl_sync(0xffffffffu, me.x, o);
+                            const uint32_t oj = __shfl_sync(0xffffffffu, me.y, o);
+                            rank += (ok > me.x || (ok == me.x && oj < me.y)) ? 1u : 0u;
+                        }
+                        if (static_cast<uint32_t>(lane) < in_bin && rank < need)
+                            atomicOr(&sm.sel_bm[me.y >> 5], 1u << (me.y & 31));
+                    } else {   // 33..64 candidates (dense tops): two per lane
+                        const uint2 m0 = sm.cand[lane];
+                        const uint2 m1 = static_cast<uint32_t>(lane) + 32u < in_bin ? sm.cand[lane + 32] : make_uint2(0u, 0u);
+                        uint32_t r0 = 0, r1 = 0;
+                        for (uint32_t o = 0; o < in_bin; ++o) {
+                            const uint32_t src = o & 31u;
+                            const uint32_t k0 = __shfl_sync(0xffffffffu, m0.x, src);
+                            const uint32_t j0 = __shfl_sync(0xffffffffu, m0.y, src);
+                            const uint32_t k1 = __shfl_sync(0xffffffffu, m1.x, src);
+                            const uint32_t j1 = __shfl_sync(0xffffffffu, m1.y, src);
+                            const uint32_t ok = o < 32u ? k0 : k1;
+                            const uint32_t oj = o < 32u ? j0 : j1;
+                            r0 += (ok > m0.x || (ok == m0.x && oj < m0.y)) ? 1u : 0u;
+                            r1 += (ok > m1.x || (ok == m1.x && oj < m1.y)) ? 1u : 0u;
+                        }
+                        if (r0 < need) atomicOr(&sm.sel_bm[m0.y >> 5], 1u << (m0.y & 31));
+                        if (static_cast<uint32_t>(lane) + 32u < in_bin && r1 < need)
+                            atomicOr(&sm.sel_bm[m1.y >> 5], 1u << (m1.y & 31));
                     }
-                    if (static_cast<uint32_t>(lane) < in_bin && rank < need)
-                        atomicOr(&sm.sel_bm[me.y >> 5], 1u << (me.y & 31));
                     __syncwarp();
                 }
                 selected = true;

@@ -121,8 +121,9 @@ def test_degenerate_chunks():
 
 def test_select_window_edges():
     """Chunks built around the compress kernel's fast path: its histogram spans the 16 octaves
-    below the chunk max and ranks a boundary bin of at most 32 keys directly; everything else
-    takes the generic radix select.  Both must agree with the oracle."""
+    below the chunk max and ranks a boundary bin of at most 64 keys directly (one per lane up to
+    32, two per lane beyond); everything else takes the generic radix select.  Both must agree
+    with the oracle."""
     rng = np.random.default_rng(17)
     L = 4096
     base = (rng.random(L).astype(np.float32) * 0.5 + 0.25)               # ~[0.25, 0.75)
@@ -142,14 +143,25 @@ def test_select_window_edges():
             c[pos[:40]] = 2.0
             c[pos[40:]] = -1.0     # the rest of the chunk stays below 0.75
         return f
+    def dense(count):
+        def f(c):                  # `count` distinct keys inside one bin, 40 above them
+            pos = rng.choice(L, 40 + count, replace=False)
+            c[pos[:40]] = 2.0
+            # 1 + (i + 1) 2^-20: keys 0x3F800008 + 8 i, inside one bin of the window whose
+            # top bin starts at the key of 2.0 (bin edges at keys ending in 0x0001)
+            vals = (1.0 + (1 + np.arange(count)) * 2.0 ** -20).astype(np.float32)
+            c[pos[40:]] = rng.permutation(vals) * rng.choice([-1.0, 1.0], count)
+        return f
     def one_per_bin(c):            # distinct powers of two: each key alone in its bin
         c[:] = 0.0
         c[rng.choice(L, 80, replace=False)] = 2.0 ** -np.arange(80, dtype=np.float32) * 8
     def exact_bin(c):              # exactly 64 keys at or above one value
         c[rng.choice(L, 64, replace=False)] = 3.0
     blocks = [chunk(spikes_far_above), chunk(spikes_just_inside), chunk(ties(20)),
-              chunk(ties(24)), chunk(ties(25)), chunk(ties(33)), chunk(ties(200)),
-              chunk(one_per_bin), chunk(exact_bin)]
+              chunk(ties(24)), chunk(ties(25)), chunk(ties(33)), chunk(ties(48)),
+              chunk(ties(64)), chunk(ties(65)), chunk(ties(200)), chunk(dense(25)),
+              chunk(dense(32)), chunk(dense(33)), chunk(dense(47)), chunk(dense(63)),
+              chunk(dense(64)), chunk(dense(65)), chunk(one_per_bin), chunk(exact_bin)]
     delta = _chunks(*blocks)
     ef = torch.zeros_like(delta)
     compare_full_round(delta, ef, 1.0, "window edges round 1")
