@@ -132,12 +132,16 @@ def read_peaks():
 
 
 def kernel_source_hash(name: str) -> str:
-    """Hash of a kernel's sources: its launch unit, its template header and the device helpers."""
+    """Hash of a kernel's code: its launch unit, its template header and the device helpers,
+    with // comments and blank lines left out (a comment edit does not change the kernel)."""
     src = os.path.join(ROOT, "compressed_pseudo_gradient_gb300", "csrc")
     h = hashlib.sha256()
     for f in (f"{name}.cu", f"{name}.cuh", "spl_device.cuh"):
-        with open(os.path.join(src, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(src, f)) as fh:
+            for line in fh:
+                code = line.split("//", 1)[0].rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

@@ -19,16 +19,24 @@
 //     chunk offsets v*1024 + 4*tid), forms a = fma(beta, e, delta) and the 31-bit magnitude
 //     keys, and keeps them there for the whole chunk; the error buffer is written back once,
 //     from registers, with streaming stores;
-//   - the 64th-largest key is found by a radix select: shared-memory histograms of key bits
-//     [30:20], then [19:9] and [8:0] restricted to the keys matching the digits found so far,
-//     stopping as soon as the boundary bin is taken whole; ties at the final threshold go to
-//     the lowest indices; the chosen positions end up in a 4096-bit shared bitmap;
+//   - the 64th-largest key: a shared-memory histogram of 2048 bins of 1/128 octave over the
+//     16 octaves below the chunk's largest key; warp 0 finds the bin holding the 64th key
+//     among the top 512 bins (a block-wide search over all 2048 runs only when those hold
+//     fewer than 64 keys); keys above that bin are marked chosen, and the bin's own keys are
+//     taken whole or, up to 64 of them, ranked by warp 0 (magnitude, then index); any other
+//     chunk (a non-finite value, the 64th key more than 16 octaves below the largest, more
+//     than 64 keys in its bin) takes an out-of-line radix select over key bits [30:20],
+//     [19:9] and [8:0] with ties to the lowest indices; the chosen positions end up in a
+//     4096-bit shared bitmap;
 //   - one warp turns the bitmap into per-word prefix counts, from which every thread that
 //     owns a chosen value knows its rank in ascending index order; it computes the code and
-//     the residual in registers and writes its 14-bit field to shared memory; one warp then
-//     assembles the 112-byte record (28 words) and stores it as seven 16-byte vectors;
-//   - mean-abs scale (variant): owners first write the chosen |a| by rank, warp 0 sums them
-//     pairwise in ascending index order and divides by k, then the owners code as above.
+//     the residual in registers and writes its 14-bit field to shared memory; the last warp
+//     assembles the 112-byte record (28 words) at the top of the next iteration, behind the
+//     barrier that already follows the owner step, and stores it as seven 16-byte vectors;
+//     five block barriers per chunk in all;
+//   - mean-abs scale (variant): owners first write the chosen |a| by rank; after a barrier
+//     every warp forms the same pairwise sum in ascending index order and divides by k, then
+//     the owners code as above.
 #pragma once
 
 #include <type_traits>
