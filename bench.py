@@ -534,7 +534,9 @@ def run_gpu(args, dev, rank, world):
 def run_e2e(args, buf, dev):
     """The same step through the public API with host buffers: H2D of the step's inputs
     (delta and the 24 peers' records and scales) from pinned memory, the two calls, and D2H
-    of the step's result (this peer's records and scales)."""
+    of the step's result (this peer's records and scales).  Two sets of device inputs: step
+    i + 1's copies run on a copy stream while step i computes (each step still copies all of
+    its inputs and reads back its result inside the timed region)."""
     import torch
     import compressed_pseudo_gradient_gb300 as spl
 
@@ -543,35 +545,58 @@ def run_e2e(args, buf, dev):
     h_sc = [s.cpu().pin_memory() for s in buf["peers_sc"]]
     out_pl = torch.empty_like(buf["payload"], device="cpu").pin_memory()
     out_sc = torch.empty_like(buf["scales"], device="cpu").pin_memory()
-    d_delta = torch.empty_like(buf["delta"])
-    d_pl = [torch.empty_like(p) for p in buf["peers_pl"]]
-    d_sc = [torch.empty_like(s) for s in buf["peers_sc"]]
+    sets = [(torch.empty_like(buf["delta"]), [torch.empty_like(p) for p in buf["peers_pl"]],
+             [torch.empty_like(s) for s in buf["peers_sc"]]) for _ in range(2)]
     h2d = h_delta.numel() * 4 + sum(p.numel() for p in h_pl) + sum(s.numel() * 4 for s in h_sc)
     d2h = out_pl.numel() + out_sc.numel() * 4
+    comp = torch.cuda.current_stream(dev)
+    copy = torch.cuda.Stream(dev)
+    copied = [torch.cuda.Event() for _ in range(2)]
+    freed = [torch.cuda.Event() for _ in range(2)]
 
-    def step():
-        d_delta.copy_(h_delta, non_blocking=True)
-        for d, h in zip(d_pl, h_pl):
-            d.copy_(h, non_blocking=True)
-        for d, h in zip(d_sc, h_sc):
-            d.copy_(h, non_blocking=True)
+    def issue_copy(i):
+        k = i % 2
+        d_delta, d_pl, d_sc = sets[k]
+        with torch.cuda.stream(copy):
+            copy.wait_event(freed[k])          # step i - 2 has finished with this set
+            d_delta.copy_(h_delta, non_blocking=True)
+            for d, h in zip(d_pl, h_pl):
+                d.copy_(h, non_blocking=True)
+            for d, h in zip(d_sc, h_sc):
+                d.copy_(h, non_blocking=True)
+            copied[k].record(copy)
+
+    def compute(i):
+        k = i % 2
+        d_delta, d_pl, d_sc = sets[k]
+        comp.wait_event(copied[k])
         spl.ef_compress(d_delta, buf["ef"], BETA, payload=buf["payload"], scales=buf["scales"])
         spl.decode_aggregate(d_pl, d_sc, buf["n"], mean=buf["mean"], theta=buf["theta"], lr=LR)
+        freed[k].record(comp)
         out_pl.copy_(buf["payload"], non_blocking=True)
         out_sc.copy_(buf["scales"], non_blocking=True)
 
-    for _ in range(max(1, args.warmup)):
-        step()
+    def run(steps, start=None):
+        for e in freed:
+            e.record(comp)
+        if start is not None:
+            copy.wait_stream(comp)             # no copy starts before the start event
+        issue_copy(0)
+        for i in range(steps):
+            if i + 1 < steps:
+                issue_copy(i + 1)
+            compute(i)
+
+    run(max(1, args.warmup))
     torch.cuda.synchronize(dev)
     steps = max(1, args.e2e_steps)
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     barrier(dev)
     torch.cuda.synchronize(dev)
-    start.record()
-    for _ in range(steps):
-        step()
-    end.record()
+    start.record(comp)
+    run(steps, start)
+    end.record(comp)                           # after the last step's compute and D2H
     torch.cuda.synchronize(dev)
     barrier(dev)
     t = max_over_ranks(start.elapsed_time(end) / 1e3, dev)
