@@ -667,12 +667,16 @@ def make_cpu_sample(S: int, seed_base: int = 1):
     n = S * CHUNK
     cpu = torch.device("cpu")
     delta = synth.laplace(n, 1e-4, synth.generator(seed_base, cpu), cpu).numpy()
-    pls, scs = [], []
-    for p in range(PEERS):
-        d = synth.laplace(n, 1e-4, synth.generator(seed_base + 1 + p, cpu), cpu).numpy()
+    peer_deltas = [synth.laplace(n, 1e-4, synth.generator(seed_base + 1 + p, cpu), cpu).numpy()
+                   for p in range(PEERS)]
+
+    def peer(d):   # the oracle's C calls release the GIL: the peers compress in parallel
         pl, sc, _ = oracle.ef_compress(d, np.zeros(n, np.float32), BETA)
-        pls.append(pl)
-        scs.append(sc)
+        return pl, sc
+    with ThreadPoolExecutor(max_workers=min(PEERS, os.cpu_count() or 1)) as ex:
+        out = list(ex.map(peer, peer_deltas))
+    pls = [o[0] for o in out]
+    scs = [o[1] for o in out]
     theta = synth.theta(n, synth.generator(seed_base + 5000, cpu), cpu).numpy()
     return {"chunks": S, "delta": delta, "ef": np.zeros(n, np.float32), "theta": theta,
             "peers_pl": pls, "peers_sc": scs}
