@@ -29,7 +29,8 @@
 //     the other resident CTAs keep the SM fed (with statistics, the threads of the other warps
 //     meanwhile fold one record each into per-CTA per-peer totals, flushed with atomics at
 //     the end);
-//   - the dense pass divides by P (correctly rounded, with a precomputed reciprocal), stores
+//   - the dense pass divides by P (correctly rounded, with a precomputed reciprocal; one
+//     multiply when P is a power of two, whose reciprocal is exact), stores
 //     the mean and the updated theta with streaming stores and clears the accumulator.  Peers
 //     are unpacked in groups of up to 64 (16 or 32 for k = 128), so shared memory stays
 //     bounded for any P.
@@ -176,6 +177,7 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
     const int64_t G = gridDim.x;
     if (static_cast<int64_t>(blockIdx.x) >= C) return;
     const float pf = static_cast<float>(P);
+    const bool pow2 = (P & (P - 1)) == 0;   // the same for every thread of the launch
     const int slice0 = kSlice * warp;    // this warp's positions: slice0 + 128 v + 4 lane + u
     const int my_peer = kWarps * lane + warp;   // the peer whose scale this lane carries
 
@@ -350,10 +352,17 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
             const int j0 = slice0 + 128 * v + 4 * lane;
             float4 m4 = *reinterpret_cast<const float4*>(&acc[j0]);
             *reinterpret_cast<float4*>(&acc[j0]) = make_float4(0.f, 0.f, 0.f, 0.f);
-            m4.x = div_rn(m4.x, pf, rp);
-            m4.y = div_rn(m4.y, pf, rp);
-            m4.z = div_rn(m4.z, pf, rp);
-            m4.w = div_rn(m4.w, pf, rp);
+            if (pow2) {   // 1/P = 2^-k exactly: the rounded product is the rounded quotient
+                m4.x = __fmul_rn(m4.x, rp);
+                m4.y = __fmul_rn(m4.y, rp);
+                m4.z = __fmul_rn(m4.z, rp);
+                m4.w = __fmul_rn(m4.w, rp);
+            } else {
+                m4.x = div_rn(m4.x, pf, rp);
+                m4.y = div_rn(m4.y, pf, rp);
+                m4.z = div_rn(m4.z, pf, rp);
+                m4.w = div_rn(m4.w, pf, rp);
+            }
             if (full) {
                 st_stream_f4(mean + base + j0, m4);
                 if (theta != nullptr) {

@@ -1,6 +1,7 @@
 // Test-only kernel: compares the library's division helper (reciprocal + Markstein
-// correction) with CUDA's correctly rounded division, bit for bit, over dividend ranges given
-// by their bit patterns and divisors 1..pmax.  Built and loaded by the GPU tests.
+// correction), and for power-of-two divisors the single multiply by the exact reciprocal,
+// with CUDA's correctly rounded division, bit for bit, over dividend ranges given by their bit
+// patterns and divisors 1..pmax.  Built and loaded by the GPU tests.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -19,7 +20,11 @@ __global__ void k_div_check(const float* rps, uint32_t bits_lo, uint32_t count,
         const float x = __uint_as_float(b);
         const float q = spl::div_rn(x, d, rd);
         const float r = __fdiv_rn(x, d);
-        const bool same = __float_as_uint(q) == __float_as_uint(r) || (q != q && r != r);
+        bool same = __float_as_uint(q) == __float_as_uint(r) || (q != q && r != r);
+        if ((P & (P - 1)) == 0) {   // the decode's path for P = 2^k: one multiply by 2^-k
+            const float m = __fmul_rn(x, rd);
+            same = same && (__float_as_uint(m) == __float_as_uint(r) || (m != m && r != r));
+        }
         if (!same) {
             atomicAdd(bad, 1ull);
             atomicCAS(first_bad, 0xffffffffu, b);
