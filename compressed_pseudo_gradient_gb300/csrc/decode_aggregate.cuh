@@ -141,7 +141,7 @@ __device__ __forceinline__ void prefetch(const DecodeTable& tab, int P, int64_t 
     }
 }
 
-template <class Geo, bool kStats>
+template <class Geo, bool kStats, bool kPow2>
 __global__ void __launch_bounds__(RecvShape<Geo>::kThreads, RecvShape<Geo>::kMinBlocks)
 k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __restrict__ mean,
                    float* __restrict__ theta, float neg_lr, PeerStats* __restrict__ stats,
@@ -177,7 +177,6 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
     const int64_t G = gridDim.x;
     if (static_cast<int64_t>(blockIdx.x) >= C) return;
     const float pf = static_cast<float>(P);
-    const bool pow2 = (P & (P - 1)) == 0;   // the same for every thread of the launch
     const int slice0 = kSlice * warp;    // this warp's positions: slice0 + 128 v + 4 lane + u
     const int my_peer = kWarps * lane + warp;   // the peer whose scale this lane carries
 
@@ -352,7 +351,7 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
             const int j0 = slice0 + 128 * v + 4 * lane;
             float4 m4 = *reinterpret_cast<const float4*>(&acc[j0]);
             *reinterpret_cast<float4*>(&acc[j0]) = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (pow2) {   // 1/P = 2^-k exactly: the rounded product is the rounded quotient
+            if constexpr (kPow2) {   // 1/P = 2^-k exactly: the rounded product is the rounded quotient
                 m4.x = __fmul_rn(m4.x, rp);
                 m4.y = __fmul_rn(m4.y, rp);
                 m4.z = __fmul_rn(m4.z, rp);
@@ -414,13 +413,12 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
     }
 }
 
-template <class Geo, bool kStats>
-cudaError_t launch_decode(const DecodeTable& tab, int P, int64_t n, float* mean, float* theta,
-                          float lr, PeerStats* stats, uint32_t* flags, cudaStream_t stream) {
-    const int64_t C = (n + Geo::kChunk - 1) / Geo::kChunk;
-    if (C == 0) return cudaSuccess;
+template <class Geo, bool kStats, bool kPow2>
+cudaError_t launch_kernel(const DecodeTable& tab, int P, int64_t n, int64_t C, float* mean,
+                          float* theta, float lr, PeerStats* stats, uint32_t* flags,
+                          cudaStream_t stream) {
     const size_t smem = Layout<Geo>(P, kStats).total;
-    const void* kern = reinterpret_cast<const void*>(&k_decode_aggregate<Geo, kStats>);
+    const void* kern = reinterpret_cast<const void*>(&k_decode_aggregate<Geo, kStats, kPow2>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -429,9 +427,21 @@ cudaError_t launch_decode(const DecodeTable& tab, int P, int64_t n, float* mean,
     if (resident <= 0) return cudaErrorInvalidConfiguration;
     const int grid = static_cast<int>(C < resident ? C : resident);
     const float rp = 1.0f / static_cast<float>(P);   // correctly rounded on the host
-    k_decode_aggregate<Geo, kStats><<<grid, kThreads, smem, stream>>>(tab, P, rp, n, mean, theta,
-                                                                      -lr, stats, flags);
+    k_decode_aggregate<Geo, kStats, kPow2><<<grid, kThreads, smem, stream>>>(tab, P, rp, n, mean,
+                                                                            theta, -lr, stats, flags);
     return cudaGetLastError();
+}
+
+// For P a power of two the mean is one multiply by 1/P = 2^-k (exact), else the corrected
+// reciprocal division; the choice is made per launch, so each kernel has one straight path.
+template <class Geo, bool kStats>
+cudaError_t launch_decode(const DecodeTable& tab, int P, int64_t n, float* mean, float* theta,
+                          float lr, PeerStats* stats, uint32_t* flags, cudaStream_t stream) {
+    const int64_t C = (n + Geo::kChunk - 1) / Geo::kChunk;
+    if (C == 0) return cudaSuccess;
+    if ((P & (P - 1)) == 0)
+        return launch_kernel<Geo, kStats, true>(tab, P, n, C, mean, theta, lr, stats, flags, stream);
+    return launch_kernel<Geo, kStats, false>(tab, P, n, C, mean, theta, lr, stats, flags, stream);
 }
 
 // Launch for one record geometry, with or without statistics.

@@ -577,18 +577,22 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
                 const uint32_t k_hi = k_lo + (1u << 16);
                 const uint32_t k_in = rank_bin ? k_hi : k_lo;
 #pragma unroll
-                for (int v = 0; v < kVec; ++v)
+                for (int v = 0; v < kVec; ++v) {
+                    // a vector's four positions share one bitmap word: one OR per vector
+                    const int j0 = v * kStride + 4 * tid;
+                    uint32_t nib = 0;
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const uint32_t kk = key[4 * v + u];
-                        const int j = v * kStride + 4 * tid + u;
                         if (kk >= k_in) {
-                            atomicOr(&sm.sel_bm[j >> 5], 1u << (j & 31));
+                            nib |= 1u << u;
                         } else if (kk >= k_lo) {
                             const uint32_t slot = atomicAdd(&sm.ncand, 1u);
-                            if (slot < 64u) sm.cand[slot] = make_uint2(kk, static_cast<uint32_t>(j));
+                            if (slot < 64u) sm.cand[slot] = make_uint2(kk, static_cast<uint32_t>(j0 + u));
                         }
                     }
+                    if (nib != 0u) atomicOr(&sm.sel_bm[j0 >> 5], nib << (j0 & 31));
+                }
                 __syncthreads();
                 if (rank_bin && warp == 0) {
                     // rank each candidate among the bin's keys (magnitude, then index)
