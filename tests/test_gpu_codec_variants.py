@@ -207,3 +207,33 @@ def test_variant_many_peers_span_several_groups(codec, P):
     for key in ("rejected", "big", "negative"):
         assert np.array_equal(got[key], ref[key]), key
     assert np.allclose(got["sumsq"], ref["sumsq"], rtol=1e-6, atol=0)
+
+
+@pytest.mark.parametrize("codec", CODECS)
+def test_variant_nonfinite_inputs_flagged_and_deterministic(codec):
+    """Inf and NaN in a few chunks: the records are still the oracle's, bit for bit (a NaN ranks
+    above every number and codes as +0.5 s); scales and the error buffer agree up to NaN bit
+    patterns; the non-finite flag is set."""
+    L, k, _ = codec
+    n = 4 * L + 5
+    delta = synth.laplace(n, 1e-4, synth.generator(9 + L + k, DEV), DEV)
+    delta[100] = float("inf")
+    delta[L + 7] = float("nan")
+    delta[2 * L + 9] = -float("inf")
+    delta[2 * L + 10] = float("nan")
+    delta[3 * L + 1] = float("inf")
+    delta[3 * L + 2] = -float("inf")
+    ef = torch.zeros(n, device=DEV)
+    d_h, e_h = host(delta), host(ef)
+    flags = torch.zeros(1, dtype=torch.int32, device=DEV)
+    payload, scales = spl.ef_compress(delta, ef, 1.0, codec=codec, flags=flags)
+    torch.cuda.synchronize()
+    o_pl, o_sc, o_flags = oracle.ef_compress(d_h, e_h, 1.0, codec=codec)
+    assert int(flags.item()) & spl.FLAG_NONFINITE and o_flags & oracle.FLAG_NONFINITE
+    assert_bit_equal(host(payload), o_pl, f"{codec}: payload with non-finite values")
+    g_sc = host(scales)
+    assert np.array_equal(np.isnan(g_sc), np.isnan(o_sc))
+    fin = ~np.isnan(o_sc)
+    assert_bit_equal(g_sc[fin], o_sc[fin], f"{codec}: scales that are not NaN")
+    g_e = host(ef)
+    assert ((g_e == e_h) | (np.isnan(g_e) & np.isnan(e_h))).all()
