@@ -119,10 +119,6 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
-__device__ __forceinline__ void mbar_inval(uint64_t* bar) {
-    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
 // Orders this thread's earlier generic-proxy shared-memory accesses before later bulk copies.
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -226,16 +222,6 @@ __device__ __forceinline__ void store_record(uint8_t* rec, uint32_t word, int la
     v.z = __shfl_sync(0xffffffffu, word, b + 2);
     v.w = __shfl_sync(0xffffffffu, word, b + 3);
     if (lane < kRecordVec) reinterpret_cast<uint4*>(rec)[lane] = v;
-}
-
-// Field r (0..63) of a record held as 28 words in shared memory.
-__device__ __forceinline__ uint32_t record_field(const uint32_t* words, int r) {
-    const int bit = kFieldBits * r;
-    const int w = bit >> 5;
-    const int off = bit & 31;
-    uint32_t v = words[w] >> off;
-    if (off > 32 - kFieldBits) v |= words[w + 1] << (32 - off);
-    return v & ((1u << kFieldBits) - 1u);
 }
 
 // The same with one funnel shift, for fields of kBits bits.  Reads words[w + 1] even when
