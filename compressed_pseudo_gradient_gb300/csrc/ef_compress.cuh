@@ -34,9 +34,10 @@
 //     assembles the 112-byte record (28 words) at the top of the next iteration, behind the
 //     barrier that already follows the owner step, and stores it as seven 16-byte vectors;
 //     five block barriers per chunk in all;
-//   - mean-abs scale (variant): owners first write the chosen |a| by rank; after a barrier
-//     every warp forms the same pairwise sum in ascending index order and divides by k, then
-//     the owners code as above.
+//   - mean-abs scale (variant): owners write the chosen values and positions by rank and
+//     store the error buffer unchanged; the last warp, after the next iteration's first
+//     barrier, forms the pairwise sum in ascending index order, divides by k, codes the k
+//     entries, writes their residuals over the stored values and packs the record.
 #pragma once
 
 #include <type_traits>
@@ -89,7 +90,7 @@ struct Smem {
     uint2 cand[64];                    // (key, index) of the keys in the boundary bin
     uint32_t ncand;
     uint16_t fields[S::kTopK];         // the record's fields, in ascending index order
-    float absval[kRule == kScaleMeanAbs ? S::kTopK : 1];   // mean-abs: chosen |a| by rank
+    float vals[kRule == kScaleMeanAbs ? S::kTopK : 1];   // mean-abs: chosen a by rank
     uint32_t full_scan;                // the k-th key lies below the top 512 bins
     alignas(16) uint16_t pre[S::kBitmapWords];   // chosen positions before each bitmap word
     uint64_t bar;                      // completes when the stage's bulk copies have landed
@@ -439,6 +440,45 @@ __device__ __forceinline__ void pack_record(const Sm& sm, uint8_t* __restrict__ 
     if (lane == 0) scales[c] = s;
 }
 
+// Mean-abs rule, one warp: the scale from the chosen values (pairwise sum of |a| over ranks
+// 0..k-1 in ascending index order, divided by k: lane l first sums its k/32 consecutive
+// ranks the same way, then the lanes combine as a tree), then each entry's code, its
+// residual written over the error-buffer value stored earlier (pads excluded), and the
+// record.  Runs after a barrier that follows the chunk's owner step and its error-buffer
+// stores, so the residuals land last.
+template <class Geo, class Sm>
+__device__ __forceinline__ void finish_record_mean(Sm& sm, uint8_t* __restrict__ payload,
+                                                   float* __restrict__ scales, int64_t c,
+                                                   float* ef, int valid, int lane) {
+    constexpr int kTopK = Geo::kTopK;
+    constexpr int kPerLane = kTopK / 32;
+    float x[kPerLane];
+    float t[kPerLane];
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+        x[i] = sm.vals[kPerLane * lane + i];
+        t[i] = fabsf(x[i]);
+    }
+#pragma unroll
+    for (int w = 1; w < kPerLane; w <<= 1)
+#pragma unroll
+        for (int i = 0; i + w < kPerLane; i += 2 * w) t[i] = __fadd_rn(t[i], t[i + w]);
+    float sum = t[0];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) sum = __fadd_rn(sum, __shfl_down_sync(0xffffffffu, sum, o));
+    const float s = __fdiv_rn(__shfl_sync(0xffffffffu, sum, 0), static_cast<float>(kTopK));
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+        const int r = kPerLane * lane + i;
+        const uint32_t code = quant_code(x[i], s);
+        const uint32_t pos = static_cast<uint32_t>(sm.fields[r]) >> 2;
+        sm.fields[r] = static_cast<uint16_t>(code | (pos << 2));
+        if (static_cast<int>(pos) < valid) ef[pos] = __fsub_rn(x[i], level_value(code, s));
+    }
+    __syncwarp();
+    pack_record<Geo>(sm, payload, scales, c, s, lane);
+}
+
 template <class Geo, int kRule, bool kBf16, bool kEfHost>
 __global__ void __launch_bounds__(SendShape<Geo>::kThreads, SendShape<Geo>::kMinBlocks)
 k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload,
@@ -476,6 +516,8 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
     bool aborted = false;
     int64_t pend_c = -1;     // the chunk whose record the last warp still has to pack
     float pend_s = 0.0f;
+    float* pend_ef = nullptr;   // mean-abs: that chunk's error buffer and extent
+    int pend_valid = 0;
 
     for (int64_t c = blockIdx.x; c < total; c += gridDim.x) {
         const ChunkRef r = locate<kChunk, kBf16>(tab, c);
@@ -536,7 +578,12 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
         // the last warp packs the previous chunk's record: its fields are complete (the
         // barrier above follows that chunk's owner step) and are next written after this
         // chunk's select
-        if (warp == kWarps - 1 && pend_c >= 0) pack_record<Geo>(sm, payload, scales, pend_c, pend_s, lane);
+        if (warp == kWarps - 1 && pend_c >= 0) {
+            if constexpr (kRule == kScaleMax)
+                pack_record<Geo>(sm, payload, scales, pend_c, pend_s, lane);
+            else
+                finish_record_mean<Geo>(sm, payload, scales, pend_c, pend_ef, pend_valid, lane);
+        }
         uint32_t mkey = 0;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) mkey = max(mkey, sm.warp_max[w]);
@@ -672,46 +719,10 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
         }
         __syncthreads();
 
-        // ---- the scale ---------------------------------------------------------------------
-        float s;
-        if constexpr (kRule == kScaleMax) {
-            s = __fdiv_rn(__uint_as_float(mkey), 1.5f);
-        } else {
-            // owners: each chosen |a| at its rank (ascending index order)
-#pragma unroll
-            for (int v = 0; v < kVec; ++v) {
-                const int j0 = v * kStride + 4 * tid;
-                const uint32_t word = sm.sel_bm[j0 >> 5];
-                const int sh = j0 & 31;
-                if (((word >> sh) & 0xfu) == 0u) continue;
-                const uint32_t base_rank = sm.pre[j0 >> 5];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    if ((word >> (sh + u)) & 1u) {
-                        const uint32_t rank = base_rank + __popc(word & ((1u << (sh + u)) - 1u));
-                        if (rank < kTopK) sm.absval[rank] = fabsf(a[4 * v + u]);
-                    }
-                }
-            }
-            __syncthreads();
-            // every warp forms the same pairwise sum (recursive halving) over ranks 0..k-1:
-            // lane l first sums its k/32 consecutive entries the same way, then the lanes
-            // combine as a tree; so each warp holds the scale without another barrier
-            constexpr int kPerLane = kTopK / 32;
-            float x[kPerLane];
-#pragma unroll
-            for (int i = 0; i < kPerLane; ++i) x[i] = sm.absval[kPerLane * lane + i];
-#pragma unroll
-            for (int w = 1; w < kPerLane; w <<= 1)
-#pragma unroll
-                for (int i = 0; i + w < kPerLane; i += 2 * w) x[i] = __fadd_rn(x[i], x[i + w]);
-            float t = x[0];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) t = __fadd_rn(t, __shfl_down_sync(0xffffffffu, t, o));
-            s = __fdiv_rn(__shfl_sync(0xffffffffu, t, 0), static_cast<float>(kTopK));
-        }
-
-        // ---- owners: rank, code and residual of each chosen value ------------------------
+        // ---- owners: rank, code and residual of each chosen value (mean-abs: rank and
+        //      value only; the last warp codes them once the scale is known) ----------------
+        float s = 0.0f;
+        if constexpr (kRule == kScaleMax) s = __fdiv_rn(__uint_as_float(mkey), 1.5f);
 #pragma unroll
         for (int v = 0; v < kVec; ++v) {
             const int j0 = v * kStride + 4 * tid;
@@ -723,10 +734,15 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
             for (int u = 0; u < 4; ++u) {
                 if ((word >> (sh + u)) & 1u) {
                     const uint32_t rank = base_rank + __popc(word & ((1u << (sh + u)) - 1u));
-                    const uint32_t code = quant_code(a[4 * v + u], s);
-                    a[4 * v + u] = __fsub_rn(a[4 * v + u], level_value(code, s));
-                    if (rank < kTopK)
-                        sm.fields[rank] = static_cast<uint16_t>(code | (static_cast<uint32_t>(j0 + u) << 2));
+                    if constexpr (kRule == kScaleMax) {
+                        const uint32_t code = quant_code(a[4 * v + u], s);
+                        a[4 * v + u] = __fsub_rn(a[4 * v + u], level_value(code, s));
+                        if (rank < kTopK)
+                            sm.fields[rank] = static_cast<uint16_t>(code | (static_cast<uint32_t>(j0 + u) << 2));
+                    } else if (rank < kTopK) {
+                        sm.vals[rank] = a[4 * v + u];
+                        sm.fields[rank] = static_cast<uint16_t>(static_cast<uint32_t>(j0 + u) << 2);
+                    }
                 }
             }
         }
@@ -748,9 +764,16 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
         // ---- the record is packed by the last warp at the top of the next iteration ------
         pend_c = c;
         pend_s = s;
+        pend_ef = r.ef;
+        pend_valid = r.valid;
     }
-    __syncthreads();   // the last chunk's fields are complete
-    if (warp == kWarps - 1 && pend_c >= 0) pack_record<Geo>(sm, payload, scales, pend_c, pend_s, lane);
+    __syncthreads();   // the last chunk's fields (and error-buffer stores) are complete
+    if (warp == kWarps - 1 && pend_c >= 0) {
+        if constexpr (kRule == kScaleMax)
+            pack_record<Geo>(sm, payload, scales, pend_c, pend_s, lane);
+        else
+            finish_record_mean<Geo>(sm, payload, scales, pend_c, pend_ef, pend_valid, lane);
+    }
     if (aborted && tid == 0) {
         // the copy that did not complete may still land: wait once more (bounded) before
         // the CTA's shared memory is released
