@@ -186,3 +186,16 @@ def test_binding_rejects_cpu_tensors():
     x = torch.zeros(4096)
     with pytest.raises(ValueError):
         spl.ef_compress(x, x.clone(), 1.0)
+
+
+def test_header_is_plain_c_and_links(tmp_path, lib):
+    """A C11 program includes spl.h, links libspl.so and calls the host-side entry points."""
+    import subprocess
+    exe = tmp_path / "abi_consumer"
+    src = os.path.join(os.path.dirname(HEADER), "..", "tests", "c", "abi_consumer.c")
+    libdir = os.path.dirname(lib_build.LIB_PATH)
+    subprocess.run(["gcc", "-std=c11", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                    "-I", os.path.dirname(HEADER), src, "-o", str(exe), "-L", libdir, "-lspl",
+                    f"-Wl,-rpath,{libdir}"], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0 and out.stdout.strip() == "ok", out.stdout
