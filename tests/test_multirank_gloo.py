@@ -53,7 +53,8 @@ def test_two_gloo_ranks_share_max_time_and_aggregate():
         assert value == pytest.approx(2 * 1e9 / 2.5 / 1e9)
     seeds = [r[3] for r in res]
     import bench
-    blocks = [set(range(s, s + 25)) | {s + 5000} for s in seeds]
+    blocks = [set(range(s, s + 25)) | {s + 5000} | set(bench.round_seeds(s)) for s in seeds]
+    assert all(len(b) == 25 + 1 + bench.ROUNDS - 1 for b in blocks)   # no clash inside a block
     assert not (blocks[0] & blocks[1])        # each rank draws its own peer's data
 
 
