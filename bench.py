@@ -664,11 +664,22 @@ def cpu_baseline_from_device(buf, chunks: int):
     }
     threads = os.cpu_count() or 1
     secs = time_oracle(sample, threads)
+    # one core, on the first eighth of the sample (the same code on one thread)
+    S1 = max(1, S // 8)
+    one = {k: (v[:S1 * CHUNK] if k in ("delta", "ef", "theta") else v) for k, v in sample.items()}
+    one["chunks"] = S1
+    one["peers_pl"] = [p[:S1] for p in sample["peers_pl"]]
+    one["peers_sc"] = [s[:S1] for s in sample["peers_sc"]]
+    secs1 = time_oracle(one, 1)
     return {"value": round(cpu_sample_bytes(S) / secs / 1e9, 4), "unit": "GB/s",
             "cores": threads, "kind": "oracle",
             "sample": f"first {S} of {N_CHUNKS} chunks of the same workload (compress + "
                       f"24-peer decode with outer step), one pass, {secs:.2f} s wall on "
-                      f"{threads} host threads"}
+                      f"{threads} host threads",
+            "single_core": {"value": round(cpu_sample_bytes(S1) / secs1 / 1e9, 4),
+                            "unit": "GB/s", "cores": 1,
+                            "sample": f"first {S1} chunks, one pass, {secs1:.2f} s on one "
+                                      f"host thread"}}
 
 
 def make_cpu_sample(S: int, seed_base: int = 1):
