@@ -606,3 +606,55 @@ def test_many_peers_span_several_groups(P):
         assert np.array_equal(got[key], ref[key]), key
     assert_bit_equal(got["max_scale"], ref["max_scale"], "max_scale")
     assert np.allclose(got["sumsq"], ref["sumsq"], rtol=1e-6, atol=0)
+
+
+# ---------------------------------------------------------------------------------------------
+# CUDA graphs: the calls are stream-ordered, allocate nothing and never synchronise, so a
+# round can be captured once and replayed
+# ---------------------------------------------------------------------------------------------
+def test_round_captures_into_a_cuda_graph_and_replays_like_eager_calls():
+    n = 9 * 4096 + 5
+    P = 3
+    gen = synth.generator(77, DEV)
+    deltas = [synth.laplace(n, 1e-4, gen, DEV) for _ in range(3)]
+    peers = []
+    for p in range(P):
+        pl, sc = gpu_round(synth.laplace(n, 1e-4, gen, DEV), torch.zeros(n, device=DEV), 1.0)
+        peers.append((pl, sc))
+    theta0 = synth.theta(n, gen, DEV)
+    C = spl.num_chunks(n)
+
+    def make_state():
+        return {"delta": torch.empty(n, device=DEV), "ef": torch.zeros(n, device=DEV),
+                "payload": torch.empty((C, 112), dtype=torch.uint8, device=DEV),
+                "scales": torch.empty(C, device=DEV), "mean": torch.empty(n, device=DEV),
+                "theta": theta0.clone()}
+
+    def step(st):
+        spl.ef_compress(st["delta"], st["ef"], 0.9, payload=st["payload"], scales=st["scales"])
+        spl.decode_aggregate([p[0] for p in peers] + [st["payload"]],
+                             [p[1] for p in peers] + [st["scales"]], n, mean=st["mean"],
+                             theta=st["theta"], lr=0.7)
+
+    eager, graphed = make_state(), make_state()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream(DEV)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):        # warm-up on the capture stream
+        graphed["delta"].copy_(deltas[0])
+        step(graphed)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    for k in ("ef", "theta"):             # restart both from the same state
+        graphed[k].copy_(eager[k])
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step(graphed)
+    for r in range(3):                    # three rounds, a fresh delta each
+        eager["delta"].copy_(deltas[r])
+        step(eager)
+        graphed["delta"].copy_(deltas[r])
+        g.replay()
+    torch.cuda.synchronize()
+    for k in ("payload", "scales", "ef", "mean", "theta"):
+        assert_bit_equal(host(graphed[k]), host(eager[k]), f"graph replay: {k}")
