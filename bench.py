@@ -353,7 +353,8 @@ def run_offload(args, dev):
 
 
 def run_other_workload(args, dev):
-    """Times one round of another workload (same metric: algorithmic bytes per second).
+    """Times one round of another workload (same metric: algorithmic bytes per second), a fresh
+    pseudo-gradient each round (the workload's round count of them, cycled).
     heavy_tail_bf16: 2^27 bf16 compress + 8-peer mean; decoder_layer: the 72B-class layer's
     nine tensors compressed in one multi-tensor call; tiny: 2^20 compress + 4-peer mean."""
     import torch
@@ -361,24 +362,25 @@ def run_other_workload(args, dev):
     from compressed_pseudo_gradient_gb300 import synth
 
     wl = synth.WORKLOADS[args.workload]
-    gen = synth.generator(1, dev)
+    R = wl.rounds
     if wl.name == "decoder_layer":
-        deltas = synth.decoder_layer_round(gen, dev)
-        efs = [torch.zeros_like(d) for d in deltas]
-        sizes = [d.numel() for d in deltas]
+        rounds = [synth.decoder_layer_round(synth.generator(1 + 1000 * r, dev), dev)
+                  for r in range(R)]
+        efs = [torch.zeros_like(d) for d in rounds[0]]
+        sizes = [d.numel() for d in rounds[0]]
         C = sum((k + CHUNK - 1) // CHUNK for k in sizes)
         payload = torch.empty((C, RECORD), dtype=torch.uint8, device=dev)
         scales = torch.empty(C, dtype=torch.float32, device=dev)
         step_bytes = sum(compress_bytes(k, (k + CHUNK - 1) // CHUNK) for k in sizes)
 
-        def step():
-            spl.ef_compress_multi(deltas, efs, wl.beta, payload=payload, scales=scales)
+        def step(r):
+            spl.ef_compress_multi(rounds[r % R], efs, wl.beta, payload=payload, scales=scales)
             return 1
         n, dtype = sum(sizes), "f32"
     else:
         n = wl.n
         C = (n + CHUNK - 1) // CHUNK
-        delta = synth.delta_round(wl, gen, dev)
+        rounds = [synth.delta_round(wl, synth.generator(1 + 1000 * r, dev), dev) for r in range(R)]
         ef = torch.zeros(n, dtype=torch.float32, device=dev)
         payload = torch.empty((C, RECORD), dtype=torch.uint8, device=dev)
         scales = torch.empty(C, dtype=torch.float32, device=dev)
@@ -391,44 +393,49 @@ def run_other_workload(args, dev):
             pls.append(pl)
             scs.append(sc)
         mean = torch.empty(n, dtype=torch.float32, device=dev)
-        esz = 2 if delta.dtype == torch.bfloat16 else 4
+        esz = 2 if rounds[0].dtype == torch.bfloat16 else 4
         step_bytes = (esz + 8) * n + (RECORD + 4) * C + decode_bytes(n, C, wl.peers, theta=False)
 
-        def step():
-            spl.ef_compress(delta, ef, wl.beta, payload=payload, scales=scales)
+        def step(r):
+            spl.ef_compress(rounds[r % R], ef, wl.beta, payload=payload, scales=scales)
             spl.decode_aggregate(pls, scs, n, mean=mean)
             return 2
         dtype = "bf16" if esz == 2 else "f32"
-    def timed(run_once):
+
+    def timed(run_round):
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
         start.record()
-        for _ in range(args.steps):
-            run_once()
+        for k in range(args.steps):
+            run_round(k)
         end.record()
         torch.cuda.synchronize(dev)
         return start.elapsed_time(end) / 1e3
 
-    for _ in range(args.warmup):
-        step()
+    for k in range(args.warmup):
+        step(k)
     torch.cuda.synchronize(dev)
     eager_secs = timed(step)
-    launches = step() * args.steps
-    # the step captured once into a CUDA graph and replayed: the calls are stream-ordered and
-    # never allocate or synchronise, so a launch-bound step sheds its per-call host cost
+    launches = step(0) * args.steps
+    # each round's step captured once into a CUDA graph and replayed in turn: the calls are
+    # stream-ordered and never allocate or synchronise, so a launch-bound step sheds its
+    # per-call host cost
     side = torch.cuda.Stream(dev)
     side.wait_stream(torch.cuda.current_stream(dev))
     with torch.cuda.stream(side):
-        step()
+        step(0)
     torch.cuda.current_stream(dev).wait_stream(side)
     torch.cuda.synchronize(dev)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        step()
-    for _ in range(args.warmup):
-        graph.replay()
+    graphs = []
+    for r in range(R):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step(r)
+        graphs.append(g)
+    for k in range(args.warmup):
+        graphs[k % R].replay()
     torch.cuda.synchronize(dev)
-    graph_secs = timed(graph.replay)
+    graph_secs = timed(lambda k: graphs[k % R].replay())
     # the faster launch mode is the one a user would take: graphs pay off where launches bound
     # the step (tiny), plain calls where the kernels do
     use_graph = graph_secs < eager_secs
@@ -440,7 +447,7 @@ def run_other_workload(args, dev):
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * secs / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
-            "config": {"workload": wl.name, "n": n, "step_bytes": step_bytes,
+            "config": {"workload": wl.name, "n": n, "rounds": R, "step_bytes": step_bytes,
                        "frac_of_hbm": round(value / peak, 4), "peak_kind": kind,
                        "launch": "CUDA graph of the step, replayed" if use_graph
                                  else "plain calls",
