@@ -56,12 +56,14 @@ constexpr int kStages = SPL_DECODE_STAGES;
 
 // Per-codec sizes of the receiver (default: 256 threads, 512 positions and 4 vectors per
 // thread of each warp, groups of 64 peers, two entries per lane, seven 16-byte pieces per
-// record).
+// record).  L = 2048 takes 128 threads (8 CTAs per SM hide its per-chunk fixed costs at the
+// usual peer counts: 0.67 -> 0.56 ms at 24 peers, 2^28 values; 200 peers, where shared memory
+// allows fewer CTAs, run 11 % slower), L = 8192 takes 512, so a warp still holds 512 positions.
 template <class Geo>
 struct RecvShape {
     static constexpr int kChunk = Geo::kChunk;
     static constexpr int kTopK = Geo::kTopK;
-    static constexpr int kThreads = kChunk == 8192 ? SPL_DECODE_THREADS_8192 : 256;
+    static constexpr int kThreads = kChunk == 8192 ? SPL_DECODE_THREADS_8192 : (kChunk == 2048 ? 128 : 256);
     static constexpr int kWarps = kThreads / 32;
     static constexpr int kSlice = kChunk / kWarps;          // positions per warp
     static constexpr int kVec = kSlice / 128;               // vectors of 4 per thread
@@ -72,7 +74,9 @@ struct RecvShape {
     static constexpr int kPieceBytes = Geo::kVecRecords ? 16 : 4;
     static constexpr int kPieces = Geo::kRecordBytes / kPieceBytes;   // copies per record
     static constexpr int kMinBlocks = kThreads == 256 && kChunk > 4096 ? 2 : 1024 / kThreads;
-    static_assert(32 * kWarps >= kMaxPeers, "one scale per lane for up to 256 peers");
+    // scales a lane carries: peer (32 W) i + W lane + w in slot i, for up to 256 peers
+    static constexpr int kScalesPerLane = (kMaxPeers + 32 * kWarps - 1) / (32 * kWarps);
+    static_assert(kScalesPerLane <= 2, "scale slots per lane");
 };
 
 __host__ __device__ constexpr size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
@@ -178,7 +182,10 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
     if (static_cast<int64_t>(blockIdx.x) >= C) return;
     const float pf = static_cast<float>(P);
     const int slice0 = kSlice * warp;    // this warp's positions: slice0 + 128 v + 4 lane + u
-    const int my_peer = kWarps * lane + warp;   // the peer whose scale this lane carries
+    constexpr int kSpl = S::kScalesPerLane;
+    int my_peer[kSpl];                            // the peers whose scales this lane carries
+#pragma unroll
+    for (int i = 0; i < kSpl; ++i) my_peer[i] = 32 * kWarps * i + kWarps * lane + warp;
 
 #pragma unroll
     for (int v = 0; v < kVec; ++v)
@@ -201,7 +208,10 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
             prefetch<Geo>(tab, P, c, (c + 1) * kChunk <= n, theta, &bars[st],
                      st_rec + st * P * kRecordBytes, st_theta + st * kChunk, tid);
     }
-    float sc_cur = my_peer < P ? __ldcs(tab.scale[my_peer] + blockIdx.x) : 0.0f;
+    float sc_cur[kSpl];
+#pragma unroll
+    for (int i = 0; i < kSpl; ++i)
+        sc_cur[i] = my_peer[i] < P ? __ldcs(tab.scale[my_peer[i]] + blockIdx.x) : 0.0f;
 
     bool bad = false;
     bool aborted = false;
@@ -223,7 +233,9 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
                 th[v] = *reinterpret_cast<const float4*>(
                     &st_theta[st * kChunk + slice0 + 128 * v + 4 * lane]);
         }
-        float sc_next = 0.0f;
+        float sc_next[kSpl];
+#pragma unroll
+        for (int i = 0; i < kSpl; ++i) sc_next[i] = 0.0f;
 
         for (int g0 = 0; g0 < P; g0 += kGroup) {
             const int gn = P - g0 < kGroup ? P - g0 : kGroup;
@@ -251,7 +263,9 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
                         asc = asc && (lane == 31 || ix[m] < next);
                     }
                 }
-                const float s = __shfl_sync(0xffffffffu, sc_cur, p / kWarps);
+                const int slot = p / (32 * kWarps);   // the same for the whole warp
+                const float sv = (kSpl == 1 || slot == 0) ? sc_cur[0] : sc_cur[kSpl - 1];
+                const float s = __shfl_sync(0xffffffffu, sv, (p / kWarps) % 32);
                 const bool ok = __all_sync(0xffffffffu, asc) && s >= 0.0f && s <= FLT_MAX;
                 if (ok) {
                     uint2* eg = ent + g * kTopK;
@@ -283,7 +297,9 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
                 if (c2 < C)
                     prefetch<Geo>(tab, P, c2, (c2 + 1) * kChunk <= n, theta, &bars[st],
                              st_rec + st * P * kRecordBytes, st_theta + st * kChunk, tid);
-                if (my_peer < P && c + G < C) sc_next = __ldcs(tab.scale[my_peer] + c + G);
+#pragma unroll
+                for (int i = 0; i < kSpl; ++i)
+                    if (my_peer[i] < P && c + G < C) sc_next[i] = __ldcs(tab.scale[my_peer[i]] + c + G);
             } else {
                 __syncthreads();
             }
@@ -343,7 +359,8 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
             __syncthreads();   // the accumulator is complete; entries are rewritten next pass
         }
         if (aborted) break;
-        sc_cur = sc_next;
+#pragma unroll
+        for (int i = 0; i < kSpl; ++i) sc_cur[i] = sc_next[i];
 
         // ---- dense pass: mean, outer step --------------------------------------------------
 #pragma unroll
