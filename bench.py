@@ -67,8 +67,6 @@ CODECS = [(4096, 64, 0), (4096, 64, 1), (4096, 32, 0), (4096, 32, 1), (4096, 128
           (4096, 128, 1), (2048, 32, 0), (2048, 32, 1), (8192, 128, 0), (8192, 128, 1)]
 
 
-STEP_BYTES = compress_bytes(N_ELEMS, N_CHUNKS) + decode_bytes(N_ELEMS, N_CHUNKS, PEERS)
-
 
 # ---------------------------------------------------------------------------------------------
 # Distributed helpers (one process per GPU; NCCL on GPUs, gloo on CPU)
