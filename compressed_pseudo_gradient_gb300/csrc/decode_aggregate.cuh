@@ -44,15 +44,11 @@
 namespace spl {
 namespace {
 
-#ifndef SPL_DECODE_STAGES
-#define SPL_DECODE_STAGES 1
-#endif
-
-constexpr int kStages = SPL_DECODE_STAGES;
-
-#ifndef SPL_DECODE_THREADS_8192
-#define SPL_DECODE_THREADS_8192 512
-#endif
+// Prefetch stages in flight per CTA (chunk c + k G's copies go to stage k): one, since the
+// decode is bound by its instructions, not by waits on copies.  The loops and the shared
+// memory layout (room for two mbarriers) also take two.
+constexpr int kStages = 1;
+static_assert(kStages == 1 || kStages == 2, "prefetch stages");
 
 // Per-codec sizes of the receiver (default: 256 threads, 512 positions and 4 vectors per
 // thread of each warp, groups of 64 peers, two entries per lane, seven 16-byte pieces per
@@ -63,7 +59,7 @@ template <class Geo>
 struct RecvShape {
     static constexpr int kChunk = Geo::kChunk;
     static constexpr int kTopK = Geo::kTopK;
-    static constexpr int kThreads = kChunk == 8192 ? SPL_DECODE_THREADS_8192 : (kChunk == 2048 ? 128 : 256);
+    static constexpr int kThreads = kChunk == 8192 ? 512 : (kChunk == 2048 ? 128 : 256);
     static constexpr int kWarps = kThreads / 32;
     static constexpr int kSlice = kChunk / kWarps;          // positions per warp
     static constexpr int kVec = kSlice / 128;               // vectors of 4 per thread

@@ -51,13 +51,6 @@ namespace {
 constexpr uint32_t kWindow = (2048u << 16) - 1u;   // 16 octaves of magnitude keys: 2048 bins
 constexpr uint32_t kNotFound = 0xffffffffu;
 
-#ifndef SPL_COMPRESS_THREADS_4096
-#define SPL_COMPRESS_THREADS_4096 256
-#endif
-#ifndef SPL_COMPRESS_MIN_BLOCKS_4096
-#define SPL_COMPRESS_MIN_BLOCKS_4096 4
-#endif
-
 // Per-codec sizes of the sender.  A CTA of L / 16 threads works on one chunk, 16 values per
 // thread (default: 256 threads, 4 vectors per thread, 128 bitmap words, 4 per lane of warp 0),
 // and 1024 / threads CTAs share an SM (64 registers per thread, 32 warps per SM).
@@ -65,14 +58,14 @@ template <class Geo>
 struct SendShape {
     static constexpr int kChunk = Geo::kChunk;
     static constexpr int kTopK = Geo::kTopK;
-    static constexpr int kThreads = kChunk == 4096 ? SPL_COMPRESS_THREADS_4096 : kChunk / 16;
+    static constexpr int kThreads = kChunk / 16;
     static constexpr int kWarps = kThreads / 32;
     static constexpr int kPer = kChunk / kThreads;       // values per thread
     static constexpr int kVec = kPer / 4;                // vectors of 4 per thread
     static constexpr int kStride = 4 * kThreads;         // between a thread's vectors
     static constexpr int kBitmapWords = kChunk / 32;
     static constexpr int kWordsPerLane = kBitmapWords / 32;
-    static constexpr int kMinBlocks = kChunk == 4096 ? SPL_COMPRESS_MIN_BLOCKS_4096 : 1024 / kThreads;
+    static constexpr int kMinBlocks = 1024 / kThreads;
     static_assert(kPer % 4 == 0 && kThreads % 32 == 0 && 2048 % kThreads == 0, "sender shape");
 };
 
