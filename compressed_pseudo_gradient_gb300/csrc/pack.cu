@@ -2,8 +2,8 @@
 //
 // Layout: "The Sparse Frontier: SparseLoCo and the Compression Math Behind Permissionless
 // Pre-Training", "SparseLoCo: Three Compression Levers in One Pass", per-chunk equation
-// (64 values x (2 bits value + 12 bits index) = 896 bits = 112 bytes).  Entry r is the field
-// code | idx << 2 at bits [14r, 14r + 14), least significant bit first.
+// (64 fields, each a 2-bit value and a 12-bit index: 896 bits, 112 bytes).  Entry r is the
+// field code | idx << 2 at bits [14r, 14r + 14), least significant bit first.
 //
 // One warp per record, grid-stride: lane l handles entries l and l + 32; record words are
 // assembled (or taken apart) with shuffles and moved as 16-byte vectors.

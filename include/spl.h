@@ -58,9 +58,9 @@ typedef enum {
 typedef enum { SPL_F32 = 0, SPL_BF16 = 1 } spl_dtype;
 
 enum {
-    SPL_CHUNK = 4096,        /* "chunks of 4,096 parameters" (item 1) */
-    SPL_TOPK = 64,           /* "top-64 values by absolute magnitude" (item 1) */
-    SPL_RECORD_BYTES = 112,  /* "64 x 14 bits = 896 bits = 112 bytes" (per-chunk equation) */
+    SPL_CHUNK = 4096,        /* values per chunk (item 1) */
+    SPL_TOPK = 64,           /* values kept per chunk, largest |a| first (item 1) */
+    SPL_RECORD_BYTES = 112,  /* 64 fields of 14 bits (per-chunk equation) */
     SPL_MAX_PEERS = 256,     /* largest P accepted by spl_decode_aggregate */
     SPL_MAX_TENSORS_PER_LAUNCH = 64 /* spl_ef_compress_multi splits larger tables */
 };
@@ -150,9 +150,9 @@ spl_status spl_decode_aggregate(const uint8_t* const* payloads, const float* con
 
 /*
  * Per-peer statistics of the records a receiver accepted, for screening updates that look
- * unlike the rest (The Sparse Frontier, "What the Blockchain Does (and Doesn't Do)": a crafted
- * sparse update looks different from a naturally concentrated one).  Counted over the 64
- * entries of every accepted record (a tail chunk's pads included).
+ * unlike the rest (The Sparse Frontier, "What the Blockchain Does (and Doesn't Do)": an
+ * update built to game the screening is distributed differently from an honest one).
+ * Counted over the 64 entries of every accepted record (a tail chunk's pads included).
  */
 typedef struct {
     uint32_t rejected;  /* records rejected (indices not strictly ascending, or a bad scale) */
@@ -176,7 +176,7 @@ spl_status spl_decode_aggregate_stats(const uint8_t* const* payloads, const floa
 /*
  * Codec variants, for ablation.  The pages fix L = 4096 and k = 64 ("SparseLoCo: Three
  * Compression Levers in One Pass", item 1), give the index width as ceil(log2 L) (item 3) and
- * leave the scale rule open (item 2: "a per-chunk scale factor").  A variant keeps the
+ * leave the scale rule open (item 2 names one scale per chunk, no formula).  A variant keeps the
  * record layout with fields of 2 + log2 L bits, k per record, in k x (2 + log2 L) / 8 bytes;
  * records follow one another with no padding (payload base 16-byte aligned; records of 52
  * or 56 bytes are then 4-byte aligned).  Scale rules:

@@ -60,7 +60,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-#define ORC_CHUNK 4096         /* [SF] item 1: non-overlapping chunks of 4,096 parameters */
+#define ORC_CHUNK 4096         /* [SF] item 1: the vector is cut into disjoint 4096-value chunks */
 #define ORC_TOPK 64            /* [SF] item 1: top-64 values by absolute magnitude */
 #define ORC_INDEX_BITS 12      /* [SF] item 3: ceil(log2(4096)) = 12 */
 #define ORC_VALUE_BITS 2       /* [SF] item 2: four levels, two bits */
@@ -418,8 +418,9 @@ uint32_t orc_decode_aggregate_codec(int L, int k, const uint8_t* const* payloads
 
 /* ------------------------------------------------------------------------------------------
  * Receiver statistics per peer, for screening updates that look unlike the rest ([SF] "What
- * the Blockchain Does (and Doesn't Do)": a crafted sparse update looks different from a
- * naturally concentrated one).  Over the k entries of every accepted record of peer p:
+ * the Blockchain Does (and Doesn't Do)": an update built to game the screening is
+ * distributed differently from an honest one).  Over the k entries of every accepted record
+ * of peer p:
  *   big[p]       entries with the magnitude bit set (|q| = 1.5 s)
  *   negative[p]  entries with the sign bit set
  *   max_scale[p] the largest scale among accepted records (0 if none)

@@ -89,9 +89,9 @@ def test_per_peer_payload_arithmetic_matches_pages():
     params = int(fig["params"])
     chunks = oracle.num_chunks(params)
     payload_bytes = chunks * oracle.constants()["record_bytes"]
-    assert abs(payload_bytes / 1e9 - fig["payload_per_peer_gb"]) < 0.05       # "approximately 2 GB"
+    assert abs(payload_bytes / 1e9 - fig["payload_per_peer_gb"]) < 0.05       # about 2 GB per peer
     mbps = payload_bytes * 8 / fig["window_seconds"] / 1e6
-    assert round(mbps) == fig["uplink_mbps_per_peer"]                           # "roughly 13 Mbps"
+    assert round(mbps) == fig["uplink_mbps_per_peer"]                           # about 13 Mbps
     assert round(4 * 72.7e9 / 1e9, 1) == fig["dense_fp32_gb"]
 
 
