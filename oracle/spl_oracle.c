@@ -14,8 +14,8 @@
  *             per-chunk size equation (64 x (2 + 12) bits = 896 bits = 112 bytes);
  *           - "Why Extreme Sparsity Doesn't Break Convergence", paragraphs "Error feedback
  *             accumulation" and "Sparse aggregation can improve model quality";
- *           - "Why DiLoCo Alone Isn't Enough" (the pseudo-gradient is the difference of the
- *             pre- and post-inner-loop weights).
+ *           - "Why DiLoCo Alone Isn't Enough" (the pseudo-gradient is how far the inner
+ *             optimisation moved the weights).
  *   [CV]  "Covenant-72B: Decentralized Training is No Longer Just a Dream" (wispaper.ai),
  *         "Methodology", item 1 (top-k sparsification + 2-bit quantisation, error feedback).
  *
@@ -61,7 +61,7 @@
 #include <string.h>
 
 #define ORC_CHUNK 4096         /* [SF] item 1: the vector is cut into disjoint 4096-value chunks */
-#define ORC_TOPK 64            /* [SF] item 1: top-64 values by absolute magnitude */
+#define ORC_TOPK 64            /* [SF] item 1: the 64 largest |a| of each chunk are kept */
 #define ORC_INDEX_BITS 12      /* [SF] item 3: ceil(log2(4096)) = 12 */
 #define ORC_VALUE_BITS 2       /* [SF] item 2: four levels, two bits */
 #define ORC_FIELD_BITS (ORC_VALUE_BITS + ORC_INDEX_BITS)
