@@ -29,15 +29,16 @@
 //     [19:9] and [8:0] with ties to the lowest indices; the chosen positions end up in a
 //     4096-bit shared bitmap;
 //   - one warp turns the bitmap into per-word prefix counts, from which every thread that
-//     owns a chosen value knows its rank in ascending index order; it computes the code and
-//     the residual in registers and writes its 14-bit field to shared memory; the last warp
-//     assembles the 112-byte record (28 words) at the top of the next iteration, behind the
-//     barrier that already follows the owner step, and stores it as seven 16-byte vectors;
-//     five block barriers per chunk in all;
-//   - mean-abs scale (variant): owners write the chosen values and positions by rank and
-//     store the error buffer unchanged; the last warp, after the next iteration's first
-//     barrier, forms the pairwise sum in ascending index order, divides by k, codes the k
-//     entries, writes their residuals over the stored values and packs the record.
+//     owns a chosen value knows its rank in ascending index order; it writes the value and
+//     its position to shared memory by rank, and every thread stores its error-buffer values
+//     unchanged; the last warp, at the top of the next iteration behind the barrier that
+//     already follows the owner step (overlapping the histogram), codes the 64 entries,
+//     writes their residuals over the stored values, assembles the 112-byte record (28
+//     words) and stores it as seven 16-byte vectors; five block barriers per chunk in all;
+//   - mean-abs scale (variant): the same, the last warp first forming the scale (pairwise sum
+//     in ascending index order, divided by k);
+//   - error buffer in host memory: the owners code their values and form the residuals in
+//     registers instead, so the buffer crosses the host link once, in whole vectors.
 #pragma once
 
 #include <type_traits>
@@ -83,7 +84,7 @@ struct Smem {
     uint2 cand[64];                    // (key, index) of the keys in the boundary bin
     uint32_t ncand;
     uint16_t fields[S::kTopK];         // the record's fields, in ascending index order
-    float vals[kRule == kScaleMeanAbs ? S::kTopK : 1];   // mean-abs: chosen a by rank
+    float vals[S::kTopK];              // the chosen a by rank (coded once the record is packed)
     uint32_t full_scan;                // the k-th key lies below the top 512 bins
     alignas(16) uint16_t pre[S::kBitmapWords];   // chosen positions before each bitmap word
     uint64_t bar;                      // completes when the stage's bulk copies have landed
@@ -433,33 +434,35 @@ __device__ __forceinline__ void pack_record(const Sm& sm, uint8_t* __restrict__ 
     if (lane == 0) scales[c] = s;
 }
 
-// Mean-abs rule, one warp: the scale from the chosen values (pairwise sum of |a| over ranks
-// 0..k-1 in ascending index order, divided by k: lane l first sums its k/32 consecutive
-// ranks the same way, then the lanes combine as a tree), then each entry's code, its
-// residual written over the error-buffer value stored earlier (pads excluded), and the
-// record.  Runs after a barrier that follows the chunk's owner step and its error-buffer
-// stores, so the residuals land last.
-template <class Geo, class Sm>
-__device__ __forceinline__ void finish_record_mean(Sm& sm, uint8_t* __restrict__ payload,
-                                                   float* __restrict__ scales, int64_t c,
-                                                   float* ef, int valid, int lane) {
+// One warp: each chosen entry's code, its residual written over the error-buffer value
+// stored earlier (pads excluded), and the record.  The max-abs scale comes in as s; the
+// mean-abs scale is formed here from the chosen values (pairwise sum of |a| over ranks 0..k-1
+// in ascending index order, divided by k: lane l first sums its k/32 consecutive ranks the
+// same way, then the lanes combine as a tree).  Runs after a barrier that follows the chunk's
+// owner step and its error-buffer stores, so the residuals land last.
+template <class Geo, int kRule, class Sm>
+__device__ __forceinline__ void finish_record(Sm& sm, uint8_t* __restrict__ payload,
+                                              float* __restrict__ scales, int64_t c, float s,
+                                              float* ef, int valid, int lane) {
     constexpr int kTopK = Geo::kTopK;
     constexpr int kPerLane = kTopK / 32;
     float x[kPerLane];
-    float t[kPerLane];
 #pragma unroll
-    for (int i = 0; i < kPerLane; ++i) {
-        x[i] = sm.vals[kPerLane * lane + i];
-        t[i] = fabsf(x[i]);
+    for (int i = 0; i < kPerLane; ++i) x[i] = sm.vals[kPerLane * lane + i];
+    if constexpr (kRule == kScaleMeanAbs) {
+        float t[kPerLane];
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) t[i] = fabsf(x[i]);
+#pragma unroll
+        for (int w = 1; w < kPerLane; w <<= 1)
+#pragma unroll
+            for (int i = 0; i + w < kPerLane; i += 2 * w) t[i] = __fadd_rn(t[i], t[i + w]);
+        float sum = t[0];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1)
+            sum = __fadd_rn(sum, __shfl_down_sync(0xffffffffu, sum, o));
+        s = __fdiv_rn(__shfl_sync(0xffffffffu, sum, 0), static_cast<float>(kTopK));
     }
-#pragma unroll
-    for (int w = 1; w < kPerLane; w <<= 1)
-#pragma unroll
-        for (int i = 0; i + w < kPerLane; i += 2 * w) t[i] = __fadd_rn(t[i], t[i + w]);
-    float sum = t[0];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) sum = __fadd_rn(sum, __shfl_down_sync(0xffffffffu, sum, o));
-    const float s = __fdiv_rn(__shfl_sync(0xffffffffu, sum, 0), static_cast<float>(kTopK));
 #pragma unroll
     for (int i = 0; i < kPerLane; ++i) {
         const int r = kPerLane * lane + i;
@@ -488,6 +491,10 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
     constexpr int kFieldBits = Geo::kFieldBits;
     constexpr int kRecordWords = Geo::kRecordWords;
     constexpr int kRecordBytes = Geo::kRecordBytes;
+    // with the error buffer in host memory the owners code their values and form the residual
+    // in registers (64 scattered 4-byte writes per chunk would cost the host link more than
+    // the divergent owner step costs); otherwise the packing warp does it
+    constexpr bool kCodeInPlace = kEfHost && kRule == kScaleMax;
     using Sm = Smem<Geo, kRule>;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Sm& sm = *reinterpret_cast<Sm*>(smem_raw);
@@ -572,10 +579,10 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
         // barrier above follows that chunk's owner step) and are next written after this
         // chunk's select
         if (warp == kWarps - 1 && pend_c >= 0) {
-            if constexpr (kRule == kScaleMax)
+            if constexpr (kCodeInPlace)
                 pack_record<Geo>(sm, payload, scales, pend_c, pend_s, lane);
             else
-                finish_record_mean<Geo>(sm, payload, scales, pend_c, pend_ef, pend_valid, lane);
+                finish_record<Geo, kRule>(sm, payload, scales, pend_c, pend_s, pend_ef, pend_valid, lane);
         }
         uint32_t mkey = 0;
 #pragma unroll
@@ -712,8 +719,8 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
         }
         __syncthreads();
 
-        // ---- owners: rank, code and residual of each chosen value (mean-abs: rank and
-        //      value only; the last warp codes them once the scale is known) ----------------
+        // ---- owners: rank and value of each chosen value (the last warp codes them and
+        //      writes their residuals; with a host error buffer, code and residual here) -----
         float s = 0.0f;
         if constexpr (kRule == kScaleMax) s = __fdiv_rn(__uint_as_float(mkey), 1.5f);
 #pragma unroll
@@ -727,7 +734,7 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
             for (int u = 0; u < 4; ++u) {
                 if ((word >> (sh + u)) & 1u) {
                     const uint32_t rank = base_rank + __popc(word & ((1u << (sh + u)) - 1u));
-                    if constexpr (kRule == kScaleMax) {
+                    if constexpr (kCodeInPlace) {
                         const uint32_t code = quant_code(a[4 * v + u], s);
                         a[4 * v + u] = __fsub_rn(a[4 * v + u], level_value(code, s));
                         if (rank < kTopK)
@@ -762,10 +769,10 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
     }
     __syncthreads();   // the last chunk's fields (and error-buffer stores) are complete
     if (warp == kWarps - 1 && pend_c >= 0) {
-        if constexpr (kRule == kScaleMax)
+        if constexpr (kCodeInPlace)
             pack_record<Geo>(sm, payload, scales, pend_c, pend_s, lane);
         else
-            finish_record_mean<Geo>(sm, payload, scales, pend_c, pend_ef, pend_valid, lane);
+            finish_record<Geo, kRule>(sm, payload, scales, pend_c, pend_s, pend_ef, pend_valid, lane);
     }
     if (aborted && tid == 0) {
         // the copy that did not complete may still land: wait once more (bounded) before
