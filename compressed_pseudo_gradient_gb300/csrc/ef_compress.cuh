@@ -37,8 +37,9 @@
 //     words) and stores it as seven 16-byte vectors; five block barriers per chunk in all;
 //   - mean-abs scale (variant): the same, the last warp first forming the scale (pairwise sum
 //     in ascending index order, divided by k);
-//   - error buffer in host memory: the owners code their values and form the residuals in
-//     registers instead, so the buffer crosses the host link once, in whole vectors.
+//   - error buffer in host memory, and k = 128 under the max-abs rule: the owners code their
+//     values and form the residuals in registers instead (the host buffer then crosses the
+//     link once, in whole vectors; the packing warp's work stays short).
 #pragma once
 
 #include <type_traits>
@@ -434,22 +435,29 @@ __device__ __forceinline__ void pack_record(const Sm& sm, uint8_t* __restrict__ 
     if (lane == 0) scales[c] = s;
 }
 
-// One warp: each chosen entry's code, its residual written over the error-buffer value
-// stored earlier (pads excluded), and the record.  The max-abs scale comes in as s; the
-// mean-abs scale is formed here from the chosen values (pairwise sum of |a| over ranks 0..k-1
-// in ascending index order, divided by k: lane l first sums its k/32 consecutive ranks the
-// same way, then the lanes combine as a tree).  Runs after a barrier that follows the chunk's
-// owner step and its error-buffer stores, so the residuals land last.
+// One warp: the scale, each chosen entry's code, its residual written over the error-buffer
+// value stored earlier (pads excluded), and the record.  The scale comes from the chosen
+// values: max-abs from the largest magnitude key among them (the chunk's largest key is always
+// chosen, so this is the chunk maximum, NaN included); mean-abs from the pairwise sum of |a|
+// over ranks 0..k-1 in ascending index order, divided by k (lane l first sums its k/32
+// consecutive ranks the same way, then the lanes combine as a tree).  Runs after a barrier
+// that follows the chunk's owner step and its error-buffer stores, so the residuals land last.
 template <class Geo, int kRule, class Sm>
 __device__ __forceinline__ void finish_record(Sm& sm, uint8_t* __restrict__ payload,
-                                              float* __restrict__ scales, int64_t c, float s,
-                                              float* ef, int valid, int lane) {
+                                              float* __restrict__ scales, int64_t c, float* ef,
+                                              int valid, int lane) {
     constexpr int kTopK = Geo::kTopK;
     constexpr int kPerLane = kTopK / 32;
     float x[kPerLane];
 #pragma unroll
     for (int i = 0; i < kPerLane; ++i) x[i] = sm.vals[kPerLane * lane + i];
-    if constexpr (kRule == kScaleMeanAbs) {
+    float s;
+    if constexpr (kRule == kScaleMax) {
+        uint32_t kmax = 0;
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) kmax = max(kmax, mag_key(x[i]));
+        s = __fdiv_rn(__uint_as_float(__reduce_max_sync(0xffffffffu, kmax)), 1.5f);
+    } else {
         float t[kPerLane];
 #pragma unroll
         for (int i = 0; i < kPerLane; ++i) t[i] = fabsf(x[i]);
@@ -491,10 +499,12 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
     constexpr int kFieldBits = Geo::kFieldBits;
     constexpr int kRecordWords = Geo::kRecordWords;
     constexpr int kRecordBytes = Geo::kRecordBytes;
-    // with the error buffer in host memory the owners code their values and form the residual
-    // in registers (64 scattered 4-byte writes per chunk would cost the host link more than
-    // the divergent owner step costs); otherwise the packing warp does it
-    constexpr bool kCodeInPlace = kEfHost && kRule == kScaleMax;
+    // max-abs scale: the packing warp codes the chosen values and writes their residuals
+    // (it overlaps the histogram), except where the owners do it cheaper in registers: with
+    // the error buffer in host memory (k scattered 4-byte writes per chunk would cost the
+    // host link more than the divergent owner step costs) and for k = 128 (four entries per
+    // lane of the packing warp then outlast the histogram: +1 % at L = 4096, +4 % at 8192)
+    constexpr bool kCodeInPlace = kRule == kScaleMax && (kEfHost || kTopK > 64);
     using Sm = Smem<Geo, kRule>;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Sm& sm = *reinterpret_cast<Sm*>(smem_raw);
@@ -582,7 +592,7 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
             if constexpr (kCodeInPlace)
                 pack_record<Geo>(sm, payload, scales, pend_c, pend_s, lane);
             else
-                finish_record<Geo, kRule>(sm, payload, scales, pend_c, pend_s, pend_ef, pend_valid, lane);
+                finish_record<Geo, kRule>(sm, payload, scales, pend_c, pend_ef, pend_valid, lane);
         }
         uint32_t mkey = 0;
 #pragma unroll
@@ -721,8 +731,8 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
 
         // ---- owners: rank and value of each chosen value (the last warp codes them and
         //      writes their residuals; with a host error buffer, code and residual here) -----
-        float s = 0.0f;
-        if constexpr (kRule == kScaleMax) s = __fdiv_rn(__uint_as_float(mkey), 1.5f);
+        float s = 0.0f;   // coding in place: the max-abs scale
+        if constexpr (kCodeInPlace) s = __fdiv_rn(__uint_as_float(mkey), 1.5f);
 #pragma unroll
         for (int v = 0; v < kVec; ++v) {
             const int j0 = v * kStride + 4 * tid;
@@ -772,7 +782,7 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
         if constexpr (kCodeInPlace)
             pack_record<Geo>(sm, payload, scales, pend_c, pend_s, lane);
         else
-            finish_record<Geo, kRule>(sm, payload, scales, pend_c, pend_s, pend_ef, pend_valid, lane);
+            finish_record<Geo, kRule>(sm, payload, scales, pend_c, pend_ef, pend_valid, lane);
     }
     if (aborted && tid == 0) {
         // the copy that did not complete may still land: wait once more (bounded) before
