@@ -505,6 +505,11 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
     // host link more than the divergent owner step costs) and for k = 128 (four entries per
     // lane of the packing warp then outlast the histogram: +1 % at L = 4096, +4 % at 8192)
     constexpr bool kCodeInPlace = kRule == kScaleMax && (kEfHost || kTopK > 64);
+    // the out-of-line select takes the keys through memory.  Handing it a copy made on that
+    // path keeps the key registers from also being stored to the stack on every chunk (-4.5 %
+    // at k = 64); where registers are scarcer (k = 128, a host error buffer) the copy makes
+    // the compiler spill more in the loop instead, so there the keys are passed directly
+    constexpr bool kCopyKeys = kTopK <= 64 && !kEfHost;
     using Sm = Smem<Geo, kRule>;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Sm& sm = *reinterpret_cast<Sm*>(smem_raw);
@@ -687,7 +692,16 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
                 selected = true;
             }
         }
-        if (!selected) generic_select<Geo>(sm, key, tid, lane, warp);
+        if (!selected) {
+            if constexpr (kCopyKeys) {
+                uint32_t key_mem[kPer];
+#pragma unroll
+                for (int i = 0; i < kPer; ++i) key_mem[i] = key[i];
+                generic_select<Geo>(sm, key_mem, tid, lane, warp);
+            } else {
+                generic_select<Geo>(sm, key, tid, lane, warp);
+            }
+        }
 
         // ---- warp 0: chosen positions before each bitmap word ----------------------------
         if (warp == 0) {
