@@ -179,6 +179,37 @@ def test_bf16_ties_stress():
     compare_full_round(delta, ef, 1.0, "bf16 ties round 2")
 
 
+def test_exact_ties_in_the_boundary_bin_and_sparse_chunks():
+    """Chunks whose boundary bin holds up to 64 keys that are all equal (chosen by index
+    alone), the same next to a bin of different keys, and chunks with fewer than 64 nonzero
+    magnitudes (every nonzero plus the lowest-index zeros), in fp32 and bf16, over rounds that
+    turn selected zeros into tied residuals."""
+    rng = np.random.default_rng(11)
+    L = 4096
+
+    def tied(n_top, n_tie, top=2.0, tie=1.0):
+        x = np.zeros(L, np.float32)
+        pos = rng.choice(L, n_top + n_tie, replace=False)
+        x[pos[:n_top]] = top * rng.choice([-1, 1], n_top)
+        x[pos[n_top:]] = tie * rng.choice([-1, 1], n_tie)
+        return x
+
+    mixed = tied(40, 30)
+    mixed[rng.choice(np.flatnonzero(mixed == 0), 3, replace=False)] = 1.0 + 2.0 ** -20
+    sparse = np.zeros(L, np.float32)
+    sparse[rng.choice(L, 10, replace=False)] = rng.standard_normal(10).astype(np.float32)
+    one = np.zeros(L, np.float32)
+    one[4095] = -3.0
+    chunks = (tied(40, 40), tied(0, 64 + 1), tied(63, 2), tied(10, 60), mixed, sparse, one,
+              tied(60, 4, 1.0, 1.0))
+    for dtype in (torch.float32, torch.bfloat16):
+        delta = _chunks(*chunks).to(dtype)
+        ef = torch.zeros(delta.numel(), device=DEV)
+        compare_full_round(delta, ef, 1.0, f"{dtype} ties round 1")
+        compare_full_round(delta, ef, 0.95, f"{dtype} ties round 2")
+        compare_full_round(torch.zeros_like(delta), ef, 0.95, f"{dtype} ties round 3 (zero delta)")
+
+
 def test_nonfinite_inputs_flagged_and_deterministic():
     n = 4 * 4096
     gen = synth.generator(9, DEV)
