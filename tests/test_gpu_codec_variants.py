@@ -78,6 +78,37 @@ def test_variant_edge_chunks(codec):
     ef = torch.zeros_like(delta)
     compare_round(delta, ef, 1.0, codec, f"{codec} edge round 1")
     compare_round(torch.zeros_like(delta), ef, 1.0, codec, f"{codec} edge round 2")
+
+
+@pytest.mark.parametrize("codec", CODECS)
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_variant_exact_ties_and_sparse_chunks(codec, dtype):
+    """At each geometry: boundary bins of up to 64 exactly tied keys (ranked by index), the
+    same beside keys of the same bin that differ, a bin of more than 64 tied keys, and chunks
+    with fewer than k nonzeros; three rounds, the last with a zero delta, so selected zeros
+    come back as tied residuals."""
+    L, k, _ = codec
+    rng = np.random.default_rng(3 * L + k)
+
+    def tied(n_top, n_tie, top=2.0, tie=1.0):
+        x = np.zeros(L, np.float32)
+        pos = rng.choice(L, n_top + n_tie, replace=False)
+        x[pos[:n_top]] = top * rng.choice([-1, 1], n_top)
+        x[pos[n_top:]] = tie * rng.choice([-1, 1], n_tie)
+        return x
+
+    mixed = tied(k - 24, 30)
+    mixed[rng.choice(np.flatnonzero(mixed == 0), 3, replace=False)] = 1.0 + 2.0 ** -20
+    sparse = np.zeros(L, np.float32)
+    sparse[rng.choice(L, k // 4, replace=False)] = rng.standard_normal(k // 4)
+    blocks = [tied(k - 24, 40), tied(k - 1, 2), tied(0, 65), tied(0, k + 1), mixed, sparse,
+              tied(k - 4, 4, 1.0, 1.0)]
+    delta = torch.cat([torch.as_tensor(b, dtype=torch.float32) for b in blocks]).to(DEV)
+    delta = delta.to(dtype)
+    ef = torch.zeros(delta.numel(), device=DEV)
+    compare_round(delta, ef, 1.0, codec, f"{codec} {dtype} ties round 1")
+    compare_round(delta, ef, 0.95, codec, f"{codec} {dtype} ties round 2")
+    compare_round(torch.zeros_like(delta), ef, 0.95, codec, f"{codec} {dtype} ties round 3")
     for n in (1, k - 1, k, k + 1, L - 1, L + 1):
         d = synth.laplace(n, 1.0, synth.generator(n, DEV), DEV)
         compare_round(d, torch.zeros(n, device=DEV), 0.5, codec, f"{codec} n={n}")
