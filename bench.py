@@ -23,8 +23,10 @@ time is the max over ranks and the value is the sum of all ranks' bytes over tha
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -174,34 +176,46 @@ def smi_id(dev) -> str:
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+    """nvidia-smi clock/throttle samples every `interval_ms` while the timed region runs.
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Entering starts nvidia-smi and waits (up to 5 s) for its first sample, so that the timed
+    region that follows is covered from its start.  Only samples whose own timestamp lies
+    between entering and leaving count (nvidia-smi's output reaches the pipe in bursts, so
+    arrival times say little)."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_id: str):
+    def __init__(self, gpu_id: str, interval_ms: int = 10):
         self.gpu = gpu_id
+        self.interval = interval_ms
         self.proc = None
-        self.lines = []
+        self.lines = []          # (arrival time, line)
+        self.t_in = self.t_out = None
+        self._first = threading.Event()
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
+            self._first.wait(timeout=5.0)
         except OSError:
             self.proc = None
+        self.t_in = datetime.datetime.now()
         return self
 
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
+            self._first.set()
 
     def __exit__(self, *exc):
+        self.t_out = datetime.datetime.now()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -215,20 +229,24 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.lines:
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                mx = float(parts[2])
+                t = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                if self.t_in is None or t < self.t_in or (self.t_out is not None and t > self.t_out):
+                    continue
+                sm.append(float(parts[2]))
+                mx = float(parts[3])
             except ValueError:
                 continue
-            for name, v in zip(names, parts[5:9]):
+            for name, v in zip(names, parts[6:10]):
                 if v.lower().startswith("active"):
                     reasons.add(name)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0,
+                    "interval_ms": self.interval}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "sm_mhz_min": min(sm), "interval_ms": self.interval}
 
 
 # ---------------------------------------------------------------------------------------------
@@ -350,16 +368,18 @@ def run_offload(args, dev):
     return 0
 
 
-def run_other_workload(args, dev):
-    """Times one round of another workload (same metric: algorithmic bytes per second), a fresh
-    pseudo-gradient each round (the workload's round count of them, cycled).
-    heavy_tail_bf16: 2^27 bf16 compress + 8-peer mean; decoder_layer: the 72B-class layer's
-    nine tensors compressed in one multi-tensor call; tiny: 2^20 compress + 4-peer mean."""
+def setup_other_workload(name: str, dev):
+    """Buffers and one-round step of another workload, a fresh pseudo-gradient each round (the
+    workload's round count of them, cycled).  heavy_tail_bf16: 2^27 bf16 compress + 8-peer mean;
+    decoder_layer: the 72B-class layer's nine tensors compressed in one multi-tensor call;
+    tiny: 2^20 compress + 4-peer mean.  Returns (step, info): step(r, ev=None) runs round r and,
+    given three events, records them before the compress, between the kernels and after the
+    decode; info holds the sizes and the algorithmic bytes of each kernel."""
     import torch
     import compressed_pseudo_gradient_gb300 as spl
     from compressed_pseudo_gradient_gb300 import synth
 
-    wl = synth.WORKLOADS[args.workload]
+    wl = synth.WORKLOADS[name]
     R = wl.rounds
     if wl.name == "decoder_layer":
         rounds = [synth.decoder_layer_round(synth.generator(1 + 1000 * r, dev), dev)
@@ -369,51 +389,129 @@ def run_other_workload(args, dev):
         C = sum((k + CHUNK - 1) // CHUNK for k in sizes)
         payload = torch.empty((C, RECORD), dtype=torch.uint8, device=dev)
         scales = torch.empty(C, dtype=torch.float32, device=dev)
-        step_bytes = sum(compress_bytes(k, (k + CHUNK - 1) // CHUNK) for k in sizes)
+        comp_bytes = sum(compress_bytes(k, (k + CHUNK - 1) // CHUNK) for k in sizes)
 
-        def step(r):
+        def step(r, ev=None):
+            if ev:
+                ev[0].record()
             spl.ef_compress_multi(rounds[r % R], efs, wl.beta, payload=payload, scales=scales)
+            if ev:
+                ev[1].record()
+                ev[2].record()
             return 1
-        n, dtype = sum(sizes), "f32"
-    else:
-        n = wl.n
-        C = (n + CHUNK - 1) // CHUNK
-        rounds = [synth.delta_round(wl, synth.generator(1 + 1000 * r, dev), dev) for r in range(R)]
-        ef = torch.zeros(n, dtype=torch.float32, device=dev)
-        payload = torch.empty((C, RECORD), dtype=torch.uint8, device=dev)
-        scales = torch.empty(C, dtype=torch.float32, device=dev)
-        pls, scs = [], []
-        tmp = torch.empty(n, dtype=torch.float32, device=dev)
-        for p in range(wl.peers):
-            d = synth.delta_round(wl, synth.generator(2 + p, dev), dev)
-            tmp.zero_()
-            pl, sc = spl.ef_compress(d, tmp, wl.beta)
-            pls.append(pl)
-            scs.append(sc)
-        mean = torch.empty(n, dtype=torch.float32, device=dev)
-        esz = 2 if rounds[0].dtype == torch.bfloat16 else 4
-        step_bytes = (esz + 8) * n + (RECORD + 4) * C + decode_bytes(n, C, wl.peers, theta=False)
+        return step, {"name": wl.name, "n": sum(sizes), "chunks": C, "rounds": R, "peers": 0,
+                      "dtype": "f32", "comp_bytes": comp_bytes, "dec_bytes": 0,
+                      "tensors": len(sizes)}
+    n = wl.n
+    C = (n + CHUNK - 1) // CHUNK
+    rounds = [synth.delta_round(wl, synth.generator(1 + 1000 * r, dev), dev) for r in range(R)]
+    ef = torch.zeros(n, dtype=torch.float32, device=dev)
+    payload = torch.empty((C, RECORD), dtype=torch.uint8, device=dev)
+    scales = torch.empty(C, dtype=torch.float32, device=dev)
+    pls, scs = [], []
+    tmp = torch.empty(n, dtype=torch.float32, device=dev)
+    for p in range(wl.peers):
+        d = synth.delta_round(wl, synth.generator(2 + p, dev), dev)
+        tmp.zero_()
+        pl, sc = spl.ef_compress(d, tmp, wl.beta)
+        pls.append(pl)
+        scs.append(sc)
+    del tmp
+    mean = torch.empty(n, dtype=torch.float32, device=dev)
+    esz = 2 if rounds[0].dtype == torch.bfloat16 else 4
+    comp_bytes = (esz + 8) * n + (RECORD + 4) * C
 
-        def step(r):
-            spl.ef_compress(rounds[r % R], ef, wl.beta, payload=payload, scales=scales)
-            spl.decode_aggregate(pls, scs, n, mean=mean)
-            return 2
-        dtype = "bf16" if esz == 2 else "f32"
+    def step(r, ev=None):
+        if ev:
+            ev[0].record()
+        spl.ef_compress(rounds[r % R], ef, wl.beta, payload=payload, scales=scales)
+        if ev:
+            ev[1].record()
+        spl.decode_aggregate(pls, scs, n, mean=mean)
+        if ev:
+            ev[2].record()
+        return 2
+    return step, {"name": wl.name, "n": n, "chunks": C, "rounds": R, "peers": wl.peers,
+                  "dtype": "bf16" if esz == 2 else "f32", "comp_bytes": comp_bytes,
+                  "dec_bytes": decode_bytes(n, C, wl.peers, theta=False)}
 
-    def timed(run_round):
-        start = torch.cuda.Event(enable_timing=True)
-        end = torch.cuda.Event(enable_timing=True)
-        start.record()
-        for k in range(args.steps):
+
+def time_steps(dev, run_round, steps: int, ev_count: int = 0):
+    """Seconds for `steps` calls of run_round(k[, events]) between two CUDA events on the
+    current stream, with per-step events when ev_count > 0 (returned as lists)."""
+    import torch
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(ev_count)] for _ in range(steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    start.record()
+    for k in range(steps):
+        if ev_count:
+            run_round(k, evs[k])
+        else:
             run_round(k)
-        end.record()
-        torch.cuda.synchronize(dev)
-        return start.elapsed_time(end) / 1e3
+    end.record()
+    torch.cuda.synchronize(dev)
+    return start.elapsed_time(end) / 1e3, evs
 
+
+def kernel_split(info, evs, peak):
+    """Per-kernel averages from three events per step: compress, then decode."""
+    out = {}
+    c_s = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) / 1e3
+    gbs = info["comp_bytes"] / c_s / 1e9
+    out["ef_compress"] = {"ms": round(1e3 * c_s, 4), "GB/s": round(gbs, 1),
+                          "frac_of_hbm": round(gbs / peak, 4),
+                          "Gelem/s": round(info["n"] / c_s / 1e9, 2)}
+    if info["dec_bytes"]:
+        d_s = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) / 1e3
+        gbs = info["dec_bytes"] / d_s / 1e9
+        out["decode_aggregate"] = {"ms": round(1e3 * d_s, 4), "GB/s": round(gbs, 1),
+                                   "frac_of_hbm": round(gbs / peak, 4),
+                                   "Gelem/s": round(info["n"] / d_s / 1e9, 2)}
+    return out
+
+
+def other_workload_record(name: str, dev, steps: int, warmup: int):
+    """A sub-record of the default line: `steps` rounds of another workload as plain calls,
+    timed as a whole and per kernel, with the clocks sampled meanwhile."""
+    import torch
+    step, info = setup_other_workload(name, dev)
+    warm_secs, _ = time_steps(dev, step, warmup)
+    # at least 0.25 s of timed steps, so the clock samples cover the region several times
+    steps = int(min(2000, max(steps, math.ceil(0.25 / (warm_secs / warmup)))))
+    with ClockSampler(smi_id(dev)) as clk:
+        secs, evs = time_steps(dev, step, steps, ev_count=3)
+    peak, _ = read_peaks()
+    step_bytes = info["comp_bytes"] + info["dec_bytes"]
+    value = step_bytes * steps / secs / 1e9
+    rec = {"workload": info["name"], "n": info["n"], "chunks": info["chunks"],
+           "dtype": info["dtype"], "rounds": info["rounds"], "peers": info["peers"],
+           "steps": steps, "ms_per_step": round(1e3 * secs / steps, 4),
+           "step_bytes": step_bytes, "GB/s": round(value, 1),
+           "frac_of_hbm": round(value / peak, 4)}
+    rec.update(kernel_split(info, evs, peak))
+    rec["clocks"] = clk.summary()
+    del step
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return rec
+
+
+def run_other_workload(args, dev):
+    """Times one round of another workload (same metric: algorithmic bytes per second), as
+    plain calls and as CUDA graphs of each round replayed in turn; reports the faster."""
+    import torch
+
+    step, info = setup_other_workload(args.workload, dev)
+    R = info["rounds"]
+    step_bytes = info["comp_bytes"] + info["dec_bytes"]
     for k in range(args.warmup):
         step(k)
-    torch.cuda.synchronize(dev)
-    eager_secs = timed(step)
+    peak, kind = read_peaks()
+    with ClockSampler(smi_id(dev)) as clk:
+        eager_secs, evs = time_steps(dev, step, args.steps, ev_count=3)
+    split = kernel_split(info, evs, peak)
     launches = step(0) * args.steps
     # each round's step captured once into a CUDA graph and replayed in turn: the calls are
     # stream-ordered and never allocate or synchronise, so a launch-bound step sheds its
@@ -432,25 +530,23 @@ def run_other_workload(args, dev):
         graphs.append(g)
     for k in range(args.warmup):
         graphs[k % R].replay()
-    torch.cuda.synchronize(dev)
-    graph_secs = timed(lambda k: graphs[k % R].replay())
+    graph_secs, _ = time_steps(dev, lambda k: graphs[k % R].replay(), args.steps)
     # the faster launch mode is the one a user would take: graphs pay off where launches bound
     # the step (tiny), plain calls where the kernels do
     use_graph = graph_secs < eager_secs
     secs = graph_secs if use_graph else eager_secs
     other = eager_secs if use_graph else graph_secs
-    peak, kind = read_peaks()
     value = step_bytes * args.steps / secs / 1e9
+    cfg = {"workload": info["name"], "n": info["n"], "rounds": R, "step_bytes": step_bytes,
+           "frac_of_hbm": round(value / peak, 4), "peak_kind": kind,
+           "launch": "CUDA graph of the step, replayed" if use_graph else "plain calls",
+           "other_launch_ms_per_step": round(1e3 * other / args.steps, 4)}
+    cfg.update(split)
     line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * secs / args.steps, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
-            "config": {"workload": wl.name, "n": n, "rounds": R, "step_bytes": step_bytes,
-                       "frac_of_hbm": round(value / peak, 4), "peak_kind": kind,
-                       "launch": "CUDA graph of the step, replayed" if use_graph
-                                 else "plain calls",
-                       "other_launch_ms_per_step": round(1e3 * other / args.steps, 4)},
-            "gpu_launches": launches}
+            "scaling": "weak", "vs_baseline": None, "dtype": info["dtype"], "data": "synthetic",
+            "config": cfg, "clocks": clk.summary(), "gpu_launches": launches}
     print(json.dumps(line), flush=True)
     return 0
 
@@ -781,6 +877,8 @@ def main(argv=None):
     ap.add_argument("--cpu-chunks", type=int, default=32768)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip the heavy-tailed bf16 and decoder-layer sub-records")
     ap.add_argument("--workload", default="receive",
                     choices=["receive", "heavy_tail_bf16", "decoder_layer", "tiny", "offload",
                              "codecs"],
@@ -815,6 +913,16 @@ def main(argv=None):
     r = run_gpu(args, dev, rank, world)
     if rank != 0:
         return 0
+    others = None
+    if world == 1 and not args.no_other_workloads and args.elements == N_ELEMS:
+        # the other two single-GPU workloads, timed per kernel after the headline step (their
+        # own buffers; the headline's are released first)
+        import gc
+        gc.collect()
+        torch.cuda.empty_cache()
+        steps = max(args.steps, 20)
+        others = [other_workload_record(name, dev, steps, args.warmup)
+                  for name in ("heavy_tail_bf16", "decoder_layer")]
 
     n = args.elements
     C = (n + CHUNK - 1) // CHUNK
@@ -861,6 +969,8 @@ def main(argv=None):
                        "d2h_bytes_per_step": e["d2h"], "steps": e["steps"]}
     if r["cpu"] is not None:
         line["cpu_baseline"] = r["cpu"]
+    if others is not None:
+        line["config"]["other_workloads"] = others
     print(json.dumps(line), flush=True)
     return 0
 

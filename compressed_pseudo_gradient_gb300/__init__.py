@@ -15,7 +15,9 @@ from __future__ import annotations
 from ._binding import (  # noqa: F401
     CHUNK,
     FLAG_BAD_RECORD,
+    FLAG_COPY_PENDING,
     FLAG_NONFINITE,
+    FLAG_TIMEOUT,
     MAX_PEERS,
     RECORD_BYTES,
     SCALE_MAX_ABS,
@@ -25,6 +27,7 @@ from ._binding import (  # noqa: F401
     decode_aggregate,
     ef_compress,
     ef_compress_multi,
+    flags_status,
     library,
     library_path,
     new_peer_stats,

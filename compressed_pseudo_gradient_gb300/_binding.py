@@ -21,6 +21,8 @@ RECORD_BYTES = 112
 MAX_PEERS = 256
 FLAG_NONFINITE = 1
 FLAG_BAD_RECORD = 2
+FLAG_TIMEOUT = 4
+FLAG_COPY_PENDING = 8
 SCALE_MAX_ABS = 0     # s = max |a| / 1.5 (the default)
 SCALE_MEAN_ABS = 1    # s = pairwise sum of the chosen |a| / k (codec variant)
 
@@ -76,8 +78,9 @@ def library():
         lib.spl_ef_compress.restype = ci
         lib.spl_ef_compress_multi.argtypes = [ctypes.POINTER(_Tensor), ci, ci, cf, vp, vp, vp, vp]
         lib.spl_ef_compress_multi.restype = ci
+        lib.spl_flags_status.argtypes, lib.spl_flags_status.restype = [ctypes.c_uint32], ci
         lib.spl_decode_aggregate.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), ci, sz, vp,
-                                             vp, cf, vp, vp]
+                                             vp, cf, ci, vp, vp]
         lib.spl_decode_aggregate.restype = ci
         lib.spl_decode_aggregate_stats.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), ci,
                                                    sz, vp, vp, cf, vp, vp, vp]
@@ -96,6 +99,16 @@ def library():
         lib.spl_unpack.argtypes, lib.spl_unpack.restype = [vp, sz, vp, vp, vp], ci
         _lib = lib
         return lib
+
+
+def flags_status(flags) -> int:
+    """The status a device flags word stands for (spl_flags_status): 0 (ok), 4 (non-finite
+    accumulated value), 5 (rejected record) or 6 (a kernel stopped on a bounded wait).
+    ``flags`` is the 1-element int32 tensor the calls OR into, or its value; reading a tensor
+    synchronises with its device."""
+    if isinstance(flags, torch.Tensor):
+        flags = int(flags.item())
+    return int(library().spl_flags_status(int(flags) & 0xffffffff))
 
 
 def _check(fn: str, status: int):
@@ -266,14 +279,18 @@ def read_peer_stats(stats: torch.Tensor) -> dict:
 
 
 def decode_aggregate(payloads, scales, n: int, *, mean=None, theta=None, lr: float = 0.0,
-                     flags=None, stats=None, codec=None):
+                     flags=None, stats=None, codec=None, validate: bool = True):
     """Mean of P peers' decoded records, optionally fused with theta -= lr * mean in place
     (spl_decode_aggregate).  With ``stats`` (from new_peer_stats, accumulated into), also the
     per-peer statistics (spl_decode_aggregate_stats).  ``codec``: (L, k, rule) of a codec
-    variant (spl_decode_aggregate_codec), or None.  Returns mean (fp32 [n])."""
+    variant (spl_decode_aggregate_codec), or None.  ``validate=False`` skips the record checks
+    (default codec without statistics only; the statistics and the variants always check).
+    Returns mean (fp32 [n])."""
     lib = library()
     cd = _codec(codec)
     rb = record_bytes(codec)
+    if not validate and (cd is not None or stats is not None):
+        raise ValueError("validate=False is only offered by the default codec without stats")
     P = len(payloads)
     if P != len(scales) or P < 1:
         raise ValueError("payloads and scales must be non-empty lists of equal length")
@@ -312,7 +329,8 @@ def decode_aggregate(payloads, scales, n: int, *, mean=None, theta=None, lr: flo
         elif stats is None:
             fn = "spl_decode_aggregate"
             st = lib.spl_decode_aggregate(parr, sarr, P, int(n), mean.data_ptr(), tptr, float(lr),
-                                          _flags_ptr(flags, dev), _stream(dev))
+                                          1 if validate else 0, _flags_ptr(flags, dev),
+                                          _stream(dev))
         else:
             fn = "spl_decode_aggregate_stats"
             st = lib.spl_decode_aggregate_stats(parr, sarr, P, int(n), mean.data_ptr(), tptr,

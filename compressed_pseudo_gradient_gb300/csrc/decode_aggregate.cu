@@ -5,11 +5,13 @@
 namespace spl {
 
 cudaError_t launch_decode_aggregate(const DecodeTable& tab, const Codec& cd, int P, int64_t n,
-                                    float* mean, float* theta, float lr, PeerStats* stats,
-                                    uint32_t* flags, cudaStream_t stream) {
+                                    float* mean, float* theta, float lr, bool validate,
+                                    PeerStats* stats, uint32_t* flags, cudaStream_t stream) {
     if (cd.chunk == kChunk && cd.topk == kTopK)
-        return launch_geometry<DefaultGeometry>(tab, P, n, mean, theta, lr, stats, flags, stream);
-    return launch_decode_aggregate_variant(tab, cd, P, n, mean, theta, lr, stats, flags, stream);
+        return launch_geometry<DefaultGeometry>(tab, P, n, mean, theta, lr, validate, stats, flags,
+                                                stream);
+    return launch_decode_aggregate_variant(tab, cd, P, n, mean, theta, lr, validate, stats, flags,
+                                           stream);
 }
 
 }  // namespace spl

@@ -144,8 +144,8 @@ __device__ __forceinline__ void prefetch(const DecodeTable& tab, int P, int64_t 
 template <class Geo, bool kStats, bool kPow2>
 __global__ void __launch_bounds__(RecvShape<Geo>::kThreads, RecvShape<Geo>::kMinBlocks)
 k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __restrict__ mean,
-                   float* __restrict__ theta, float neg_lr, PeerStats* __restrict__ stats,
-                   uint32_t* __restrict__ flags) {
+                   float* __restrict__ theta, float neg_lr, bool validate,
+                   PeerStats* __restrict__ stats, uint32_t* __restrict__ flags) {
     using S = RecvShape<Geo>;
     constexpr int kThreads = S::kThreads;
     constexpr int kWarps = S::kWarps;
@@ -246,23 +246,26 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
                     f[m] = record_field_fs<Geo::kFieldBits>(words, lane + 32 * m);
                     ix[m] = f[m] >> 2;
                 }
-                // indices strictly ascending: each entry below the next one
-                bool asc = true;
-#pragma unroll
-                for (int m = 0; m < kPerLane; ++m) {
-                    uint32_t next = __shfl_down_sync(0xffffffffu, ix[m], 1);
-                    if (m + 1 < kPerLane) {
-                        const uint32_t first = __shfl_sync(0xffffffffu, ix[m + 1 < kPerLane ? m + 1 : m], 0);
-                        if (lane == 31) next = first;
-                        asc = asc && ix[m] < next;
-                    } else {
-                        asc = asc && (lane == 31 || ix[m] < next);
-                    }
-                }
                 const int slot = p / (32 * kWarps);   // the same for the whole warp
                 const float sv = (kSpl == 1 || slot == 0) ? sc_cur[0] : sc_cur[kSpl - 1];
                 const float s = __shfl_sync(0xffffffffu, sv, (p / kWarps) % 32);
-                const bool ok = __all_sync(0xffffffffu, asc) && s >= 0.0f && s <= FLT_MAX;
+                bool ok = true;
+                if (validate) {   // uniform: a launch argument
+                    // indices strictly ascending: each entry below the next one
+                    bool asc = true;
+#pragma unroll
+                    for (int m = 0; m < kPerLane; ++m) {
+                        uint32_t next = __shfl_down_sync(0xffffffffu, ix[m], 1);
+                        if (m + 1 < kPerLane) {
+                            const uint32_t first = __shfl_sync(0xffffffffu, ix[m + 1 < kPerLane ? m + 1 : m], 0);
+                            if (lane == 31) next = first;
+                            asc = asc && ix[m] < next;
+                        } else {
+                            asc = asc && (lane == 31 || ix[m] < next);
+                        }
+                    }
+                    ok = __all_sync(0xffffffffu, asc) && s >= 0.0f && s <= FLT_MAX;
+                }
                 if (ok) {
                     uint2* eg = ent + g * kTopK;
 #pragma unroll
@@ -399,12 +402,16 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
             }
         }
     }
+    bool copy_pending = false;
     if (aborted && tid == 0) {
         // copies still in flight may land late: wait for them (bounded) before the CTA's
-        // shared memory is released: the stage that timed out and any armed after it
+        // shared memory is released: the stage that timed out and any armed after it (if a
+        // wait runs out again, the block exits with a copy possibly in flight: reported)
         for (int k = 0; k < kStages; ++k) {
             const int it2 = it + k;
-            if (c + k * G < C) mbar_wait(&bars[it2 % kStages], static_cast<uint32_t>(it2 / kStages) & 1u);
+            if (c + k * G < C &&
+                !mbar_wait(&bars[it2 % kStages], static_cast<uint32_t>(it2 / kStages) & 1u))
+                copy_pending = true;
         }
     }
     if constexpr (kStats) {
@@ -422,13 +429,13 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
     }
     if (flags != nullptr) {
         if (bad && lane == 0) atomicOr(flags, kFlagBadRecord);
-        if (aborted && tid == 0) atomicOr(flags, kFlagTimeout);
+        if (aborted && tid == 0) atomicOr(flags, kFlagTimeout | (copy_pending ? kFlagCopyPending : 0u));
     }
 }
 
 template <class Geo, bool kStats, bool kPow2>
 cudaError_t launch_kernel(const DecodeTable& tab, int P, int64_t n, int64_t C, float* mean,
-                          float* theta, float lr, PeerStats* stats, uint32_t* flags,
+                          float* theta, float lr, bool validate, PeerStats* stats, uint32_t* flags,
                           cudaStream_t stream) {
     const size_t smem = Layout<Geo>(P, kStats).total;
     const void* kern = reinterpret_cast<const void*>(&k_decode_aggregate<Geo, kStats, kPow2>);
@@ -440,8 +447,8 @@ cudaError_t launch_kernel(const DecodeTable& tab, int P, int64_t n, int64_t C, f
     if (resident <= 0) return cudaErrorInvalidConfiguration;
     const int grid = static_cast<int>(C < resident ? C : resident);
     const float rp = 1.0f / static_cast<float>(P);   // correctly rounded on the host
-    k_decode_aggregate<Geo, kStats, kPow2><<<grid, kThreads, smem, stream>>>(tab, P, rp, n, mean,
-                                                                            theta, -lr, stats, flags);
+    k_decode_aggregate<Geo, kStats, kPow2><<<grid, kThreads, smem, stream>>>(
+        tab, P, rp, n, mean, theta, -lr, validate || kStats, stats, flags);
     return cudaGetLastError();
 }
 
@@ -449,21 +456,26 @@ cudaError_t launch_kernel(const DecodeTable& tab, int P, int64_t n, int64_t C, f
 // reciprocal division; the choice is made per launch, so each kernel has one straight path.
 template <class Geo, bool kStats>
 cudaError_t launch_decode(const DecodeTable& tab, int P, int64_t n, float* mean, float* theta,
-                          float lr, PeerStats* stats, uint32_t* flags, cudaStream_t stream) {
+                          float lr, bool validate, PeerStats* stats, uint32_t* flags,
+                          cudaStream_t stream) {
     const int64_t C = (n + Geo::kChunk - 1) / Geo::kChunk;
     if (C == 0) return cudaSuccess;
     if ((P & (P - 1)) == 0)
-        return launch_kernel<Geo, kStats, true>(tab, P, n, C, mean, theta, lr, stats, flags, stream);
-    return launch_kernel<Geo, kStats, false>(tab, P, n, C, mean, theta, lr, stats, flags, stream);
+        return launch_kernel<Geo, kStats, true>(tab, P, n, C, mean, theta, lr, validate, stats,
+                                                flags, stream);
+    return launch_kernel<Geo, kStats, false>(tab, P, n, C, mean, theta, lr, validate, stats, flags,
+                                             stream);
 }
 
-// Launch for one record geometry, with or without statistics.
+// Launch for one record geometry, with or without statistics (which need validation on).
 template <class Geo>
 cudaError_t launch_geometry(const DecodeTable& tab, int P, int64_t n, float* mean, float* theta,
-                            float lr, PeerStats* stats, uint32_t* flags, cudaStream_t stream) {
+                            float lr, bool validate, PeerStats* stats, uint32_t* flags,
+                            cudaStream_t stream) {
     return stats != nullptr
-               ? launch_decode<Geo, true>(tab, P, n, mean, theta, lr, stats, flags, stream)
-               : launch_decode<Geo, false>(tab, P, n, mean, theta, lr, stats, flags, stream);
+               ? launch_decode<Geo, true>(tab, P, n, mean, theta, lr, true, stats, flags, stream)
+               : launch_decode<Geo, false>(tab, P, n, mean, theta, lr, validate, stats, flags,
+                                           stream);
 }
 
 }  // namespace

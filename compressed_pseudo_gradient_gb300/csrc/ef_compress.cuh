@@ -798,14 +798,16 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
         else
             finish_record<Geo, kRule>(sm, payload, scales, pend_c, pend_ef, pend_valid, lane);
     }
+    bool copy_pending = false;
     if (aborted && tid == 0) {
         // the copy that did not complete may still land: wait once more (bounded) before
-        // the CTA's shared memory is released
-        mbar_wait(&sm.bar, parity ^ 1u);
+        // the CTA's shared memory is released; if that wait runs out too, the block exits with
+        // the copy possibly in flight, which the flags report
+        copy_pending = !mbar_wait(&sm.bar, parity ^ 1u);
     }
     if (flags != nullptr) {
         if (nonfinite) atomicOr(flags, kFlagNonFinite);
-        if (aborted && tid == 0) atomicOr(flags, kFlagTimeout);
+        if (aborted && tid == 0) atomicOr(flags, kFlagTimeout | (copy_pending ? kFlagCopyPending : 0u));
     }
 }
 

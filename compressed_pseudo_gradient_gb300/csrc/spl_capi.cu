@@ -78,8 +78,18 @@ const char* spl_status_string(int status) {
         case SPL_ERR_INVALID_ARG: return "invalid argument";
         case SPL_ERR_ALIGNMENT: return "misaligned pointer";
         case SPL_ERR_CUDA: return "CUDA error";
+        case SPL_ERR_NONFINITE: return "non-finite accumulated value";
+        case SPL_ERR_BAD_PAYLOAD: return "rejected record";
+        case SPL_ERR_TIMEOUT: return "kernel stopped on a bounded wait";
         default: return "unknown status";
     }
+}
+
+spl_status spl_flags_status(uint32_t flags) {
+    if (flags & (SPL_FLAG_TIMEOUT | SPL_FLAG_COPY_PENDING)) return SPL_ERR_TIMEOUT;
+    if (flags & SPL_FLAG_BAD_RECORD) return SPL_ERR_BAD_PAYLOAD;
+    if (flags & SPL_FLAG_NONFINITE) return SPL_ERR_NONFINITE;
+    return SPL_OK;
 }
 
 int spl_last_cuda_error(void) { return g_last_cuda_error; }
@@ -118,7 +128,9 @@ static spl_status check_outputs(const spl_tensor* t, int num, spl_dtype dt, cons
     if (!aligned(payload, 16) || !aligned(scales, 4) || !aligned(flags, 4))
         return SPL_ERR_ALIGNMENT;
     const size_t esz = dt == SPL_F32 ? 4 : 2;
-    if (overlap(payload, C * rb, scales, C * 4)) return SPL_ERR_INVALID_ARG;
+    if (overlap(payload, C * rb, scales, C * 4) || overlap(flags, 4, payload, C * rb) ||
+        overlap(flags, 4, scales, C * 4))
+        return SPL_ERR_INVALID_ARG;
     for (int i = 0; i < num; ++i) {
         const size_t n = t[i].n;
         if (overlap(payload, C * rb, t[i].delta, n * esz) ||
@@ -240,8 +252,8 @@ static_assert(sizeof(spl_peer_stats) == sizeof(spl::PeerStats), "spl_peer_stats 
 
 static spl_status decode_impl(const spl::Codec& cd, const uint8_t* const* payloads,
                               const float* const* scales, int P, size_t n, float* mean_out,
-                              float* theta, float lr, spl_peer_stats* d_stats, uint32_t* d_flags,
-                              spl_stream_t stream) {
+                              float* theta, float lr, bool validate, spl_peer_stats* d_stats,
+                              uint32_t* d_flags, spl_stream_t stream) {
     if (P < 1 || P > SPL_MAX_PEERS) return SPL_ERR_INVALID_ARG;
     if (theta != nullptr && !std::isfinite(lr)) return SPL_ERR_INVALID_ARG;
     if (n == 0) return SPL_OK;
@@ -254,6 +266,7 @@ static spl_status decode_impl(const spl::Codec& cd, const uint8_t* const* payloa
     if (overlap(mean_out, n * 4, theta, n * 4)) return SPL_ERR_INVALID_ARG;
     if (overlap(d_flags, 4, mean_out, n * 4) || overlap(d_flags, 4, theta, n * 4))
         return SPL_ERR_INVALID_ARG;
+    const size_t sb = static_cast<size_t>(P) * sizeof(spl_peer_stats);   // d_stats, if given
     spl::DecodeTable tab;
     std::memset(&tab, 0, sizeof tab);
     for (int p = 0; p < P; ++p) {
@@ -261,7 +274,9 @@ static spl_status decode_impl(const spl::Codec& cd, const uint8_t* const* payloa
         if (!aligned(payloads[p], 16) || !aligned(scales[p], 4)) return SPL_ERR_ALIGNMENT;
         if (overlap(payloads[p], C * rb, mean_out, n * 4) ||
             overlap(payloads[p], C * rb, theta, n * 4) ||
-            overlap(scales[p], C * 4, mean_out, n * 4) || overlap(scales[p], C * 4, theta, n * 4))
+            overlap(scales[p], C * 4, mean_out, n * 4) || overlap(scales[p], C * 4, theta, n * 4) ||
+            overlap(d_flags, 4, payloads[p], C * rb) || overlap(d_flags, 4, scales[p], C * 4) ||
+            overlap(d_stats, sb, payloads[p], C * rb) || overlap(d_stats, sb, scales[p], C * 4))
             return SPL_ERR_INVALID_ARG;
         tab.payload[p] = payloads[p];
         tab.scale[p] = scales[p];
@@ -271,16 +286,17 @@ static spl_status decode_impl(const spl::Codec& cd, const uint8_t* const* payloa
     // plain stores; those take any memory the device can address)
     if (theta != nullptr && memory_type(theta) != cudaMemoryTypeDevice) return SPL_ERR_INVALID_ARG;
     return cuda_status(spl::launch_decode_aggregate(
-        tab, cd, P, static_cast<int64_t>(n), mean_out, theta, lr,
+        tab, cd, P, static_cast<int64_t>(n), mean_out, theta, lr, validate,
         reinterpret_cast<spl::PeerStats*>(d_stats), d_flags, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 spl_status spl_decode_aggregate(const uint8_t* const* payloads, const float* const* scales, int P,
-                                size_t n, float* mean_out, float* theta, float lr,
+                                size_t n, float* mean_out, float* theta, float lr, int validate,
                                 uint32_t* d_flags, spl_stream_t stream) {
     spl::Codec cd;
     resolve_codec(nullptr, &cd);
-    return decode_impl(cd, payloads, scales, P, n, mean_out, theta, lr, nullptr, d_flags, stream);
+    return decode_impl(cd, payloads, scales, P, n, mean_out, theta, lr, validate != 0, nullptr,
+                       d_flags, stream);
 }
 
 // Checks of a statistics array (P entries, 8-byte aligned, apart from the outputs).
@@ -306,7 +322,8 @@ spl_status spl_decode_aggregate_codec(const spl_codec* codec, const uint8_t* con
         const spl_status st = check_stats(d_stats, P, n, mean_out, theta, d_flags);
         if (st != SPL_OK) return st;
     }
-    return decode_impl(cd, payloads, scales, P, n, mean_out, theta, lr, d_stats, d_flags, stream);
+    return decode_impl(cd, payloads, scales, P, n, mean_out, theta, lr, true, d_stats, d_flags,
+                       stream);
 }
 
 spl_status spl_decode_aggregate_stats(const uint8_t* const* payloads, const float* const* scales,
@@ -318,7 +335,8 @@ spl_status spl_decode_aggregate_stats(const uint8_t* const* payloads, const floa
     if (st != SPL_OK) return st;
     spl::Codec cd;
     resolve_codec(nullptr, &cd);
-    return decode_impl(cd, payloads, scales, P, n, mean_out, theta, lr, d_stats, d_flags, stream);
+    return decode_impl(cd, payloads, scales, P, n, mean_out, theta, lr, true, d_stats, d_flags,
+                       stream);
 }
 
 spl_status spl_pack(const uint16_t* idx, const uint8_t* codes, size_t num_chunks, uint8_t* payload,

@@ -46,6 +46,7 @@ static_assert(DefaultGeometry::kRecordBytes == kRecordBytes, "default record siz
 constexpr uint32_t kFlagNonFinite = 1u;
 constexpr uint32_t kFlagBadRecord = 2u;
 constexpr uint32_t kFlagTimeout = 4u;
+constexpr uint32_t kFlagCopyPending = 8u;   // after a timeout, the copy's own wait ran out too
 
 // Upper bound on any wait for an asynchronous copy: a healthy copy lands in microseconds.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;

@@ -74,14 +74,16 @@ struct PeerStats {
     double sumsq;
 };
 
+// validate: check every record (strictly ascending indices, a finite non-negative scale) and
+// leave out the ones that fail; always on when stats is given.
 cudaError_t launch_decode_aggregate(const DecodeTable& tab, const Codec& cd, int P, int64_t n,
-                                    float* mean, float* theta, float lr, PeerStats* stats,
-                                    uint32_t* flags, cudaStream_t stream);
+                                    float* mean, float* theta, float lr, bool validate,
+                                    PeerStats* stats, uint32_t* flags, cudaStream_t stream);
 // The same for a record geometry other than the default (the scale rule does not matter to
 // the receiver).
 cudaError_t launch_decode_aggregate_variant(const DecodeTable& tab, const Codec& cd, int P,
                                             int64_t n, float* mean, float* theta, float lr,
-                                            PeerStats* stats, uint32_t* flags,
+                                            bool validate, PeerStats* stats, uint32_t* flags,
                                             cudaStream_t stream);
 
 cudaError_t launch_pack(const uint16_t* idx, const uint8_t* codes, int64_t C,

@@ -31,7 +31,12 @@
  *   - conditions found on the device are OR-ed into *d_flags (if d_flags is not NULL), which
  *     the caller reads after synchronising: SPL_FLAG_NONFINITE, SPL_FLAG_BAD_RECORD, and
  *     SPL_FLAG_TIMEOUT (an asynchronous copy into shared memory did not complete within one
- *     second; the kernel stopped early and its outputs are incomplete);
+ *     second; the kernel stopped early and its outputs are incomplete), with
+ *     SPL_FLAG_COPY_PENDING as well when a further bounded wait for that copy also ran out (a
+ *     block then exited with the copy possibly still in flight into its shared memory, so the
+ *     device's state is suspect and the context should be discarded); spl_flags_status()
+ *     turns a flags word read back into a status.  No call returns a device-detected
+ *     condition itself: calls never wait for the device, so they cannot know it;
  *   - device pointers to fp32/bf16 dense arrays and to records must be 16-byte aligned;
  *     scales and flags 4-byte aligned; idx 2-byte aligned.
  */
@@ -52,7 +57,11 @@ typedef enum {
     SPL_OK = 0,
     SPL_ERR_INVALID_ARG = 1, /* NULL pointer, bad size, non-finite beta/lr, overlap, bad dtype */
     SPL_ERR_ALIGNMENT = 2,   /* a pointer breaks the alignment rule above */
-    SPL_ERR_CUDA = 3         /* a CUDA call failed; see spl_last_cuda_error() */
+    SPL_ERR_CUDA = 3,        /* a CUDA call failed; see spl_last_cuda_error() */
+    /* the next three are only returned by spl_flags_status(), from a flags word read back */
+    SPL_ERR_NONFINITE = 4,   /* some accumulated value a was NaN or infinite */
+    SPL_ERR_BAD_PAYLOAD = 5, /* some record was rejected by the receiver's validation */
+    SPL_ERR_TIMEOUT = 6      /* a kernel stopped early on a bounded wait: outputs incomplete */
 } spl_status;
 
 typedef enum { SPL_F32 = 0, SPL_BF16 = 1 } spl_dtype;
@@ -61,11 +70,25 @@ enum {
     SPL_CHUNK = 4096,        /* values per chunk (item 1) */
     SPL_TOPK = 64,           /* values kept per chunk, largest |a| first (item 1) */
     SPL_RECORD_BYTES = 112,  /* 64 fields of 14 bits (per-chunk equation) */
+    SPL_PAYLOAD_BYTES = SPL_RECORD_BYTES,  /* the same, by the name of the payload */
     SPL_MAX_PEERS = 256,     /* largest P accepted by spl_decode_aggregate */
+    SPL_P_MAX = SPL_MAX_PEERS,             /* the same */
     SPL_MAX_TENSORS_PER_LAUNCH = 64 /* spl_ef_compress_multi splits larger tables */
 };
 
-enum { SPL_FLAG_NONFINITE = 1u, SPL_FLAG_BAD_RECORD = 2u, SPL_FLAG_TIMEOUT = 4u };
+enum {
+    SPL_FLAG_NONFINITE = 1u,   /* sender: some a = beta * e + delta was not finite */
+    SPL_FLAG_BAD_RECORD = 2u,  /* receiver: some record was rejected */
+    SPL_FLAG_TIMEOUT = 4u,     /* a bounded wait for an asynchronous copy ran out */
+    SPL_FLAG_COPY_PENDING = 8u /* ... and so did the wait for that copy after stopping */
+};
+
+/*
+ * The status a flags word stands for, most severe first: SPL_ERR_TIMEOUT (SPL_FLAG_TIMEOUT or
+ * SPL_FLAG_COPY_PENDING), SPL_ERR_BAD_PAYLOAD (SPL_FLAG_BAD_RECORD), SPL_ERR_NONFINITE
+ * (SPL_FLAG_NONFINITE), else SPL_OK.  A host-side helper: `flags` is the value read back.
+ */
+spl_status spl_flags_status(uint32_t flags);
 
 /* Number of 4096-value chunks of an n-value tensor: ceil(n / 4096). */
 size_t spl_num_chunks(size_t n);
@@ -137,16 +160,21 @@ spl_status spl_ef_compress_multi(const spl_tensor* tensors, int num_tensors,
  * mean_out: device, n fp32, overwritten (not accumulated)
  * theta:    device, n fp32, updated in place, or NULL (then lr is ignored)
  * lr:       outer learning rate, finite when theta is given
- * d_flags:  device uint32 or NULL; SPL_FLAG_BAD_RECORD is OR-ed in when some record has
- *           indices that are not strictly ascending, or a NaN, infinite or negative scale;
- *           such a record contributes nothing (the mean still divides by P)
+ * validate: nonzero: every record is checked first, and one whose indices are not strictly
+ *           ascending, or whose scale is NaN, infinite or negative, contributes nothing (the
+ *           mean still divides by P) and sets SPL_FLAG_BAD_RECORD in *d_flags;
+ *           0: the checks are skipped (for records the caller made or has already checked);
+ *           a malformed record then gives an unspecified mean and theta, and still reads and
+ *           writes nothing outside the arrays above (indices are 12 bits wide by construction)
+ * d_flags:  device uint32 or NULL
  * Entries that decode past n (the pads of a tail chunk) are dropped.  mean_out and theta must
- * not overlap each other or any record or scale array.  theta must be device memory
- * (SPL_ERR_INVALID_ARG otherwise); the other arrays any memory the device can address.
+ * not overlap each other or any record or scale array, nor d_flags any array.  theta must be
+ * device memory (SPL_ERR_INVALID_ARG otherwise); the other arrays any memory the device can
+ * address.
  */
 spl_status spl_decode_aggregate(const uint8_t* const* payloads, const float* const* scales,
                                 int P, size_t n, float* mean_out, float* theta, float lr,
-                                uint32_t* d_flags, spl_stream_t stream);
+                                int validate, uint32_t* d_flags, spl_stream_t stream);
 
 /*
  * Per-peer statistics of the records a receiver accepted, for screening updates that look
@@ -164,9 +192,11 @@ typedef struct {
 } spl_peer_stats;       /* 24 bytes */
 
 /*
- * spl_decode_aggregate, and in the same pass the statistics above for each peer.
+ * spl_decode_aggregate with validation on, and in the same pass the statistics above for each
+ * peer (counting rejected records needs the checks, so this call always makes them).
  * d_stats: device array of P entries (8-byte aligned), ACCUMULATED into: zero it before the
- * first call (counts add up, max_scale takes the maximum, sumsq adds up across calls).
+ * first call (counts add up, max_scale takes the maximum, sumsq adds up across calls); it must
+ * not overlap any other array of the call.
  */
 spl_status spl_decode_aggregate_stats(const uint8_t* const* payloads, const float* const* scales,
                                       int P, size_t n, float* mean_out, float* theta, float lr,
@@ -215,8 +245,8 @@ spl_status spl_ef_compress_codec(const spl_codec* codec, const spl_tensor* tenso
                                  spl_stream_t stream);
 
 /*
- * spl_decode_aggregate (d_stats NULL) or spl_decode_aggregate_stats (d_stats given) for
- * records of the given codec (only its L and k matter to the receiver): each payloads[p] holds
+ * spl_decode_aggregate with validation on (d_stats NULL) or spl_decode_aggregate_stats
+ * (d_stats given) for records of the given codec (only its L and k matter to the receiver): each payloads[p] holds
  * spl_codec_num_chunks(n) records of spl_codec_record_bytes bytes, 16-byte aligned at its
  * start; the statistics count over the k entries of each accepted record.
  */

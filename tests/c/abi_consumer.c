@@ -30,8 +30,20 @@ int main(void) {
            "empty table");
     expect(spl_ef_compress_codec(&bad, &t, 1, SPL_F32, 1.0f, 0, 0, 0, 0) == SPL_ERR_INVALID_ARG,
            "unsupported codec rejected");
-    expect(spl_decode_aggregate(0, 0, 0, 16, 0, 0, 0.0f, 0, 0) == SPL_ERR_INVALID_ARG,
+    expect(spl_decode_aggregate(0, 0, 0, 16, 0, 0, 0.0f, 1, 0, 0) == SPL_ERR_INVALID_ARG,
            "P = 0 rejected");
+    expect(spl_decode_aggregate(0, 0, SPL_P_MAX + 1, 16, 0, 0, 0.0f, 0, 0, 0) ==
+               SPL_ERR_INVALID_ARG, "P above SPL_P_MAX rejected");
+    expect(SPL_PAYLOAD_BYTES == SPL_RECORD_BYTES && SPL_P_MAX == SPL_MAX_PEERS, "aliases");
+    /* a flags word read back maps to a status, most severe first */
+    expect(spl_flags_status(0u) == SPL_OK, "no flags");
+    expect(spl_flags_status(SPL_FLAG_NONFINITE) == SPL_ERR_NONFINITE, "non-finite");
+    expect(spl_flags_status(SPL_FLAG_BAD_RECORD | SPL_FLAG_NONFINITE) == SPL_ERR_BAD_PAYLOAD,
+           "bad record before non-finite");
+    expect(spl_flags_status(SPL_FLAG_TIMEOUT | SPL_FLAG_BAD_RECORD) == SPL_ERR_TIMEOUT,
+           "timeout first");
+    expect(spl_flags_status(SPL_FLAG_COPY_PENDING) == SPL_ERR_TIMEOUT, "copy pending");
+    expect(spl_status_string(SPL_ERR_BAD_PAYLOAD)[0] != 'u', "status string of a flag status");
     expect(spl_pack(0, 0, 0, 0, 0) == SPL_OK, "empty pack");
     if (fails == 0) printf("ok\n");
     return fails != 0;

@@ -31,7 +31,7 @@ def test_header_declares_the_boundary():
     for fn in ("spl_ef_compress", "spl_ef_compress_multi", "spl_decode_aggregate",
                "spl_decode_aggregate_stats", "spl_ef_compress_codec",
                "spl_decode_aggregate_codec", "spl_codec_record_bytes", "spl_codec_num_chunks",
-               "spl_pack", "spl_unpack", "spl_num_chunks",
+               "spl_pack", "spl_unpack", "spl_num_chunks", "spl_flags_status",
                "spl_status_string", "spl_last_cuda_error"):
         assert fn in names
 
@@ -50,10 +50,20 @@ def test_num_chunks_and_status_strings(lib):
     for n, c in [(0, 0), (1, 1), (4095, 1), (4096, 1), (4097, 2), (1 << 30, 262144)]:
         assert lib.spl_num_chunks(n) == c
         assert spl.num_chunks(n) == c
-    for s in range(4):
-        assert lib.spl_status_string(s)
+    for s in range(7):
+        assert lib.spl_status_string(s) and lib.spl_status_string(s) != b"unknown status"
     assert lib.spl_status_string(99) == b"unknown status"
     assert lib.spl_last_cuda_error() == 0
+
+
+def test_flags_status(lib):
+    """A flags word read back from the device maps to one status, most severe first."""
+    NONFINITE, BAD, TIMEOUT, PENDING = 1, 2, 4, 8
+    expect = {0: 0, NONFINITE: 4, BAD: 5, BAD | NONFINITE: 5, TIMEOUT: 6, TIMEOUT | BAD: 6,
+              TIMEOUT | PENDING: 6, PENDING: 6, 0x10: 0}
+    for flags, status in expect.items():
+        assert lib.spl_flags_status(flags) == status
+        assert spl.flags_status(flags) == status
 
 
 # Fake device addresses: the checks below fail on the host before any CUDA call is made.
@@ -101,7 +111,8 @@ def test_compress_multi_argument_errors(lib):
 
 
 def test_decode_argument_errors(lib):
-    f = lib.spl_decode_aggregate
+    def f(pl, sc, P, n, mean, theta, lr, flags, stream):   # validation on
+        return lib.spl_decode_aggregate(pl, sc, P, n, mean, theta, lr, 1, flags, stream)
     P = 2
     pl = (ctypes.c_void_p * P)(A, A + 0x100000)
     sc = (ctypes.c_void_p * P)(B, B + 0x100000)
@@ -121,6 +132,35 @@ def test_decode_argument_errors(lib):
     assert f(pl_null, sc, P, n, Cp, None, 0.0, None, None) == INVALID
     pl_alias = (ctypes.c_void_p * P)(A, Cp + 4096)                          # record in mean
     assert f(pl_alias, sc, P, n, Cp, None, 0.0, None, None) == INVALID
+    assert f(pl, sc, P, n, Cp, None, 0.0, A + 0x100000 + 64, None) == INVALID   # flags in a record
+    assert f(pl, sc, P, n, Cp, None, 0.0, B + 4, None) == INVALID           # flags in scales
+    # validation off takes the same argument checks
+    g = lib.spl_decode_aggregate
+    assert g(pl, sc, 0, n, Cp, None, 0.0, 0, None, None) == INVALID
+    assert g(pl, sc, P, n, Cp + 8, None, 0.0, 0, None, None) == ALIGN
+    assert g(pl, sc, P, 0, Cp, None, 0.0, 0, None, None) == OK
+
+
+def test_compress_flags_alias_outputs(lib):
+    f = lib.spl_ef_compress
+    n = 8192
+    assert f(A, 0, B, n, 1.0, Cp, D, Cp + 32, None) == INVALID              # flags in payload
+    assert f(A, 0, B, n, 1.0, Cp, D, D + 4, None) == INVALID                # flags in scales
+
+
+def test_decode_stats_alias_records(lib):
+    f = lib.spl_decode_aggregate_stats
+    P = 2
+    pl = (ctypes.c_void_p * P)(A, A + 0x100000)
+    sc = (ctypes.c_void_p * P)(B, B + 0x100000)
+    n = 8192
+    assert f(pl, sc, P, n, Cp, None, 0.0, A + 0x100000 + 16, None, None) == INVALID  # in a record
+    assert f(pl, sc, P, n, Cp, None, 0.0, B + 0x100000, None, None) == INVALID       # in scales
+    assert f(pl, sc, P, n, Cp, None, 0.0, D, D + 8, None) == INVALID          # flags in stats
+    Codec = spl._binding._Codec
+    g = lib.spl_decode_aggregate_codec
+    c = Codec(2048, 32, 0)
+    assert g(ctypes.byref(c), pl, sc, P, n, Cp, None, 0.0, A + 32, None, None) == INVALID
 
 
 def test_decode_stats_argument_errors(lib):

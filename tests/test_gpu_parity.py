@@ -440,6 +440,35 @@ def test_malformed_records_rejected_like_oracle():
     assert_bit_equal(host(mean), o_mean, "mean with rejected records")
 
 
+@pytest.mark.parametrize("P", [1, 5, 8, 24])
+def test_decode_without_validation_matches_oracle(P):
+    """validate = 0 skips the record checks: on well-formed records the mean and theta are
+    the validated call's, bit for bit (and the oracle's)."""
+    n = 37 * 4096 + 1001
+    pls, scs = [], []
+    for p in range(P):
+        d = synth.laplace(n, 1e-4, synth.generator(400 + p, DEV), DEV)
+        pl, sc = gpu_round(d, synth.normal(n, 1e-4, synth.generator(500 + p, DEV), DEV), 0.95)
+        pls.append(pl), scs.append(sc)
+    theta = synth.theta(n, synth.generator(600, DEV), DEV)
+    th_h = host(theta)
+    theta2 = theta.clone()
+    flags = torch.zeros(1, dtype=torch.int32, device=DEV)
+    m_on = spl.decode_aggregate(pls, scs, n, theta=theta, lr=0.7, flags=flags)
+    m_off = spl.decode_aggregate(pls, scs, n, theta=theta2, lr=0.7, flags=flags, validate=False)
+    m_plain = spl.decode_aggregate(pls, scs, n, flags=flags, validate=False)
+    torch.cuda.synchronize()
+    assert int(flags.item()) == 0
+    o_mean, o_flags = oracle.decode_aggregate([host(p) for p in pls], [host(s) for s in scs], n,
+                                              theta=th_h, lr=0.7)
+    assert o_flags == 0
+    assert_bit_equal(host(m_off), host(m_on), "mean, validation off vs on")
+    assert_bit_equal(host(m_plain), host(m_on), "mean without theta, validation off")
+    assert_bit_equal(host(theta2), host(theta), "theta, validation off vs on")
+    assert_bit_equal(host(m_off), o_mean, "mean, validation off vs oracle")
+    assert_bit_equal(host(theta2), th_h, "theta, validation off vs oracle")
+
+
 # ---------------------------------------------------------------------------------------------
 # Checkpoint/resume of the only codec state, and streams
 # ---------------------------------------------------------------------------------------------
@@ -541,7 +570,7 @@ def test_memory_kinds_that_bulk_copies_cannot_read_are_rejected():
     parr = (ctypes.c_void_p * 1)(payload.data_ptr())
     sarr = (ctypes.c_void_p * 1)(scales.data_ptr())
     assert lib.spl_decode_aggregate(parr, sarr, 1, n, mean.data_ptr(), pinned.data_ptr(), 0.7,
-                                    None, st) == 1                    # theta in host memory
+                                    1, None, st) == 1                 # theta in host memory
     torch.cuda.synchronize()
 
 
