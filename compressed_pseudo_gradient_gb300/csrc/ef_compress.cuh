@@ -71,13 +71,17 @@ struct SendShape {
     static_assert(kPer % 4 == 0 && kThreads % 32 == 0 && 2048 % kThreads == 0, "sender shape");
 };
 
-template <class Geo, int kRule>
+// kFast: the select's marking pass keeps the boundary bin's keys by position (keybuf) for the
+// warp that ranks them, and the packing warp finds the chosen positions itself (no owner step).
+template <class Geo, int kRule, bool kFast>
 struct Smem {
     using S = SendShape<Geo>;
     float stage_e[S::kChunk];          // prefetched error-buffer chunk (bulk copy)
     uint32_t stage_d[S::kChunk];       // prefetched delta chunk: fp32, or bf16 in the first half
     uint32_t hist[2048];               // histogram bins (one select pass at a time)
-    uint32_t sel_bm[S::kBitmapWords];  // chosen positions (complete once the select is done)
+    // chosen positions (complete once the select is done); kFast alternates two, one per
+    // chunk, so the packing warp reads the previous chunk's while this chunk's is marked
+    uint32_t sel_bm[kFast ? 2 : 1][S::kBitmapWords];
     uint32_t eq_bm[S::kBitmapWords];   // ties at the final threshold (many-candidate path)
     uint32_t warp_tot[S::kWarps];
     uint32_t warp_max[S::kWarps];
@@ -85,9 +89,17 @@ struct Smem {
     uint2 cand[64];                    // (key, index) of the keys in the boundary bin
     uint32_t ncand;
     uint16_t fields[S::kTopK];         // the record's fields, in ascending index order
-    float vals[S::kTopK];              // the chosen a by rank (coded once the record is packed)
+    float vals[S::kTopK];              // kFast: the chosen values by rank, read back
+    uint32_t gcount[8];                // kFast: chosen positions per gather warp
+    float psum[4];                     // kFast, mean-abs: each packing warp's partial sum
     uint32_t full_scan;                // the k-th key lies below the top 512 bins
     alignas(16) uint16_t pre[S::kBitmapWords];   // chosen positions before each bitmap word
+    // boundary-bin keys by position, as offsets from the bin's lowest key (kFast only)
+    alignas(16) uint16_t keybuf[kFast ? S::kChunk : 8];
+    const void* next_delta;            // the next chunk of this CTA, located by thread 0
+    float* next_ef;
+    int next_valid;
+    int next_tensor;                   // thread 0: the tensor of the last chunk it located
     uint64_t bar;                      // completes when the stage's bulk copies have landed
 };
 
@@ -186,14 +198,11 @@ struct ChunkRef {
     bool full;
 };
 
+// t: the tensor of the last chunk located by this caller; a CTA visits its chunks in
+// increasing order, so the tensor index only moves forward (past empty tensors too).
 template <int kChunk, bool kBf16>
-__device__ __forceinline__ ChunkRef locate(const CompressTable& tab, int64_t c) {
-    int t = 0;
-    int hi = tab.num;
-    while (hi - t > 1) {
-        const int mid = (t + hi) >> 1;
-        if (tab.chunk_begin[mid] <= c) t = mid; else hi = mid;
-    }
+__device__ __forceinline__ ChunkRef locate(const CompressTable& tab, int64_t c, int& t) {
+    while (t + 1 < tab.num && tab.chunk_begin[t + 1] <= c) ++t;
     const int64_t base = (c - tab.chunk_begin[t]) * kChunk;
     const int64_t n = tab.n[t];
     ChunkRef r;
@@ -271,12 +280,51 @@ __device__ __forceinline__ void accumulate_tail(const ChunkRef& r, float beta, i
         }
 }
 
+// Shared-memory OR of v into *w when v is nonzero, as one predicated instruction (no branch:
+// the marking pass runs it for every vector of four values).
+__device__ __forceinline__ void red_or_nonzero(uint32_t* w, uint32_t v) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "@p red.shared.or.b32 [%0], %1;\n\t}" ::"r"(smem_addr(w)), "r"(v)
+        : "memory");
+}
+
+// Shared-memory 16-bit store of v when keep is set, as one predicated instruction.
+__device__ __forceinline__ void st_u16_if(uint16_t* p, uint32_t v, bool keep) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t"
+        "@p st.shared.u16 [%0], %1;\n\t}" ::"r"(smem_addr(p)), "h"(static_cast<uint16_t>(v)),
+        "r"(keep ? 1u : 0u)
+        : "memory");
+}
+
+// This thread's 16 values of a chunk's error buffer (a tail chunk's pads are not stored).
+template <class S>
+__device__ __forceinline__ void store_error_buffer(const ChunkRef& r, const float (&a)[S::kPer],
+                                                   int tid) {
+    if (r.full) {
+#pragma unroll
+        for (int v = 0; v < S::kVec; ++v)
+            st_stream_f4(r.ef + v * S::kStride + 4 * tid,
+                         make_float4(a[4 * v], a[4 * v + 1], a[4 * v + 2], a[4 * v + 3]));
+    } else {
+#pragma unroll
+        for (int v = 0; v < S::kVec; ++v)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int j = v * S::kStride + 4 * tid + u;
+                if (j < r.valid) r.ef[j] = a[4 * v + u];
+            }
+    }
+}
+
 // Generic select (any data): radix passes on key bits [30:20], [19:9] and [8:0], each over
 // the keys matching the digits found so far, stopping once the boundary bin is taken whole;
 // ties at the final threshold go to the lowest indices.  Marks the 64 chosen positions in
-// sm.sel_bm.  Entered by all threads with sm.sel_bm/eq_bm cleared; clears hist itself.
+// sm.sel_bm[cur].  Entered by all threads with it and sm.eq_bm cleared; clears hist itself.
 template <class Geo, class Sm>
-__device__ __noinline__ void generic_select(Sm& sm, const uint32_t (&key)[SendShape<Geo>::kPer],
+__device__ __noinline__ void generic_select(Sm& sm, int cur,
+                                            const uint32_t (&key)[SendShape<Geo>::kPer],
                                             int tid, int lane, int warp) {
     using S = SendShape<Geo>;
     constexpr int kPer = S::kPer;
@@ -306,7 +354,7 @@ __device__ __noinline__ void generic_select(Sm& sm, const uint32_t (&key)[SendSh
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int j = v * kStride + 4 * tid + u;
-                if ((key[4 * v + u] >> 20) >= dig) atomicOr(&sm.sel_bm[j >> 5], 1u << (j & 31));
+                if ((key[4 * v + u] >> 20) >= dig) atomicOr(&sm.sel_bm[cur][j >> 5], 1u << (j & 31));
             }
         __syncthreads();
     } else {
@@ -350,7 +398,7 @@ __device__ __noinline__ void generic_select(Sm& sm, const uint32_t (&key)[SendSh
             for (int u = 0; u < 4; ++u) {
                 const uint32_t mk = key[4 * v + u] & pmask;
                 const int j = v * kStride + 4 * tid + u;
-                if (mk > prefix) atomicOr(&sm.sel_bm[j >> 5], 1u << (j & 31));
+                if (mk > prefix) atomicOr(&sm.sel_bm[cur][j >> 5], 1u << (j & 31));
                 else if (mk == prefix) atomicOr(&sm.eq_bm[j >> 5], 1u << (j & 31));
             }
         __syncthreads();
@@ -381,7 +429,7 @@ __device__ __noinline__ void generic_select(Sm& sm, const uint32_t (&key)[SendSh
                     w ^= low;
                     --take;
                 }
-                sm.sel_bm[kWpl * lane + qq] |= kept;
+                sm.sel_bm[cur][kWpl * lane + qq] |= kept;
             }
         }
         __syncthreads();
@@ -435,52 +483,127 @@ __device__ __forceinline__ void pack_record(const Sm& sm, uint8_t* __restrict__ 
     if (lane == 0) scales[c] = s;
 }
 
-// One warp: the scale, each chosen entry's code, its residual written over the error-buffer
-// value stored earlier (pads excluded), and the record.  The scale comes from the chosen
-// values: max-abs from the largest magnitude key among them (the chunk's largest key is always
-// chosen, so this is the chunk maximum, NaN included); mean-abs from the pairwise sum of |a|
-// over ranks 0..k-1 in ascending index order, divided by k (lane l first sums its k/32
-// consecutive ranks the same way, then the lanes combine as a tree).  Runs after a barrier
-// that follows the chunk's owner step and its error-buffer stores, so the residuals land last.
-template <class Geo, int kRule, class Sm>
-__device__ __forceinline__ void finish_record(Sm& sm, uint8_t* __restrict__ payload,
-                                              float* __restrict__ scales, int64_t c, float* ef,
-                                              int valid, int lane) {
-    constexpr int kTopK = Geo::kTopK;
-    constexpr int kPerLane = kTopK / 32;
-    float x[kPerLane];
+// Named barrier among `threads` threads (a multiple of 32) of the CTA; ids 1.. (0 is
+// __syncthreads).
+__device__ __forceinline__ void named_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// kFast sizes: the gather group (the last kChunk / 1024 warps: one bitmap word per lane) turns
+// a finished chunk's bitmap into positions by rank; the packing group (the last k / 32 warps:
+// one rank per lane) codes and packs the record, warp p forming words [p b, p b + b) of the
+// record from ranks [32 p, 32 p + 32), b the field width (32 fields of b bits fill b words).
+template <class Geo>
+struct FinishShape {
+    static constexpr int kWarps = SendShape<Geo>::kWarps;
+    static constexpr int kGatherWarps = SendShape<Geo>::kBitmapWords / 32;
+    static constexpr int kPackWarps = Geo::kTopK / 32;
+    static_assert(kGatherWarps < kWarps && kPackWarps < kWarps, "warp 0 is never in a group");
+};
+
+constexpr int kBarGather = 1;   // named barrier ids
+constexpr int kBarPack = 2;
+
+// kFast, the gather group (called by its warps only, g = the warp's index in the group): the
+// positions of a finished chunk's chosen entries into sm.fields by rank (ascending position),
+// from its bitmap sm.sel_bm[which] (complete behind a barrier that precedes this call), and
+// asynchronous copies of their values, read back from the error buffer (where every thread
+// stored the chunk's accumulated values unchanged), into sm.vals by rank; pads (past `valid`)
+// are +0.  Clears the bitmap for a later chunk.  The copies are this thread's own: it waits for
+// them (cp.async.wait_all) before the barrier after which the packing group reads them.
+template <class Geo, class Sm>
+__device__ __forceinline__ void gather_chosen(Sm& sm, int which, const float* ef, int valid,
+                                              int g, int lane) {
+    using F = FinishShape<Geo>;
+    const int w = 32 * g + lane;
+    uint32_t word = sm.sel_bm[which][w];
+    sm.sel_bm[which][w] = 0u;
+    const uint32_t cnt = __popc(word);
+    uint32_t incl = cnt;
 #pragma unroll
-    for (int i = 0; i < kPerLane; ++i) x[i] = sm.vals[kPerLane * lane + i];
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) sm.gcount[g] = incl;
+    named_sync(kBarGather, 32 * F::kGatherWarps);
+    uint32_t rank = incl - cnt;
+    for (int h = 0; h < g; ++h) rank += sm.gcount[h];
+    while (word != 0u) {
+        const int b = __ffs(word) - 1;
+        word &= word - 1u;
+        const int pos = 32 * w + b;
+        if (rank < static_cast<uint32_t>(Geo::kTopK)) {
+            sm.fields[rank] = static_cast<uint16_t>(pos);
+            if (pos < valid) cp_async4(&sm.vals[rank], ef + pos);
+            else sm.vals[rank] = 0.0f;
+        }
+        ++rank;
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// kFast, the packing group (called by its warps only, p = the warp's index in the group): rank
+// r = 32 p + lane's code, its residual written over the stored value (pads excluded), and
+// record words [p b, p b + b).  The scale: max-abs from the chunk's largest key (always among
+// the chosen); mean-abs from the pairwise sum of |a| over ranks 0..k-1 in ascending order
+// divided by k: each warp sums its 32 ranks pairwise (the tree over lanes), and the group
+// combines the warps' sums as the upper levels of the same tree.
+template <class Geo, int kRule, class Sm>
+__device__ __forceinline__ void code_and_pack(Sm& sm, uint8_t* __restrict__ payload,
+                                              float* __restrict__ scales, int64_t c, float* ef,
+                                              int valid, uint32_t mkey, int p, int lane) {
+    using F = FinishShape<Geo>;
+    constexpr int kTopK = Geo::kTopK;
+    constexpr int kB = Geo::kFieldBits;
+    const int r = 32 * p + lane;
+    const float x = sm.vals[r];
+    const uint32_t pos = sm.fields[r];
     float s;
     if constexpr (kRule == kScaleMax) {
-        uint32_t kmax = 0;
-#pragma unroll
-        for (int i = 0; i < kPerLane; ++i) kmax = max(kmax, mag_key(x[i]));
-        s = __fdiv_rn(__uint_as_float(__reduce_max_sync(0xffffffffu, kmax)), 1.5f);
+        s = __fdiv_rn(__uint_as_float(mkey), 1.5f);
     } else {
-        float t[kPerLane];
-#pragma unroll
-        for (int i = 0; i < kPerLane; ++i) t[i] = fabsf(x[i]);
-#pragma unroll
-        for (int w = 1; w < kPerLane; w <<= 1)
-#pragma unroll
-            for (int i = 0; i + w < kPerLane; i += 2 * w) t[i] = __fadd_rn(t[i], t[i + w]);
-        float sum = t[0];
+        float sum = fabsf(x);
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1)
             sum = __fadd_rn(sum, __shfl_down_sync(0xffffffffu, sum, o));
-        s = __fdiv_rn(__shfl_sync(0xffffffffu, sum, 0), static_cast<float>(kTopK));
-    }
+        if constexpr (F::kPackWarps > 1) {
+            if (lane == 0) sm.psum[p] = sum;
+            named_sync(kBarPack, 32 * F::kPackWarps);
+            float t[F::kPackWarps];
 #pragma unroll
-    for (int i = 0; i < kPerLane; ++i) {
-        const int r = kPerLane * lane + i;
-        const uint32_t code = quant_code(x[i], s);
-        const uint32_t pos = static_cast<uint32_t>(sm.fields[r]) >> 2;
-        sm.fields[r] = static_cast<uint16_t>(code | (pos << 2));
-        if (static_cast<int>(pos) < valid) ef[pos] = __fsub_rn(x[i], level_value(code, s));
+            for (int q = 0; q < F::kPackWarps; ++q) t[q] = sm.psum[q];
+#pragma unroll
+            for (int wdt = 1; wdt < F::kPackWarps; wdt <<= 1)
+#pragma unroll
+                for (int q = 0; q + wdt < F::kPackWarps; q += 2 * wdt) t[q] = __fadd_rn(t[q], t[q + wdt]);
+            sum = t[0];
+        } else {
+            sum = __shfl_sync(0xffffffffu, sum, 0);
+        }
+        s = __fdiv_rn(sum, static_cast<float>(kTopK));
     }
-    __syncwarp();
-    pack_record<Geo>(sm, payload, scales, c, s, lane);
+    const uint32_t code = quant_code(x, s);
+    if (static_cast<int>(pos) < valid) ef[pos] = __fsub_rn(x, level_value(code, s));
+    const uint32_t field = code | (pos << 2);
+    // word p b + k (k < b) holds bits [32 k, 32 k + 32) of this warp's 32 fields: field j at
+    // bits [b j, b j + b); a word touches at most 4 fields of >= 13 bits
+    const int k = lane < kB ? lane : kB - 1;
+    const int j_first = (32 * k) / kB;
+    const int j_last = (32 * k + 31) / kB;
+    uint32_t word = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int j = j_first + q;
+        const uint32_t f = __shfl_sync(0xffffffffu, field, j < 32 ? j : 31);
+        if (j <= j_last) {
+            const int off = kB * j - 32 * k;
+            word |= off >= 0 ? (f << off) : (f >> (-off));
+        }
+    }
+    uint32_t* rec = reinterpret_cast<uint32_t*>(payload + c * Geo::kRecordBytes);
+    if (lane < kB) rec[kB * p + lane] = word;
+    if (p == 0 && lane == 0) scales[c] = s;
 }
 
 template <class Geo, int kRule, bool kBf16, bool kEfHost>
@@ -496,21 +619,30 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
     constexpr int kVec = S::kVec;
     constexpr int kStride = S::kStride;
     constexpr int kBitmapWords = S::kBitmapWords;
-    constexpr int kFieldBits = Geo::kFieldBits;
-    constexpr int kRecordWords = Geo::kRecordWords;
-    constexpr int kRecordBytes = Geo::kRecordBytes;
-    // max-abs scale: the packing warp codes the chosen values and writes their residuals
-    // (it overlaps the histogram), except where the owners do it cheaper in registers: with
-    // the error buffer in host memory (k scattered 4-byte writes per chunk would cost the
-    // host link more than the divergent owner step costs) and for k = 128 (four entries per
-    // lane of the packing warp then outlast the histogram: +1 % at L = 4096, +4 % at 8192)
+    constexpr int kWpl = S::kWordsPerLane;
+    using F = FinishShape<Geo>;
+    constexpr int kGatherFirst = kWarps - F::kGatherWarps;   // first warp of the gather group
+    constexpr int kPackFirst = kWarps - F::kPackWarps;       // first warp of the packing group
+    // Two ways to finish a chunk once its positions are chosen:
+    //   - kFast (the usual one): every thread stores its accumulated values unchanged; in the
+    //     next iteration the gather group turns the chunk's bitmap into positions by rank and
+    //     reads their values back (still in L2) beside warp 0's bin search, and the packing
+    //     group codes them, writes their residuals over them and packs the record beside warp
+    //     0's boundary-bin ranking.  No owner step and no prefix barrier: four block barriers
+    //     per chunk.
+    //   - coding in place (max-abs with the error buffer in host memory, where k scattered
+    //     writes per chunk would cost the host link more than the owner step costs, and
+    //     k = 128, whose four entries per lane outlast the histogram): warp 0 forms prefix
+    //     counts of the bitmap, and the owners code their chosen values and form the residuals
+    //     in registers before the one store; five barriers per chunk.
     constexpr bool kCodeInPlace = kRule == kScaleMax && (kEfHost || kTopK > 64);
+    constexpr bool kFast = !kCodeInPlace;
     // the out-of-line select takes the keys through memory.  Handing it a copy made on that
     // path keeps the key registers from also being stored to the stack on every chunk (-4.5 %
     // at k = 64); where registers are scarcer (k = 128, a host error buffer) the copy makes
     // the compiler spill more in the loop instead, so there the keys are passed directly
     constexpr bool kCopyKeys = kTopK <= 64 && !kEfHost;
-    using Sm = Smem<Geo, kRule>;
+    using Sm = Smem<Geo, kRule, kFast>;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Sm& sm = *reinterpret_cast<Sm*>(smem_raw);
     const int tid = threadIdx.x;
@@ -519,9 +651,19 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
     const int64_t total = tab.chunk_begin[tab.num];
     if (static_cast<int64_t>(blockIdx.x) >= total) return;
 
+    // thread 0 locates each chunk once, when it starts the chunk's copies, and leaves it in
+    // shared memory for the CTA
+    if constexpr (kFast) {   // the packing warp clears each bitmap after use; start clean
+        for (int i = tid; i < 2 * kBitmapWords; i += kThreads)
+            sm.sel_bm[i / kBitmapWords][i % kBitmapWords] = 0;
+    }
     if (tid == 0) {
         mbar_init(&sm.bar, 1);
-        const ChunkRef r0 = locate<kChunk, kBf16>(tab, blockIdx.x);
+        sm.next_tensor = 0;
+        const ChunkRef r0 = locate<kChunk, kBf16>(tab, blockIdx.x, sm.next_tensor);
+        sm.next_delta = r0.delta;
+        sm.next_ef = r0.ef;
+        sm.next_valid = r0.valid;
         if (r0.full) prefetch<kChunk, kBf16, kEfHost>(sm, r0);
     }
     __syncthreads();
@@ -529,13 +671,22 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
     uint32_t parity = 0;
     bool nonfinite = false;
     bool aborted = false;
-    int64_t pend_c = -1;     // the chunk whose record the last warp still has to pack
-    float pend_s = 0.0f;
-    float* pend_ef = nullptr;   // mean-abs: that chunk's error buffer and extent
+    int pend_c = -1;         // the chunk whose record the last warp still has to pack
+    float pend_s = 0.0f;     // coding in place: its scale
+    uint32_t pend_mkey = 0;  // kFast: its largest key
+    float* pend_ef = nullptr;   // its error buffer and extent
     int pend_valid = 0;
 
-    for (int64_t c = blockIdx.x; c < total; c += gridDim.x) {
-        const ChunkRef r = locate<kChunk, kBf16>(tab, c);
+    // chunk indices stay below 2^31 (the host checks), so they are 32-bit here
+    const int total32 = static_cast<int>(total);
+    int it = 0;   // this CTA's iteration: kFast alternates the bitmaps by its parity
+    for (int c = blockIdx.x; c < total32; c += gridDim.x, ++it) {
+        const int cur = kFast ? (it & 1) : 0;   // this chunk's bitmap: sm.sel_bm[cur]
+        ChunkRef r;
+        r.delta = sm.next_delta;
+        r.ef = sm.next_ef;
+        r.valid = sm.next_valid;
+        r.full = r.valid == kChunk;
 
         // ---- a = beta * e + delta (from the prefetched stage), and the magnitude keys -----
         float a[kPer];
@@ -555,6 +706,12 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
             kmax = max(kmax, key[i]);
         }
         nonfinite |= kmax >= kKeyInf;
+        if constexpr (kFast) {
+            // the accumulated values go to the error buffer now, unchanged (the packing group
+            // writes the chosen ones' residuals over them in the next iteration): from here on
+            // only the keys stay in registers
+            store_error_buffer<S>(r, a, tid);
+        }
 
         // ---- clear the histogram; chunk max ----------------------------------------------
         // (the previous chunk's select is done, and nothing reads the histogram after it)
@@ -574,30 +731,33 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
             aborted = true;
             break;
         }
-        // the stage has been read by every thread: start the next chunk's copies
-        if (tid == 0 && c + gridDim.x < total) {
-            const ChunkRef rn = locate<kChunk, kBf16>(tab, c + gridDim.x);
+        // the stage has been read by every thread: start the next chunk's copies (and every
+        // thread has read this chunk's location: replace it with the next one's)
+        if (tid == 0 && c + static_cast<int>(gridDim.x) < total32) {
+            const ChunkRef rn = locate<kChunk, kBf16>(tab, c + gridDim.x, sm.next_tensor);
+            sm.next_delta = rn.delta;
+            sm.next_ef = rn.ef;
+            sm.next_valid = rn.valid;
             if (rn.full) prefetch<kChunk, kBf16, kEfHost>(sm, rn);
         }
-        // the previous chunk's owners have read the bitmaps (the barrier above follows their
-        // step): clear them for this chunk's select, which first writes them two barriers on
-        if constexpr (2 * kBitmapWords == kThreads) {
-            if (tid < kBitmapWords) sm.sel_bm[tid] = 0;
-            else sm.eq_bm[tid - kBitmapWords] = 0;
-        } else {
-            for (int i = tid; i < 2 * kBitmapWords; i += kThreads) {
-                if (i < kBitmapWords) sm.sel_bm[i] = 0;
-                else sm.eq_bm[i - kBitmapWords] = 0;
+        if constexpr (!kFast) {
+            // the previous chunk's owners have read the bitmaps (the barrier above follows
+            // their step): clear them for this chunk's select, which first writes them two
+            // barriers on
+            if constexpr (2 * kBitmapWords == kThreads) {
+                if (tid < kBitmapWords) sm.sel_bm[cur][tid] = 0;
+                else sm.eq_bm[tid - kBitmapWords] = 0;
+            } else {
+                for (int i = tid; i < 2 * kBitmapWords; i += kThreads) {
+                    if (i < kBitmapWords) sm.sel_bm[cur][i] = 0;
+                    else sm.eq_bm[i - kBitmapWords] = 0;
+                }
             }
-        }
-        // the last warp packs the previous chunk's record: its fields are complete (the
-        // barrier above follows that chunk's owner step) and are next written after this
-        // chunk's select
-        if (warp == kWarps - 1 && pend_c >= 0) {
-            if constexpr (kCodeInPlace)
+            // the last warp packs the previous chunk's record: its fields are complete (the
+            // barrier above follows that chunk's owner step) and are next written after this
+            // chunk's select
+            if (warp == kWarps - 1 && pend_c >= 0)
                 pack_record<Geo>(sm, payload, scales, pend_c, pend_s, lane);
-            else
-                finish_record<Geo, kRule>(sm, payload, scales, pend_c, pend_ef, pend_valid, lane);
         }
         uint32_t mkey = 0;
 #pragma unroll
@@ -608,18 +768,36 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
         //      few keys, which warp 0 ranks directly.  Otherwise: the generic radix select.
         //      (A narrower first window does not pay: with ~10 % of the keys inside it, nearly
         //      every warp still has a lane that takes the in-window path.)
-        // lo_key puts the largest key exactly in the top bin, so no key needs clamping
+        // lo_key puts the largest key exactly in the top bin; a key below the window counts
+        // in bin 0 (one unconditional atomic per key, no branch), so bin 0 is exact only when
+        // nothing lies below the window (lo_key = 0), and a boundary bin of 0 otherwise
+        // takes the generic select
         const bool windowed = mkey < kKeyInf;
         const uint32_t lo_key = mkey > kWindow ? mkey - kWindow : 0u;
         if (windowed) {
 #pragma unroll
             for (int i = 0; i < kPer; ++i)
-                if (key[i] >= lo_key) atomicAdd(&sm.hist[(key[i] - lo_key) >> 16], 1u);
+                atomicAdd(&sm.hist[(max(key[i], lo_key) - lo_key) >> 16], 1u);
         }
         __syncthreads();
         if (windowed && warp == 0) {
             const bool found = top_digit(sm, kTopK, lane);
             if (lane == 0) sm.full_scan = found ? 0u : 1u;
+        }
+        if constexpr (kFast) {
+            // beside warp 0's bin search: the gather group takes the previous chunk's chosen
+            // positions from its bitmap (complete: a barrier follows that chunk's select),
+            // clears that bitmap and starts reading the chosen values back; the warps between
+            // clear the tie bitmap (warp 0 read it before the previous barrier) for this
+            // chunk's marking, one barrier on
+            if (warp >= kGatherFirst) {
+                if (pend_c >= 0)   // the previous chunk's bitmap is the other one
+                    gather_chosen<Geo>(sm, (it + 1) & 1, pend_ef, pend_valid, warp - kGatherFirst,
+                                       lane);
+            } else {
+                for (int i = tid - 32; i >= 0 && i < kBitmapWords; i += 32 * (kGatherFirst - 1))
+                    sm.eq_bm[i] = 0;
+            }
         }
         __syncthreads();
         if (windowed && sm.full_scan != 0u) {   // uniform: every thread read the same flag
@@ -627,7 +805,7 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
             __syncthreads();
         }
         bool selected = false;
-        if (windowed && sm.bcast[0] != kNotFound) {
+        if (windowed && sm.bcast[0] != kNotFound && (sm.bcast[0] != 0u || lo_key == 0u)) {
             const uint32_t need = kTopK - sm.bcast[1];
             const uint32_t dig = sm.bcast[0];
             const uint32_t in_bin = sm.bcast[2];
@@ -638,25 +816,90 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
                 const uint32_t k_lo = lo_key + (dig << 16);
                 const uint32_t k_hi = k_lo + (1u << 16);
                 const uint32_t k_in = rank_bin ? k_hi : k_lo;
+                if constexpr (kFast) {
+                    // branch-free marking: one predicated OR per vector of four (its positions
+                    // share a bitmap word); a candidate's key offset is kept by position
+                    if (rank_bin) {
 #pragma unroll
-                for (int v = 0; v < kVec; ++v) {
-                    // a vector's four positions share one bitmap word: one OR per vector
-                    const int j0 = v * kStride + 4 * tid;
-                    uint32_t nib = 0;
+                        for (int v = 0; v < kVec; ++v) {
+                            const int j0 = v * kStride + 4 * tid;
+                            uint32_t nib = 0, nib_cd = 0;
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const uint32_t kk = key[4 * v + u];
-                        if (kk >= k_in) {
-                            nib |= 1u << u;
-                        } else if (kk >= k_lo) {
-                            const uint32_t slot = atomicAdd(&sm.ncand, 1u);
-                            if (slot < 64u) sm.cand[slot] = make_uint2(kk, static_cast<uint32_t>(j0 + u));
+                            for (int u = 0; u < 4; ++u) {
+                                const uint32_t kk = key[4 * v + u];
+                                const uint32_t d = kk - k_lo;
+                                const bool cd = d < (1u << 16);
+                                nib |= (kk >= k_hi ? 1u : 0u) << u;
+                                nib_cd |= (cd ? 1u : 0u) << u;
+                                st_u16_if(&sm.keybuf[j0 + u], d, cd);
+                            }
+                            red_or_nonzero(&sm.sel_bm[cur][j0 >> 5], nib << (j0 & 31));
+                            red_or_nonzero(&sm.eq_bm[j0 >> 5], nib_cd << (j0 & 31));
+                        }
+                    } else {
+#pragma unroll
+                        for (int v = 0; v < kVec; ++v) {
+                            const int j0 = v * kStride + 4 * tid;
+                            uint32_t nib = 0;
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+                                nib |= (key[4 * v + u] >= k_lo ? 1u : 0u) << u;
+                            red_or_nonzero(&sm.sel_bm[cur][j0 >> 5], nib << (j0 & 31));
                         }
                     }
-                    if (nib != 0u) atomicOr(&sm.sel_bm[j0 >> 5], nib << (j0 & 31));
+                    // the gather group's read-back copies have landed before the barrier
+                    // after which the packing group reads them
+                    if (warp >= kGatherFirst) asm volatile("cp.async.wait_all;" ::: "memory");
+                } else {
+#pragma unroll
+                    for (int v = 0; v < kVec; ++v) {
+                        // a vector's four positions share one bitmap word: one OR per vector
+                        const int j0 = v * kStride + 4 * tid;
+                        uint32_t nib = 0;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const uint32_t kk = key[4 * v + u];
+                            if (kk >= k_in) {
+                                nib |= 1u << u;
+                            } else if (kk >= k_lo) {
+                                const uint32_t slot = atomicAdd(&sm.ncand, 1u);
+                                if (slot < 64u) sm.cand[slot] = make_uint2(kk, static_cast<uint32_t>(j0 + u));
+                            }
+                        }
+                        if (nib != 0u) atomicOr(&sm.sel_bm[cur][j0 >> 5], nib << (j0 & 31));
+                    }
                 }
                 __syncthreads();
                 if (rank_bin && warp == 0) {
+                    if constexpr (kFast) {
+                        // the candidates in ascending position order, from the tie bitmap
+                        uint32_t w[kWpl];
+                        uint32_t mine = 0;
+#pragma unroll
+                        for (int q = 0; q < kWpl; ++q) {
+                            w[q] = sm.eq_bm[kWpl * lane + q];
+                            mine += __popc(w[q]);
+                        }
+                        uint32_t incl = mine;
+#pragma unroll
+                        for (int o = 1; o < 32; o <<= 1) {
+                            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                            if (lane >= o) incl += y;
+                        }
+                        uint32_t slot = incl - mine;
+#pragma unroll
+                        for (int q = 0; q < kWpl; ++q) {
+                            uint32_t bitsq = w[q];
+                            while (bitsq != 0u) {
+                                const int b = __ffs(bitsq) - 1;
+                                bitsq &= bitsq - 1u;
+                                const uint32_t pos = 32 * (kWpl * lane + q) + b;
+                                if (slot < 64u) sm.cand[slot] = make_uint2(k_lo + sm.keybuf[pos], pos);
+                                ++slot;
+                            }
+                        }
+                        __syncwarp();
+                    }
                     // rank each candidate among the bin's keys (magnitude, then index)
                     if (in_bin <= 32u) {
                         const uint2 me = static_cast<uint32_t>(lane) < in_bin ? sm.cand[lane] : make_uint2(0u, 0u);
@@ -667,7 +910,7 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
                             rank += (ok > me.x || (ok == me.x && oj < me.y)) ? 1u : 0u;
                         }
                         if (static_cast<uint32_t>(lane) < in_bin && rank < need)
-                            atomicOr(&sm.sel_bm[me.y >> 5], 1u << (me.y & 31));
+                            atomicOr(&sm.sel_bm[cur][me.y >> 5], 1u << (me.y & 31));
                     } else {   // 33..64 candidates (dense tops): two per lane
                         const uint2 m0 = sm.cand[lane];
                         const uint2 m1 = static_cast<uint32_t>(lane) + 32u < in_bin ? sm.cand[lane + 32] : make_uint2(0u, 0u);
@@ -683,9 +926,9 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
                             r0 += (ok > m0.x || (ok == m0.x && oj < m0.y)) ? 1u : 0u;
                             r1 += (ok > m1.x || (ok == m1.x && oj < m1.y)) ? 1u : 0u;
                         }
-                        if (r0 < need) atomicOr(&sm.sel_bm[m0.y >> 5], 1u << (m0.y & 31));
+                        if (r0 < need) atomicOr(&sm.sel_bm[cur][m0.y >> 5], 1u << (m0.y & 31));
                         if (static_cast<uint32_t>(lane) + 32u < in_bin && r1 < need)
-                            atomicOr(&sm.sel_bm[m1.y >> 5], 1u << (m1.y & 31));
+                            atomicOr(&sm.sel_bm[cur][m1.y >> 5], 1u << (m1.y & 31));
                     }
                     __syncwarp();
                 }
@@ -693,110 +936,113 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
             }
         }
         if (!selected) {
+            if (kFast && warp >= kGatherFirst) asm volatile("cp.async.wait_all;" ::: "memory");
             if constexpr (kCopyKeys) {
                 uint32_t key_mem[kPer];
 #pragma unroll
                 for (int i = 0; i < kPer; ++i) key_mem[i] = key[i];
-                generic_select<Geo>(sm, key_mem, tid, lane, warp);
+                generic_select<Geo>(sm, cur, key_mem, tid, lane, warp);
             } else {
-                generic_select<Geo>(sm, key, tid, lane, warp);
+                generic_select<Geo>(sm, cur, key, tid, lane, warp);
             }
         }
-
-        // ---- warp 0: chosen positions before each bitmap word ----------------------------
-        if (warp == 0) {
-            if constexpr (S::kWordsPerLane == 4) {
-                const uint4 w4 = *reinterpret_cast<const uint4*>(&sm.sel_bm[4 * lane]);
-                const uint32_t c0 = __popc(w4.x), c1 = __popc(w4.y), c2 = __popc(w4.z);
-                const uint32_t mine = c0 + c1 + c2 + __popc(w4.w);
-                uint32_t incl = mine;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += y;
-                }
-                const uint32_t p0 = incl - mine;
-                *reinterpret_cast<uint2*>(&sm.pre[4 * lane]) =
-                    make_uint2(p0 | ((p0 + c0) << 16), (p0 + c0 + c1) | ((p0 + c0 + c1 + c2) << 16));
-            } else {
-                constexpr int kWpl = S::kWordsPerLane;
-                uint32_t cnt[kWpl];
-                uint32_t mine = 0;
-#pragma unroll
-                for (int q = 0; q < kWpl; ++q) {
-                    cnt[q] = __popc(sm.sel_bm[kWpl * lane + q]);
-                    mine += cnt[q];
-                }
-                uint32_t incl = mine;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += y;
-                }
-                uint32_t run = incl - mine;
-#pragma unroll
-                for (int q = 0; q < kWpl; ++q) {
-                    sm.pre[kWpl * lane + q] = static_cast<uint16_t>(run);
-                    run += cnt[q];
-                }
-            }
+        // kFast: the packing group codes and packs the previous chunk's record while warp 0
+        // ranks this chunk's boundary bin
+        if constexpr (kFast) {
+            if (warp >= kPackFirst && pend_c >= 0)
+                code_and_pack<Geo, kRule>(sm, payload, scales, pend_c, pend_ef, pend_valid,
+                                          pend_mkey, warp - kPackFirst, lane);
         }
-        __syncthreads();
 
-        // ---- owners: rank and value of each chosen value (the last warp codes them and
-        //      writes their residuals; with a host error buffer, code and residual here) -----
         float s = 0.0f;   // coding in place: the max-abs scale
-        if constexpr (kCodeInPlace) s = __fdiv_rn(__uint_as_float(mkey), 1.5f);
+        if constexpr (!kFast) {
+            // ---- warp 0: chosen positions before each bitmap word ------------------------
+            if (warp == 0) {
+                if constexpr (kWpl == 4) {
+                    const uint4 w4 = *reinterpret_cast<const uint4*>(&sm.sel_bm[cur][4 * lane]);
+                    const uint32_t c0 = __popc(w4.x), c1 = __popc(w4.y), c2 = __popc(w4.z);
+                    const uint32_t mine = c0 + c1 + c2 + __popc(w4.w);
+                    uint32_t incl = mine;
 #pragma unroll
-        for (int v = 0; v < kVec; ++v) {
-            const int j0 = v * kStride + 4 * tid;
-            const uint32_t word = sm.sel_bm[j0 >> 5];
-            const int sh = j0 & 31;
-            if (((word >> sh) & 0xfu) == 0u) continue;
-            const uint32_t base_rank = sm.pre[j0 >> 5];
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o) incl += y;
+                    }
+                    const uint32_t p0 = incl - mine;
+                    *reinterpret_cast<uint2*>(&sm.pre[4 * lane]) =
+                        make_uint2(p0 | ((p0 + c0) << 16), (p0 + c0 + c1) | ((p0 + c0 + c1 + c2) << 16));
+                } else {
+                    uint32_t cnt[kWpl];
+                    uint32_t mine = 0;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                if ((word >> (sh + u)) & 1u) {
-                    const uint32_t rank = base_rank + __popc(word & ((1u << (sh + u)) - 1u));
-                    if constexpr (kCodeInPlace) {
+                    for (int q = 0; q < kWpl; ++q) {
+                        cnt[q] = __popc(sm.sel_bm[cur][kWpl * lane + q]);
+                        mine += cnt[q];
+                    }
+                    uint32_t incl = mine;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o) incl += y;
+                    }
+                    uint32_t run = incl - mine;
+#pragma unroll
+                    for (int q = 0; q < kWpl; ++q) {
+                        sm.pre[kWpl * lane + q] = static_cast<uint16_t>(run);
+                        run += cnt[q];
+                    }
+                }
+            }
+            __syncthreads();
+
+            // ---- owners: code each chosen value, form its residual in place, and write its
+            //      field by rank ------------------------------------------------------------
+            s = __fdiv_rn(__uint_as_float(mkey), 1.5f);
+#pragma unroll
+            for (int v = 0; v < kVec; ++v) {
+                const int j0 = v * kStride + 4 * tid;
+                const uint32_t word = sm.sel_bm[cur][j0 >> 5];
+                const int sh = j0 & 31;
+                if (((word >> sh) & 0xfu) == 0u) continue;
+                const uint32_t base_rank = sm.pre[j0 >> 5];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if ((word >> (sh + u)) & 1u) {
+                        const uint32_t rank = base_rank + __popc(word & ((1u << (sh + u)) - 1u));
                         const uint32_t code = quant_code(a[4 * v + u], s);
                         a[4 * v + u] = __fsub_rn(a[4 * v + u], level_value(code, s));
                         if (rank < kTopK)
                             sm.fields[rank] = static_cast<uint16_t>(code | (static_cast<uint32_t>(j0 + u) << 2));
-                    } else if (rank < kTopK) {
-                        sm.vals[rank] = a[4 * v + u];
-                        sm.fields[rank] = static_cast<uint16_t>(static_cast<uint32_t>(j0 + u) << 2);
                     }
                 }
             }
         }
-        if (r.full) {
-#pragma unroll
-            for (int v = 0; v < kVec; ++v)
-                st_stream_f4(r.ef + v * kStride + 4 * tid,
-                             make_float4(a[4 * v], a[4 * v + 1], a[4 * v + 2], a[4 * v + 3]));
-        } else {
-#pragma unroll
-            for (int v = 0; v < kVec; ++v)
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int j = v * kStride + 4 * tid + u;
-                    if (j < r.valid) r.ef[j] = a[4 * v + u];
-                }
-        }
+        // ---- coding in place: the error buffer, stored once, with the residuals ----------
+        if constexpr (!kFast) store_error_buffer<S>(r, a, tid);
 
-        // ---- the record is packed by the last warp at the top of the next iteration ------
+        // ---- the record is packed by the last warp in the next iteration ------------------
         pend_c = c;
         pend_s = s;
+        pend_mkey = mkey;
         pend_ef = r.ef;
         pend_valid = r.valid;
     }
-    __syncthreads();   // the last chunk's fields (and error-buffer stores) are complete
-    if (warp == kWarps - 1 && pend_c >= 0) {
-        if constexpr (kCodeInPlace)
+    __syncthreads();   // the last chunk's select (and error-buffer stores) are complete
+    if constexpr (kFast) {
+        if (pend_c >= 0) {   // uniform
+            if (warp >= kGatherFirst) {
+                gather_chosen<Geo>(sm, (it - 1) & 1, pend_ef, pend_valid, warp - kGatherFirst,
+                                   lane);
+                asm volatile("cp.async.wait_all;" ::: "memory");
+            }
+            __syncthreads();
+            if (warp >= kPackFirst)
+                code_and_pack<Geo, kRule>(sm, payload, scales, pend_c, pend_ef, pend_valid,
+                                          pend_mkey, warp - kPackFirst, lane);
+        }
+    } else {
+        if (warp == kWarps - 1 && pend_c >= 0)
             pack_record<Geo>(sm, payload, scales, pend_c, pend_s, lane);
-        else
-            finish_record<Geo, kRule>(sm, payload, scales, pend_c, pend_ef, pend_valid, lane);
     }
     bool copy_pending = false;
     if (aborted && tid == 0) {
@@ -815,7 +1061,8 @@ template <class Geo, int kRule, bool kBf16, bool kEfHost>
 cudaError_t launch_compress(const CompressTable& tab, int64_t total, float beta, uint8_t* payload,
                             float* scales, uint32_t* flags, cudaStream_t stream) {
     const void* kern = reinterpret_cast<const void*>(&k_ef_compress<Geo, kRule, kBf16, kEfHost>);
-    const size_t smem = sizeof(Smem<Geo, kRule>);
+    constexpr bool kFast = !(kRule == kScaleMax && (kEfHost || Geo::kTopK > 64));
+    const size_t smem = sizeof(Smem<Geo, kRule, kFast>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
