@@ -44,22 +44,22 @@
 namespace spl {
 namespace {
 
-// Prefetch stages in flight per CTA (chunk c + k G's copies go to stage k): one, since the
-// decode is bound by its instructions, not by waits on copies.  The loops and the shared
-// memory layout (room for two mbarriers) also take two.
-constexpr int kStages = 1;
-static_assert(kStages == 1 || kStages == 2, "prefetch stages");
-
 // Per-codec sizes of the receiver (default: 256 threads, 512 positions and 4 vectors per
 // thread of each warp, groups of 64 peers, two entries per lane, seven 16-byte pieces per
-// record).  L = 2048 takes 128 threads (8 CTAs per SM hide its per-chunk fixed costs at the
-// usual peer counts: 0.67 -> 0.56 ms at 24 peers, 2^28 values; 200 peers, where shared memory
-// allows fewer CTAs, run 11 % slower), L = 8192 takes 512, so a warp still holds 512 positions.
-template <class Geo>
+// record, one prefetch stage: chunk c + G's copies fly while chunk c is worked on).  L = 2048
+// takes 128 threads (8 CTAs per SM hide its per-chunk fixed costs at the usual peer counts:
+// 0.67 -> 0.56 ms at 24 peers, 2^28 values; 200 peers, where shared memory allows fewer CTAs,
+// run 11 % slower), L = 8192 takes 512, so a warp still holds 512 positions.
+// kLean (L = 4096, k <= 64, a few peers, no theta, no statistics): 128 threads, so 8 CTAs share
+// an SM, and four prefetch stages (chunks c + G .. c + 4G), cheap without a theta stage: the
+// 8-peer mean of 2^27 values goes from 63 % to 73 % of the measured copy bandwidth.
+template <class Geo, bool kLean = false>
 struct RecvShape {
     static constexpr int kChunk = Geo::kChunk;
     static constexpr int kTopK = Geo::kTopK;
-    static constexpr int kThreads = kChunk == 8192 ? 512 : (kChunk == 2048 ? 128 : 256);
+    static_assert(!kLean || (kChunk == 4096 && kTopK <= 64), "lean receiver shape");
+    static constexpr int kThreads = kLean ? 128 : (kChunk == 8192 ? 512 : (kChunk == 2048 ? 128 : 256));
+    static constexpr int kStages = kLean ? 4 : 1;           // prefetch stages (<= 4 mbarriers)
     static constexpr int kWarps = kThreads / 32;
     static constexpr int kSlice = kChunk / kWarps;          // positions per warp
     static constexpr int kVec = kSlice / 128;               // vectors of 4 per thread
@@ -77,22 +77,26 @@ struct RecvShape {
 
 __host__ __device__ constexpr size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
+// Largest P the lean shape takes (its record stages and entries then still let 7-8 CTAs share
+// an SM).
+constexpr int kLeanMaxPeers = 16;
+
 // Dynamic shared memory for P peers (offsets 16-byte aligned), G = min(P, group):
-//   bar[2] | theta stage [S][4096] f32 | record stage [S][P][112] (+16) | acc [4096] f32 |
+//   bar[4] | theta stage [S][4096] f32 (with theta only) | record stage [S][P][112] (+16) |
+//   acc [4096] f32 |
 //   entries [G][64] (position, value) | validity [G] u32 |
 //   with statistics only: (scale, magnitude | sign << 8 bit counts) [G] | per-peer totals of
 //   this CTA: sum of squares and its Kahan compensation [2][P] f32 | rejected, big, negative
 //   [3][P] u32 | max scale [P] f32
-template <class Geo>
+template <class Geo, class S>
 struct Layout {
     size_t bar, theta, rec, acc, ent, ok, sgrp, st_sq, st_cnt, st_max, total;
-    __host__ __device__ Layout(int P, bool stats) {
-        using S = RecvShape<Geo>;
+    __host__ __device__ Layout(int P, bool stats, bool with_theta) {
         const size_t G = static_cast<size_t>(P < S::kGroup ? P : S::kGroup);
         bar = 0;
-        theta = 16;
-        rec = theta + kStages * S::kChunk * 4;
-        acc = rec + align16(kStages * static_cast<size_t>(P) * Geo::kRecordBytes) + 16;
+        theta = 32;
+        rec = theta + (with_theta ? S::kStages * S::kChunk * 4 : 0);
+        acc = rec + align16(S::kStages * static_cast<size_t>(P) * Geo::kRecordBytes) + 16;
         ent = acc + S::kChunk * 4;
         ok = ent + G * S::kTopK * 8;
         sgrp = ok + align16(G * 4);
@@ -108,11 +112,10 @@ struct Layout {
 // record pieces (7 x 16 B per peer; 4-byte pieces for a variant whose records are not 16-byte
 // aligned) are spread over the threads, each of which arrives once its own copies have
 // landed.  Arrivals per phase: min(pieces, 256) + 1.
-template <class Geo>
+template <class Geo, class S>
 __device__ __forceinline__ void prefetch(const DecodeTable& tab, int P, int64_t c, bool full,
                                          const float* theta, uint64_t* bar, uint8_t* st_rec,
                                          float* st_theta, int tid) {
-    using S = RecvShape<Geo>;
     constexpr int kThreads = S::kThreads;
     constexpr int kChunk = S::kChunk;
     constexpr int kRecordBytes = Geo::kRecordBytes;
@@ -141,12 +144,15 @@ __device__ __forceinline__ void prefetch(const DecodeTable& tab, int P, int64_t 
     }
 }
 
-template <class Geo, bool kStats, bool kPow2>
-__global__ void __launch_bounds__(RecvShape<Geo>::kThreads, RecvShape<Geo>::kMinBlocks)
+template <class Geo, bool kLean, bool kStats, bool kPow2>
+__global__ void __launch_bounds__(RecvShape<Geo, kLean>::kThreads, RecvShape<Geo, kLean>::kMinBlocks)
 k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __restrict__ mean,
-                   float* __restrict__ theta, float neg_lr, bool validate,
+                   float* __restrict__ theta_arg, float neg_lr, bool validate,
                    PeerStats* __restrict__ stats, uint32_t* __restrict__ flags) {
-    using S = RecvShape<Geo>;
+    using S = RecvShape<Geo, kLean>;
+    constexpr int kStages = S::kStages;
+    // the lean shape is launched without theta: knowing so here drops its code and registers
+    float* __restrict__ const theta = kLean ? nullptr : theta_arg;
     constexpr int kThreads = S::kThreads;
     constexpr int kWarps = S::kWarps;
     constexpr int kChunk = S::kChunk;
@@ -157,7 +163,7 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
     constexpr int kPerLane = S::kPerLane;
     constexpr int kRecordBytes = Geo::kRecordBytes;
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    const Layout<Geo> L(P, kStats);
+    const Layout<Geo, S> L(P, kStats, theta != nullptr);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + L.bar);
     float* st_theta = reinterpret_cast<float*>(smem_raw + L.theta);
     uint8_t* st_rec = smem_raw + L.rec;
@@ -201,7 +207,7 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
     for (int st = 0; st < kStages; ++st) {
         const int64_t c = blockIdx.x + st * G;
         if (c < C)
-            prefetch<Geo>(tab, P, c, (c + 1) * kChunk <= n, theta, &bars[st],
+            prefetch<Geo, S>(tab, P, c, (c + 1) * kChunk <= n, theta, &bars[st],
                      st_rec + st * P * kRecordBytes, st_theta + st * kChunk, tid);
     }
     float sc_cur[kSpl];
@@ -294,7 +300,7 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
                 // the stage has been read: start chunk c + S G's copies, and c + G's scales
                 const int64_t c2 = c + kStages * G;
                 if (c2 < C)
-                    prefetch<Geo>(tab, P, c2, (c2 + 1) * kChunk <= n, theta, &bars[st],
+                    prefetch<Geo, S>(tab, P, c2, (c2 + 1) * kChunk <= n, theta, &bars[st],
                              st_rec + st * P * kRecordBytes, st_theta + st * kChunk, tid);
 #pragma unroll
                 for (int i = 0; i < kSpl; ++i)
@@ -433,21 +439,22 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
     }
 }
 
-template <class Geo, bool kStats, bool kPow2>
+template <class Geo, bool kLean, bool kStats, bool kPow2>
 cudaError_t launch_kernel(const DecodeTable& tab, int P, int64_t n, int64_t C, float* mean,
                           float* theta, float lr, bool validate, PeerStats* stats, uint32_t* flags,
                           cudaStream_t stream) {
-    const size_t smem = Layout<Geo>(P, kStats).total;
-    const void* kern = reinterpret_cast<const void*>(&k_decode_aggregate<Geo, kStats, kPow2>);
+    using S = RecvShape<Geo, kLean>;
+    const size_t smem = Layout<Geo, S>(P, kStats, theta != nullptr).total;
+    const void* kern = reinterpret_cast<const void*>(&k_decode_aggregate<Geo, kLean, kStats, kPow2>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    constexpr int kThreads = RecvShape<Geo>::kThreads;
+    constexpr int kThreads = S::kThreads;
     const int resident = persistent_grid(kern, kThreads, smem);
     if (resident <= 0) return cudaErrorInvalidConfiguration;
     const int grid = static_cast<int>(C < resident ? C : resident);
     const float rp = 1.0f / static_cast<float>(P);   // correctly rounded on the host
-    k_decode_aggregate<Geo, kStats, kPow2><<<grid, kThreads, smem, stream>>>(
+    k_decode_aggregate<Geo, kLean, kStats, kPow2><<<grid, kThreads, smem, stream>>>(
         tab, P, rp, n, mean, theta, -lr, validate || kStats, stats, flags);
     return cudaGetLastError();
 }
@@ -460,11 +467,21 @@ cudaError_t launch_decode(const DecodeTable& tab, int P, int64_t n, float* mean,
                           cudaStream_t stream) {
     const int64_t C = (n + Geo::kChunk - 1) / Geo::kChunk;
     if (C == 0) return cudaSuccess;
-    if ((P & (P - 1)) == 0)
-        return launch_kernel<Geo, kStats, true>(tab, P, n, C, mean, theta, lr, validate, stats,
-                                                flags, stream);
-    return launch_kernel<Geo, kStats, false>(tab, P, n, C, mean, theta, lr, validate, stats, flags,
-                                             stream);
+    // the lean shape where it applies: a mean of at most 16 peers with no outer step and no
+    // statistics, for the chunk lengths and k it is built for
+    constexpr bool kLeanOk = !kStats && Geo::kChunk == 4096 && Geo::kTopK <= 64;
+    const bool pow2 = (P & (P - 1)) == 0;
+    if constexpr (kLeanOk) {
+        if (theta == nullptr && P <= kLeanMaxPeers)
+            return pow2 ? launch_kernel<Geo, true, kStats, true>(tab, P, n, C, mean, theta, lr,
+                                                                 validate, stats, flags, stream)
+                        : launch_kernel<Geo, true, kStats, false>(tab, P, n, C, mean, theta, lr,
+                                                                  validate, stats, flags, stream);
+    }
+    return pow2 ? launch_kernel<Geo, false, kStats, true>(tab, P, n, C, mean, theta, lr, validate,
+                                                          stats, flags, stream)
+                : launch_kernel<Geo, false, kStats, false>(tab, P, n, C, mean, theta, lr, validate,
+                                                           stats, flags, stream);
 }
 
 // Launch for one record geometry, with or without statistics (which need validation on).

@@ -630,18 +630,17 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
     //     group codes them, writes their residuals over them and packs the record beside warp
     //     0's boundary-bin ranking.  No owner step and no prefix barrier: four block barriers
     //     per chunk.
-    //   - coding in place (max-abs with the error buffer in host memory, where k scattered
-    //     writes per chunk would cost the host link more than the owner step costs, and
-    //     k = 128, whose four entries per lane outlast the histogram): warp 0 forms prefix
+    //   - coding in place (the error buffer in host memory, where k scattered writes per
+    //     chunk would cost the host link more than the owner step costs): warp 0 forms prefix
     //     counts of the bitmap, and the owners code their chosen values and form the residuals
     //     in registers before the one store; five barriers per chunk.
-    constexpr bool kCodeInPlace = kRule == kScaleMax && (kEfHost || kTopK > 64);
+    constexpr bool kCodeInPlace = kEfHost;
     constexpr bool kFast = !kCodeInPlace;
     // the out-of-line select takes the keys through memory.  Handing it a copy made on that
     // path keeps the key registers from also being stored to the stack on every chunk (-4.5 %
-    // at k = 64); where registers are scarcer (k = 128, a host error buffer) the copy makes
-    // the compiler spill more in the loop instead, so there the keys are passed directly
-    constexpr bool kCopyKeys = kTopK <= 64 && !kEfHost;
+    // at k = 64); with a host error buffer, where registers are scarcer, the copy makes the
+    // compiler spill more in the loop instead, so there the keys are passed directly
+    constexpr bool kCopyKeys = !kEfHost;
     using Sm = Smem<Geo, kRule, kFast>;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Sm& sm = *reinterpret_cast<Sm*>(smem_raw);
@@ -1061,7 +1060,7 @@ template <class Geo, int kRule, bool kBf16, bool kEfHost>
 cudaError_t launch_compress(const CompressTable& tab, int64_t total, float beta, uint8_t* payload,
                             float* scales, uint32_t* flags, cudaStream_t stream) {
     const void* kern = reinterpret_cast<const void*>(&k_ef_compress<Geo, kRule, kBf16, kEfHost>);
-    constexpr bool kFast = !(kRule == kScaleMax && (kEfHost || Geo::kTopK > 64));
+    constexpr bool kFast = !kEfHost;
     const size_t smem = sizeof(Smem<Geo, kRule, kFast>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
