@@ -24,6 +24,8 @@ from ._binding import (  # noqa: F401
     SCALE_MEAN_ABS,
     TOPK,
     SplError,
+    checked_library_path,
+    debug_words,
     decode_aggregate,
     ef_compress,
     ef_compress_multi,
@@ -36,4 +38,5 @@ from ._binding import (  # noqa: F401
     read_peer_stats,
     record_bytes,
     unpack,
+    use_library,
 )

@@ -29,6 +29,7 @@ SCALE_MEAN_ABS = 1    # s = pairwise sum of the chosen |a| / k (codec variant)
 _F32, _BF16 = 0, 1
 _lock = threading.Lock()
 _lib = None
+_lib_path = None   # None: the library this package builds (libspl.so)
 
 
 class SplError(RuntimeError):
@@ -55,20 +56,40 @@ class _Codec(ctypes.Structure):
 
 
 def library_path() -> str:
-    return _build.LIB_PATH
+    return _lib_path or _build.LIB_PATH
+
+
+def checked_library_path() -> str:
+    """Path of the checked build (libspl_checked.so): the same calls, with every kernel memory
+    index tested before the access (include/spl_checked.h)."""
+    return _build.CHECKED_LIB_PATH
+
+
+def use_library(path=None):
+    """Makes later calls go through another build of the library, e.g. checked_library_path();
+    None returns to libspl.so.  Returns the previous selection.  Both builds are built together
+    by build.build(); work already enqueued is not affected."""
+    global _lib, _lib_path
+    with _lock:
+        prev = _lib_path
+        _lib_path = path
+        _lib = None
+        return prev
 
 
 def library():
-    """The loaded libspl.so (built first if missing or older than its sources)."""
+    """The loaded libspl.so, or the build chosen with use_library (built first if missing or
+    older than its sources)."""
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
-        path = _build.LIB_PATH
+        path = _lib_path or _build.LIB_PATH
         if _build.is_stale():
             _build.build()
         if not os.path.exists(path):
-            raise RuntimeError(f"libspl.so is missing at {path}; the CUDA library must be built")
+            raise RuntimeError(f"{os.path.basename(path)} is missing at {path}; the CUDA "
+                               f"library must be built")
         lib = ctypes.CDLL(path)
         vp, sz, ci, cf = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_float
         lib.spl_num_chunks.argtypes, lib.spl_num_chunks.restype = [sz], sz
@@ -97,8 +118,26 @@ def library():
         lib.spl_decode_aggregate_codec.restype = ci
         lib.spl_pack.argtypes, lib.spl_pack.restype = [vp, vp, sz, vp, vp], ci
         lib.spl_unpack.argtypes, lib.spl_unpack.restype = [vp, sz, vp, vp, vp], ci
+        if hasattr(lib, "spl_debug_read"):   # the checked build
+            lib.spl_debug_read.argtypes, lib.spl_debug_read.restype = [vp, ci], ci
         _lib = lib
         return lib
+
+
+DEBUG_WORDS = 16
+DEBUG_NAMES = {0: "sites", 1: "first_site", 2: "first_index", 3: "failures", 8: "chunks",
+               9: "whole", 10: "rank32", 11: "rank64", 12: "full_scan", 13: "generic"}
+
+
+def debug_words(reset: bool = False) -> dict:
+    """Checked build only (use_library(checked_library_path())): the debug words of every kernel
+    since the last reset, by name (spl_debug_read); waits for the device."""
+    lib = library()
+    if not hasattr(lib, "spl_debug_read"):
+        raise RuntimeError("debug_words needs the checked build of the library")
+    out = (ctypes.c_uint32 * DEBUG_WORDS)()
+    _check("spl_debug_read", lib.spl_debug_read(out, 1 if reset else 0))
+    return {name: int(out[i]) for i, name in DEBUG_NAMES.items()}
 
 
 def flags_status(flags) -> int:

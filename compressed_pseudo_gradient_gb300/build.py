@@ -1,8 +1,10 @@
 """Builds libspl.so (the codec's CUDA kernels and C ABI) in-tree for sm_103a with nvcc.
 
 Each translation unit compiles in parallel; the result is linked with the static CUDA runtime
-into ``compressed_pseudo_gradient_gb300/libspl.so``.  Rebuilds only when a source or header is
-newer than the library.
+into ``compressed_pseudo_gradient_gb300/libspl.so``.  The same sources compiled with
+``-DSPL_CHECKED=1`` give ``libspl_checked.so``, a diagnostic build whose kernels test every
+memory index before the access (recording, not trapping, a bad one; see include/spl_checked.h).
+Rebuilds only when a source or header is newer than the libraries.
 """
 from __future__ import annotations
 
@@ -17,6 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libspl.so")
+CHECKED_LIB_PATH = os.path.join(PKG, "libspl_checked.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = [
@@ -46,28 +49,35 @@ def _deps():
 
 
 def is_stale() -> bool:
-    if not os.path.exists(LIB_PATH):
-        return True
-    t = os.path.getmtime(LIB_PATH)
-    return any(os.path.getmtime(p) > t for p in _deps())
+    for lib in (LIB_PATH, CHECKED_LIB_PATH):
+        if not os.path.exists(lib):
+            return True
+        t = os.path.getmtime(lib)
+        if any(os.path.getmtime(p) > t for p in _deps()):
+            return True
+    return False
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link libspl.so if stale (or when forced); returns its path."""
+    """Compile and link libspl.so and libspl_checked.so if stale (or when forced); returns the
+    path of libspl.so."""
     if not force and not is_stale():
         return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
     cc = nvcc()
+    variants = [(LIB_PATH, BUILD_DIR, []),
+                (CHECKED_LIB_PATH, os.path.join(BUILD_DIR, "checked"), ["-DSPL_CHECKED=1"])]
     procs = []
-    objs = []
-    for src in _sources():
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
-        cmd = [cc, *NVCC_FLAGS, "-c", src, "-o", obj]
-        if verbose:
-            cmd.insert(1, "-Xptxas=-v")
-        procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE,
-                                            stderr=subprocess.STDOUT, text=True)))
-        objs.append(obj)
+    objs = {lib: [] for lib, _, _ in variants}
+    for lib, odir, extra in variants:
+        os.makedirs(odir, exist_ok=True)
+        for src in _sources():
+            obj = os.path.join(odir, os.path.basename(src)[:-3] + ".o")
+            cmd = [cc, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
+            if verbose:
+                cmd.insert(1, "-Xptxas=-v")
+            procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE,
+                                                stderr=subprocess.STDOUT, text=True)))
+            objs[lib].append(obj)
     failed = []
     for src, p in procs:
         out, _ = p.communicate()
@@ -77,9 +87,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
             failed.append(src)
     if failed:
         raise RuntimeError(f"nvcc failed on {', '.join(os.path.basename(f) for f in failed)}")
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
-    subprocess.run([cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs], check=True)
-    os.replace(tmp, LIB_PATH)
+    for lib, _, _ in variants:
+        tmp = lib + f".tmp{os.getpid()}"
+        subprocess.run([cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs[lib]],
+                       check=True)
+        os.replace(tmp, lib)
     return LIB_PATH
 
 

@@ -14,4 +14,8 @@ cudaError_t launch_decode_aggregate(const DecodeTable& tab, const Codec& cd, int
                                            stream);
 }
 
+#if SPL_CHECKED
+SPL_DEBUG_READER(debug_read_decode)
+#endif
+
 }  // namespace spl

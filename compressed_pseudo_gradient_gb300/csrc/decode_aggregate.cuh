@@ -113,9 +113,9 @@ struct Layout {
 // aligned) are spread over the threads, each of which arrives once its own copies have
 // landed.  Arrivals per phase: min(pieces, 256) + 1.
 template <class Geo, class S>
-__device__ __forceinline__ void prefetch(const DecodeTable& tab, int P, int64_t c, bool full,
-                                         const float* theta, uint64_t* bar, uint8_t* st_rec,
-                                         float* st_theta, int tid) {
+__device__ __forceinline__ void prefetch(const DecodeTable& tab, int P, int64_t c, int64_t C,
+                                         bool full, const float* theta, uint64_t* bar,
+                                         uint8_t* st_rec, float* st_theta, int tid) {
     constexpr int kThreads = S::kThreads;
     constexpr int kChunk = S::kChunk;
     constexpr int kRecordBytes = Geo::kRecordBytes;
@@ -135,6 +135,7 @@ __device__ __forceinline__ void prefetch(const DecodeTable& tab, int P, int64_t 
         for (int i = tid; i < pieces; i += kThreads) {
             const int p = i / kPieces;
             const int w = i - p * kPieces;
+            if (!SPL_CHECK(c < C && p < P, kSiteRecCopy, c)) continue;
             if constexpr (kPieceBytes == 16)
                 cp_async16(st_rec + i * 16, tab.payload[p] + c * kRecordBytes + w * 16);
             else
@@ -207,7 +208,7 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
     for (int st = 0; st < kStages; ++st) {
         const int64_t c = blockIdx.x + st * G;
         if (c < C)
-            prefetch<Geo, S>(tab, P, c, (c + 1) * kChunk <= n, theta, &bars[st],
+            prefetch<Geo, S>(tab, P, c, C, (c + 1) * kChunk <= n, theta, &bars[st],
                      st_rec + st * P * kRecordBytes, st_theta + st * kChunk, tid);
     }
     float sc_cur[kSpl];
@@ -245,11 +246,13 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
             for (int g = warp; g < gn; g += kWarps) {
                 const int p = g0 + g;
                 const uint32_t* words = reinterpret_cast<const uint32_t*>(rec + p * kRecordBytes);
-                // entry lane + 32 m of the record, m = 0 .. k/32 - 1
+                // entry lane + 32 m of the record, m = 0 .. k/32 - 1 (its two words lie inside
+                // the stage and the 16 bytes after it)
                 uint32_t f[kPerLane], ix[kPerLane];
 #pragma unroll
                 for (int m = 0; m < kPerLane; ++m) {
-                    f[m] = record_field_fs<Geo::kFieldBits>(words, lane + 32 * m);
+                    f[m] = SPL_CHECK(p < P && g < kGroup, kSiteRecStage, p)
+                               ? record_field_fs<Geo::kFieldBits>(words, lane + 32 * m) : 0u;
                     ix[m] = f[m] >> 2;
                 }
                 const int slot = p / (32 * kWarps);   // the same for the whole warp
@@ -300,7 +303,7 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
                 // the stage has been read: start chunk c + S G's copies, and c + G's scales
                 const int64_t c2 = c + kStages * G;
                 if (c2 < C)
-                    prefetch<Geo, S>(tab, P, c2, (c2 + 1) * kChunk <= n, theta, &bars[st],
+                    prefetch<Geo, S>(tab, P, c2, C, (c2 + 1) * kChunk <= n, theta, &bars[st],
                              st_rec + st * P * kRecordBytes, st_theta + st * kChunk, tid);
 #pragma unroll
                 for (int i = 0; i < kSpl; ++i)
@@ -310,7 +313,8 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
             }
             // ---- the other warps, meanwhile: per-peer statistics, one record per thread ----
             // (a group holds at most 64 peers; peer p is always thread 32 + p mod 64)
-            if (kStats && tid >= 32 && tid - 32 < gn) {
+            if (kStats && tid >= 32 && tid - 32 < gn &&
+                SPL_CHECK(g0 + tid - 32 < P, kSiteStats, g0 + tid - 32)) {
                 const int g = tid - 32;
                 const int p = g0 + g;
                 if (okp[g] == 0u) {
@@ -356,7 +360,8 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
                     if (ok != 0u) {
 #pragma unroll
                         for (int m = 0; m < kPerLane; ++m)
-                            acc[e[m].x] = __fadd_rn(acc[e[m].x], __uint_as_float(e[m].y));
+                            if (SPL_CHECK(e[m].x < static_cast<uint32_t>(kChunk), kSiteAcc, e[m].x))
+                                acc[e[m].x] = __fadd_rn(acc[e[m].x], __uint_as_float(e[m].y));
                     }
                     __syncwarp();
                 }
@@ -384,6 +389,7 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
                 m4.z = div_rn(m4.z, pf, rp);
                 m4.w = div_rn(m4.w, pf, rp);
             }
+            if (!SPL_CHECK(j0 + 3 < kChunk, kSiteMean, j0)) continue;
             if (full) {
                 st_stream_f4(mean + base + j0, m4);
                 if (theta != nullptr) {
@@ -399,7 +405,7 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int j = j0 + u;
-                    if (j < valid) {
+                    if (j < valid && SPL_CHECK(base + j < n, kSiteMean, j)) {
                         mean[base + j] = m[u];
                         if (theta != nullptr)
                             theta[base + j] = __fmaf_rn(neg_lr, m[u], theta[base + j]);

@@ -24,4 +24,8 @@ cudaError_t launch_decode_aggregate_variant(const DecodeTable& tab, const Codec&
     return cudaErrorNotSupported;
 }
 
+#if SPL_CHECKED
+SPL_DEBUG_READER(debug_read_decode_variants)
+#endif
+
 }  // namespace spl

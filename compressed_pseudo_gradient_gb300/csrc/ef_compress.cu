@@ -13,4 +13,8 @@ cudaError_t launch_ef_compress(const CompressTable& tab, const Codec& cd, bool b
     return launch_ef_compress_variant(tab, cd, bf16, ef_host, beta, payload, scales, flags, stream);
 }
 
+#if SPL_CHECKED
+SPL_DEBUG_READER(debug_read_compress)
+#endif
+
 }  // namespace spl

@@ -221,6 +221,7 @@ __device__ __forceinline__ ChunkRef locate(const CompressTable& tab, int64_t c, 
 template <int kChunk, bool kBf16, bool kEfHost, class Sm>
 __device__ __forceinline__ void prefetch(Sm& sm, const ChunkRef& r) {
     constexpr uint32_t kDeltaBytes = kChunk * (kBf16 ? 2 : 4);
+    if (!SPL_CHECK(r.full, kSiteBulk, r.valid)) return;
     fence_async_smem();
     mbar_expect_tx(&sm.bar, (kEfHost ? 0u : kChunk * 4u) + kDeltaBytes);
     if constexpr (!kEfHost) bulk_load(sm.stage_e, r.ef, kChunk * 4, &sm.bar);
@@ -241,6 +242,7 @@ __device__ __forceinline__ void accumulate_from_stage(const Sm& sm, const ChunkR
 #pragma unroll
     for (int v = 0; v < kVec; ++v) {
         const int j0 = v * S::kStride + 4 * tid;
+        if (!SPL_CHECK(j0 + 3 < S::kChunk, kSiteStage, j0)) continue;
         const float4 e4 = kEfHost ? eh[v] : *reinterpret_cast<const float4*>(&sm.stage_e[j0]);
         float d[4];
         if constexpr (kBf16) {
@@ -271,7 +273,7 @@ __device__ __forceinline__ void accumulate_tail(const ChunkRef& r, float beta, i
         for (int u = 0; u < 4; ++u) {
             const int j = v * S::kStride + 4 * tid + u;
             float d = 0.0f, e = 0.0f;
-            if (j < r.valid) {
+            if (j < r.valid && SPL_CHECK(r.valid <= S::kChunk, kSiteTail, r.valid)) {
                 e = r.ef[j];
                 d = kBf16 ? bf16_bits_to_float(static_cast<const uint16_t*>(r.delta)[j])
                           : static_cast<const float*>(r.delta)[j];
@@ -305,15 +307,17 @@ __device__ __forceinline__ void store_error_buffer(const ChunkRef& r, const floa
     if (r.full) {
 #pragma unroll
         for (int v = 0; v < S::kVec; ++v)
-            st_stream_f4(r.ef + v * S::kStride + 4 * tid,
-                         make_float4(a[4 * v], a[4 * v + 1], a[4 * v + 2], a[4 * v + 3]));
+            if (SPL_CHECK(v * S::kStride + 4 * tid + 3 < S::kChunk, kSiteEfStore, 4 * tid))
+                st_stream_f4(r.ef + v * S::kStride + 4 * tid,
+                             make_float4(a[4 * v], a[4 * v + 1], a[4 * v + 2], a[4 * v + 3]));
     } else {
 #pragma unroll
         for (int v = 0; v < S::kVec; ++v)
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int j = v * S::kStride + 4 * tid + u;
-                if (j < r.valid) r.ef[j] = a[4 * v + u];
+                if (j < r.valid && SPL_CHECK(r.valid <= S::kChunk, kSiteEfStore, r.valid))
+                    r.ef[j] = a[4 * v + u];
             }
     }
 }
@@ -339,7 +343,9 @@ __device__ __noinline__ void generic_select(Sm& sm, int cur,
     }
     __syncthreads();
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) atomicAdd(&sm.hist[key[i] >> 20], 1u);
+    for (int i = 0; i < kPer; ++i)
+        if (SPL_CHECK((key[i] >> 20) < 2048u, kSiteGenericHist, key[i]))
+            atomicAdd(&sm.hist[key[i] >> 20], 1u);
     __syncthreads();
     find_digit<2048, S>(sm, sm.hist, kTopK, tid, lane, warp);
     __syncthreads();
@@ -354,7 +360,9 @@ __device__ __noinline__ void generic_select(Sm& sm, int cur,
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int j = v * kStride + 4 * tid + u;
-                if ((key[4 * v + u] >> 20) >= dig) atomicOr(&sm.sel_bm[cur][j >> 5], 1u << (j & 31));
+                if ((key[4 * v + u] >> 20) >= dig &&
+                    SPL_CHECK((j >> 5) < S::kBitmapWords, kSiteBitmap, j))
+                    atomicOr(&sm.sel_bm[cur][j >> 5], 1u << (j & 31));
             }
         __syncthreads();
     } else {
@@ -398,6 +406,7 @@ __device__ __noinline__ void generic_select(Sm& sm, int cur,
             for (int u = 0; u < 4; ++u) {
                 const uint32_t mk = key[4 * v + u] & pmask;
                 const int j = v * kStride + 4 * tid + u;
+                if (!SPL_CHECK((j >> 5) < S::kBitmapWords, kSiteBitmap, j)) continue;
                 if (mk > prefix) atomicOr(&sm.sel_bm[cur][j >> 5], 1u << (j & 31));
                 else if (mk == prefix) atomicOr(&sm.eq_bm[j >> 5], 1u << (j & 31));
             }
@@ -533,7 +542,7 @@ __device__ __forceinline__ void gather_chosen(Sm& sm, int which, const float* ef
         const int b = __ffs(word) - 1;
         word &= word - 1u;
         const int pos = 32 * w + b;
-        if (rank < static_cast<uint32_t>(Geo::kTopK)) {
+        if (SPL_CHECK(rank < static_cast<uint32_t>(Geo::kTopK), kSiteFields, rank)) {
             sm.fields[rank] = static_cast<uint16_t>(pos);
             if (pos < valid) cp_async4(&sm.vals[rank], ef + pos);
             else sm.vals[rank] = 0.0f;
@@ -584,7 +593,9 @@ __device__ __forceinline__ void code_and_pack(Sm& sm, uint8_t* __restrict__ payl
         s = __fdiv_rn(sum, static_cast<float>(kTopK));
     }
     const uint32_t code = quant_code(x, s);
-    if (static_cast<int>(pos) < valid) ef[pos] = __fsub_rn(x, level_value(code, s));
+    if (static_cast<int>(pos) < valid &&
+        SPL_CHECK(valid <= SendShape<Geo>::kChunk, kSiteEfStore, pos))
+        ef[pos] = __fsub_rn(x, level_value(code, s));
     const uint32_t field = code | (pos << 2);
     // word p b + k (k < b) holds bits [32 k, 32 k + 32) of this warp's 32 fields: field j at
     // bits [b j, b j + b); a word touches at most 4 fields of >= 13 bits
@@ -602,7 +613,8 @@ __device__ __forceinline__ void code_and_pack(Sm& sm, uint8_t* __restrict__ payl
         }
     }
     uint32_t* rec = reinterpret_cast<uint32_t*>(payload + c * Geo::kRecordBytes);
-    if (lane < kB) rec[kB * p + lane] = word;
+    if (lane < kB && SPL_CHECK(kB * p + lane < Geo::kRecordWords, kSiteRecord, kB * p + lane))
+        rec[kB * p + lane] = word;
     if (p == 0 && lane == 0) scales[c] = s;
 }
 
@@ -775,8 +787,10 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
         const uint32_t lo_key = mkey > kWindow ? mkey - kWindow : 0u;
         if (windowed) {
 #pragma unroll
-            for (int i = 0; i < kPer; ++i)
-                atomicAdd(&sm.hist[(max(key[i], lo_key) - lo_key) >> 16], 1u);
+            for (int i = 0; i < kPer; ++i) {
+                const uint32_t bin = (max(key[i], lo_key) - lo_key) >> 16;
+                if (SPL_CHECK(bin < 2048u, kSiteHist, bin)) atomicAdd(&sm.hist[bin], 1u);
+            }
         }
         __syncthreads();
         if (windowed && warp == 0) {
@@ -800,9 +814,11 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
         }
         __syncthreads();
         if (windowed && sm.full_scan != 0u) {   // uniform: every thread read the same flag
+            if (tid == 0) SPL_COUNT(kDbgFullScan);
             find_digit<2048, S>(sm, sm.hist, kTopK, tid, lane, warp);
             __syncthreads();
         }
+        if (tid == 0) SPL_COUNT(kDbgChunks);
         bool selected = false;
         if (windowed && sm.bcast[0] != kNotFound && (sm.bcast[0] != 0u || lo_key == 0u)) {
             const uint32_t need = kTopK - sm.bcast[1];
@@ -810,6 +826,7 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
             const uint32_t in_bin = sm.bcast[2];
             if (in_bin == need || in_bin <= 64u) {
                 const bool rank_bin = in_bin != need;
+                if (tid == 0) SPL_COUNT(rank_bin ? (in_bin <= 32u ? kDbgRank32 : kDbgRank64) : kDbgWhole);
                 // bin D as a key range [k_lo, k_hi): keys at or above k_hi are in, keys in the
                 // range are in when the bin is taken whole, else they are the candidates
                 const uint32_t k_lo = lo_key + (dig << 16);
@@ -830,10 +847,13 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
                                 const bool cd = d < (1u << 16);
                                 nib |= (kk >= k_hi ? 1u : 0u) << u;
                                 nib_cd |= (cd ? 1u : 0u) << u;
-                                st_u16_if(&sm.keybuf[j0 + u], d, cd);
+                                if (SPL_CHECK(j0 + u < kChunk, kSiteKeybuf, j0 + u))
+                                    st_u16_if(&sm.keybuf[j0 + u], d, cd);
                             }
-                            red_or_nonzero(&sm.sel_bm[cur][j0 >> 5], nib << (j0 & 31));
-                            red_or_nonzero(&sm.eq_bm[j0 >> 5], nib_cd << (j0 & 31));
+                            if (SPL_CHECK((j0 >> 5) < kBitmapWords, kSiteBitmap, j0)) {
+                                red_or_nonzero(&sm.sel_bm[cur][j0 >> 5], nib << (j0 & 31));
+                                red_or_nonzero(&sm.eq_bm[j0 >> 5], nib_cd << (j0 & 31));
+                            }
                         }
                     } else {
 #pragma unroll
@@ -843,7 +863,8 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
 #pragma unroll
                             for (int u = 0; u < 4; ++u)
                                 nib |= (key[4 * v + u] >= k_lo ? 1u : 0u) << u;
-                            red_or_nonzero(&sm.sel_bm[cur][j0 >> 5], nib << (j0 & 31));
+                            if (SPL_CHECK((j0 >> 5) < kBitmapWords, kSiteBitmap, j0))
+                                red_or_nonzero(&sm.sel_bm[cur][j0 >> 5], nib << (j0 & 31));
                         }
                     }
                     // the gather group's read-back copies have landed before the barrier
@@ -865,7 +886,8 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
                                 if (slot < 64u) sm.cand[slot] = make_uint2(kk, static_cast<uint32_t>(j0 + u));
                             }
                         }
-                        if (nib != 0u) atomicOr(&sm.sel_bm[cur][j0 >> 5], nib << (j0 & 31));
+                        if (nib != 0u && SPL_CHECK((j0 >> 5) < kBitmapWords, kSiteBitmap, j0))
+                            atomicOr(&sm.sel_bm[cur][j0 >> 5], nib << (j0 & 31));
                     }
                 }
                 __syncthreads();
@@ -893,7 +915,8 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
                                 const int b = __ffs(bitsq) - 1;
                                 bitsq &= bitsq - 1u;
                                 const uint32_t pos = 32 * (kWpl * lane + q) + b;
-                                if (slot < 64u) sm.cand[slot] = make_uint2(k_lo + sm.keybuf[pos], pos);
+                                if (SPL_CHECK(slot < 64u && pos < static_cast<uint32_t>(kChunk), kSiteCand, slot))
+                                    sm.cand[slot] = make_uint2(k_lo + sm.keybuf[pos], pos);
                                 ++slot;
                             }
                         }
@@ -908,7 +931,8 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
                             const uint32_t oj = __shfl_sync(0xffffffffu, me.y, o);
                             rank += (ok > me.x || (ok == me.x && oj < me.y)) ? 1u : 0u;
                         }
-                        if (static_cast<uint32_t>(lane) < in_bin && rank < need)
+                        if (static_cast<uint32_t>(lane) < in_bin && rank < need &&
+                            SPL_CHECK((me.y >> 5) < kBitmapWords, kSiteBitmap, me.y))
                             atomicOr(&sm.sel_bm[cur][me.y >> 5], 1u << (me.y & 31));
                     } else {   // 33..64 candidates (dense tops): two per lane
                         const uint2 m0 = sm.cand[lane];
@@ -925,8 +949,10 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
                             r0 += (ok > m0.x || (ok == m0.x && oj < m0.y)) ? 1u : 0u;
                             r1 += (ok > m1.x || (ok == m1.x && oj < m1.y)) ? 1u : 0u;
                         }
-                        if (r0 < need) atomicOr(&sm.sel_bm[cur][m0.y >> 5], 1u << (m0.y & 31));
-                        if (static_cast<uint32_t>(lane) + 32u < in_bin && r1 < need)
+                        if (r0 < need && SPL_CHECK((m0.y >> 5) < kBitmapWords, kSiteBitmap, m0.y))
+                            atomicOr(&sm.sel_bm[cur][m0.y >> 5], 1u << (m0.y & 31));
+                        if (static_cast<uint32_t>(lane) + 32u < in_bin && r1 < need &&
+                            SPL_CHECK((m1.y >> 5) < kBitmapWords, kSiteBitmap, m1.y))
                             atomicOr(&sm.sel_bm[cur][m1.y >> 5], 1u << (m1.y & 31));
                     }
                     __syncwarp();
@@ -935,6 +961,7 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
             }
         }
         if (!selected) {
+            if (tid == 0) SPL_COUNT(kDbgGeneric);
             if (kFast && warp >= kGatherFirst) asm volatile("cp.async.wait_all;" ::: "memory");
             if constexpr (kCopyKeys) {
                 uint32_t key_mem[kPer];

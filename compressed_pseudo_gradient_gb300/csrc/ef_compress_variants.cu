@@ -36,4 +36,8 @@ cudaError_t launch_ef_compress_variant(const CompressTable& tab, const Codec& cd
     return cudaErrorNotSupported;
 }
 
+#if SPL_CHECKED
+SPL_DEBUG_READER(debug_read_compress_variants)
+#endif
+
 }  // namespace spl

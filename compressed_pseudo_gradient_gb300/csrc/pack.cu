@@ -23,6 +23,7 @@ k_pack(const uint16_t* __restrict__ idx, const uint8_t* __restrict__ codes, int6
     for (int64_t c = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5; c < C;
          c += warps) {
         const int64_t e = c * kTopK;
+        if (!SPL_CHECK(c < C, kSitePack, c)) continue;
         const uint32_t f0 = (codes[e + lane] & 3u) | ((idx[e + lane] & 0xfffu) << 2);
         const uint32_t f1 = (codes[e + lane + 32] & 3u) | ((idx[e + lane + 32] & 0xfffu) << 2);
         store_record(payload + c * kRecordBytes, record_word(f0, f1, lane), lane);
@@ -36,6 +37,7 @@ k_unpack(const uint8_t* __restrict__ payload, int64_t C, uint16_t* __restrict__ 
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (kThreads / 32);
     for (int64_t c = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5; c < C;
          c += warps) {
+        if (!SPL_CHECK(c < C, kSitePack, c)) continue;
         const uint32_t* words = reinterpret_cast<const uint32_t*>(payload + c * kRecordBytes);
         const uint32_t mine = lane < kRecordWords ? words[lane] : 0u;
         const int64_t e = c * kTopK;
@@ -63,6 +65,10 @@ int warp_grid(int64_t C) {
 }
 
 }  // namespace
+
+#if SPL_CHECKED
+SPL_DEBUG_READER(debug_read_pack)
+#endif
 
 cudaError_t launch_pack(const uint16_t* idx, const uint8_t* codes, int64_t C, uint8_t* payload,
                         cudaStream_t stream) {

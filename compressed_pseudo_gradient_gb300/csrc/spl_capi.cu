@@ -5,7 +5,11 @@
 #include <mutex>
 
 #include "spl.h"
+#include "spl_device.cuh"
 #include "spl_kernels.h"
+#if SPL_CHECKED
+#include "spl_checked.h"
+#endif
 
 namespace {
 
@@ -338,6 +342,32 @@ spl_status spl_decode_aggregate_stats(const uint8_t* const* payloads, const floa
     return decode_impl(cd, payloads, scales, P, n, mean_out, theta, lr, true, d_stats, d_flags,
                        stream);
 }
+
+#if SPL_CHECKED
+// Checked build: the debug arrays of every translation unit, merged (failed-check sites OR-ed,
+// the first failure of the first unit that saw one, counts added).  Synchronises the device
+// (symbol copies).
+spl_status spl_debug_read(uint32_t* out, int reset) {
+    if (out == nullptr) return SPL_ERR_INVALID_ARG;
+    cudaError_t (*const readers[])(uint32_t*, bool) = {
+        spl::debug_read_compress, spl::debug_read_compress_variants, spl::debug_read_decode,
+        spl::debug_read_decode_variants, spl::debug_read_pack};
+    for (int w = 0; w < spl::kDebugWords; ++w) out[w] = 0;
+    for (auto rd : readers) {
+        uint32_t d[spl::kDebugWords];
+        const spl_status st = cuda_status(rd(d, reset != 0));
+        if (st != SPL_OK) return st;
+        out[spl::kDbgSites] |= d[spl::kDbgSites];
+        if (out[spl::kDbgFirstSite] == 0 && d[spl::kDbgFirstSite] != 0) {
+            out[spl::kDbgFirstSite] = d[spl::kDbgFirstSite];
+            out[spl::kDbgFirstIndex] = d[spl::kDbgFirstIndex];
+        }
+        out[spl::kDbgFailures] += d[spl::kDbgFailures];
+        for (int w = spl::kDbgChunks; w < spl::kDebugWords; ++w) out[w] += d[w];
+    }
+    return SPL_OK;
+}
+#endif
 
 spl_status spl_pack(const uint16_t* idx, const uint8_t* codes, size_t num_chunks, uint8_t* payload,
                     spl_stream_t stream) {

@@ -48,6 +48,58 @@ constexpr uint32_t kFlagBadRecord = 2u;
 constexpr uint32_t kFlagTimeout = 4u;
 constexpr uint32_t kFlagCopyPending = 8u;   // after a timeout, the copy's own wait ran out too
 
+// ---- checked build (compiled with -DSPL_CHECKED=1 into a library of its own) ---------------
+// Every shared- and global-memory index of the kernels is tested before the access; an index
+// out of range is recorded in a device debug array of this translation unit and the access is
+// skipped (nothing traps).  The same array counts which select path each chunk took.  In the
+// normal build SPL_CHECK is the constant true and SPL_COUNT nothing, so the code is unchanged.
+constexpr int kDebugWords = 16;
+enum DebugWord : int {
+    kDbgSites = 0,        // OR of 1 << site over failed checks
+    kDbgFirstSite = 1,    // site + 1 of the first failed check (0: none)
+    kDbgFirstIndex = 2,   // its index (low 32 bits)
+    kDbgFailures = 3,     // failed checks
+    kDbgChunks = 8,       // sender chunks (fast-flow kernels)
+    kDbgWhole = 9,        // ... whose boundary bin was taken whole
+    kDbgRank32 = 10,      // ... whose boundary bin (<= 32 keys) was ranked
+    kDbgRank64 = 11,      // ... whose boundary bin (33..64 keys) was ranked
+    kDbgFullScan = 12,    // ... whose bin search went past the top 512 bins
+    kDbgGeneric = 13      // ... that took the generic radix select
+};
+enum CheckSite : uint32_t {
+    kSiteStage = 0, kSiteTail, kSiteHist, kSiteKeybuf, kSiteBitmap, kSiteCand, kSiteFields,
+    kSiteEfStore, kSiteRecord, kSiteBulk, kSiteGenericHist, kSiteRecStage, kSiteAcc, kSiteEnt,
+    kSiteMean, kSiteRecCopy, kSiteScale, kSiteStats, kSitePack
+};
+
+#if SPL_CHECKED
+namespace {   // one array per translation unit
+__device__ uint32_t g_debug[kDebugWords];
+__device__ __noinline__ bool spl_check_failed(uint32_t site, uint64_t index) {
+    atomicOr(&g_debug[kDbgSites], 1u << (site & 31u));
+    atomicAdd(&g_debug[kDbgFailures], 1u);
+    if (atomicCAS(&g_debug[kDbgFirstSite], 0u, site + 1u) == 0u)
+        g_debug[kDbgFirstIndex] = static_cast<uint32_t>(index);
+    return false;
+}
+}  // namespace
+#define SPL_CHECK(cond, site, index) ((cond) ? true : ::spl::spl_check_failed((site), (index)))
+#define SPL_COUNT(word) atomicAdd(&::spl::g_debug[(word)], 1u)
+// Host side, one per translation unit: copy (and optionally clear) this unit's debug array.
+#define SPL_DEBUG_READER(fn)                                                                  \
+    cudaError_t fn(uint32_t* out, bool reset) {                                               \
+        cudaError_t e = cudaMemcpyFromSymbol(out, g_debug, sizeof(uint32_t) * kDebugWords);  \
+        if (e == cudaSuccess && reset) {                                                      \
+            const uint32_t zero[kDebugWords] = {0};                                           \
+            e = cudaMemcpyToSymbol(g_debug, zero, sizeof zero);                               \
+        }                                                                                     \
+        return e;                                                                             \
+    }
+#else
+#define SPL_CHECK(cond, site, index) true
+#define SPL_COUNT(word) ((void)0)
+#endif
+
 // Upper bound on any wait for an asynchronous copy: a healthy copy lands in microseconds.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 

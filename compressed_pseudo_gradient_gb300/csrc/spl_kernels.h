@@ -91,6 +91,16 @@ cudaError_t launch_pack(const uint16_t* idx, const uint8_t* codes, int64_t C,
 cudaError_t launch_unpack(const uint8_t* payload, int64_t C, uint16_t* idx, uint8_t* codes,
                           cudaStream_t stream);
 
+#if SPL_CHECKED
+// Checked build only: each translation unit's debug array (see spl_device.cuh), copied to out
+// (kDebugWords words) and cleared when reset is set.
+cudaError_t debug_read_compress(uint32_t* out, bool reset);
+cudaError_t debug_read_compress_variants(uint32_t* out, bool reset);
+cudaError_t debug_read_decode(uint32_t* out, bool reset);
+cudaError_t debug_read_decode_variants(uint32_t* out, bool reset);
+cudaError_t debug_read_pack(uint32_t* out, bool reset);
+#endif
+
 // Resident-CTA count used to size persistent grids: SMs x blocks per SM for the kernel.
 int persistent_grid(const void* kernel, int threads, size_t dyn_smem);
 

@@ -3,6 +3,7 @@
 #include <stdio.h>
 
 #include "spl.h"
+#include "spl_checked.h" /* declarations only: the reader is exported by the checked build */
 
 static int fails = 0;
 
@@ -45,6 +46,7 @@ int main(void) {
     expect(spl_flags_status(SPL_FLAG_COPY_PENDING) == SPL_ERR_TIMEOUT, "copy pending");
     expect(spl_status_string(SPL_ERR_BAD_PAYLOAD)[0] != 'u', "status string of a flag status");
     expect(spl_pack(0, 0, 0, 0, 0) == SPL_OK, "empty pack");
+    expect(SPL_DEBUG_WORDS == 16 && SPL_DEBUG_GENERIC < SPL_DEBUG_WORDS, "debug word layout");
     if (fails == 0) printf("ok\n");
     return fails != 0;
 }

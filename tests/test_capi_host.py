@@ -42,6 +42,20 @@ def test_library_exports_every_declared_symbol(lib):
     assert os.path.exists(lib_build.LIB_PATH)
 
 
+def test_checked_library_exports_the_same_calls_and_its_reader():
+    """The checked build (same sources, -DSPL_CHECKED=1) exports every call of spl.h and the
+    one call of spl_checked.h; the normal build does not export the reader."""
+    chk = ctypes.CDLL(lib_build.CHECKED_LIB_PATH)
+    for fn in declared_functions():
+        assert hasattr(chk, fn), f"{fn} missing from the checked build"
+    text = open(os.path.join(ROOT, "include", "spl_checked.h")).read()
+    assert "spl_debug_read" in re.findall(r"\b(spl_[a-z_]+)\s*\(", re.sub(r"/\*.*?\*/", "", text, flags=re.S))
+    assert hasattr(chk, "spl_debug_read")
+    assert not hasattr(ctypes.CDLL(lib_build.LIB_PATH), "spl_debug_read")
+    chk.spl_debug_read.argtypes, chk.spl_debug_read.restype = [ctypes.c_void_p, ctypes.c_int], ctypes.c_int
+    assert chk.spl_debug_read(None, 0) == INVALID
+
+
 def test_library_is_built_for_sm103a_only():
     assert any("arch=compute_103a,code=sm_103a" in f for f in lib_build.ARCH)
 

@@ -2,8 +2,8 @@
 
 Bar: payload bytes, indices, codes, scales and the error buffer bit-exact; the mean and theta
 within 1e-6 of max |reference| (and, with the fixed peer summation order, bit-exact where
-checked).  Small and medium cases compare every chunk; full workload sizes compare sampled
-chunks in the launch configuration the benchmark times.
+checked).  Small and medium cases compare every chunk here; the full workload sizes are in
+test_gpu_fullsize.py (every chunk as well).
 """
 import numpy as np
 import pytest
@@ -12,8 +12,7 @@ import torch
 import compressed_pseudo_gradient_gb300 as spl
 import oracle
 from compressed_pseudo_gradient_gb300 import synth
-from parity_util import (assert_bit_equal, assert_close, check_compress_sampled,
-                         check_decode_sampled, gather_chunks, host, sample_chunks)
+from parity_util import assert_bit_equal, assert_close, host
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -249,30 +248,6 @@ def test_heavy_tail_bf16_medium_all_chunks():
         compare_full_round(delta, ef, wl.beta, f"heavy tail medium round {r}")
 
 
-def test_heavy_tail_bf16_full_size_sampled():
-    wl = synth.WORKLOADS["heavy_tail_bf16"]
-    n = wl.n
-    C = spl.num_chunks(n)
-    gen = synth.generator(0, DEV)
-    ef = torch.zeros(n, device=DEV)
-    for r in range(wl.rounds):
-        delta = synth.delta_round(wl, gen, DEV)
-        ids = sample_chunks(C, 200, seed=r)
-        check_compress_sampled(lambda: gpu_round(delta, ef, wl.beta), delta, ef, wl.beta, ids,
-                               f"heavy tail round {r}")
-    payloads, scales = [], []
-    for p in range(wl.peers):
-        d = synth.delta_round(wl, synth.generator(1 + p, DEV), DEV)
-        e = torch.zeros(n, device=DEV)
-        pl, sc = gpu_round(d, e, wl.beta)
-        payloads.append(pl), scales.append(sc)
-        del d, e
-    mean = spl.decode_aggregate(payloads, scales, n)
-    torch.cuda.synchronize()
-    check_decode_sampled(payloads, scales, n, mean, None, None, 0.0, sample_chunks(C, 200, 99),
-                         "heavy tail P=8")
-
-
 # ---------------------------------------------------------------------------------------------
 # 72B-class decoder layer, chunked per tensor (multi-tensor launch)
 # ---------------------------------------------------------------------------------------------
@@ -316,84 +291,6 @@ def test_multi_tensor_matches_single_calls_and_splits_long_tables():
     assert_bit_equal(host(scales), np.concatenate([host(s) for _, s in singles]), "scales")
     for e, e2 in zip(efs, efs2):
         assert_bit_equal(host(e), host(e2), "error buffer")
-
-
-def test_decoder_layer_full_size_sampled():
-    wl = synth.WORKLOADS["decoder_layer"]
-    gen = synth.generator(0, DEV)
-    deltas = synth.decoder_layer_round(gen, DEV)
-    efs = [torch.zeros_like(d) for d in deltas]
-    for r in range(2):
-        snaps = []
-        chunk0 = 0
-        for i, d in enumerate(deltas):
-            C = spl.num_chunks(d.numel())
-            ids = sample_chunks(C, 24, seed=10 * r + i)
-            snaps.append((ids, chunk0, gather_chunks(d, ids, d.numel()),
-                          gather_chunks(efs[i], ids, d.numel())))
-            chunk0 += C
-        payload, scales = spl.ef_compress_multi(deltas, efs, wl.beta)
-        torch.cuda.synchronize()
-        pl, sc = host(payload), host(scales)
-        for i, (ids, c0, (d_body, d_tail, full_ids), (e_body, e_tail, _)) in enumerate(snaps):
-            n_i = deltas[i].numel()
-            assert d_tail is None or n_i % 4096
-            o_pl, o_sc, _ = oracle.ef_compress(d_body, e_body, wl.beta)
-            rows = [c0 + c for c in full_ids]
-            assert_bit_equal(pl[rows], o_pl, f"layer tensor {i}: payload")
-            assert_bit_equal(sc[rows], o_sc, f"layer tensor {i}: scales")
-            e_after, _, _ = gather_chunks(efs[i], ids, n_i)
-            assert_bit_equal(e_after, e_body, f"layer tensor {i}: error buffer")
-        deltas = synth.decoder_layer_round(gen, DEV)
-    # decode of the own payload (P = 1) for one tensor slice of the concatenated records
-    n_q = deltas[0].numel()
-    Cq = spl.num_chunks(n_q)
-    mean = spl.decode_aggregate([payload[:Cq]], [scales[:Cq]], n_q)
-    torch.cuda.synchronize()
-    check_decode_sampled([payload[:Cq]], [scales[:Cq]], n_q, mean, None, None, 0.0,
-                         sample_chunks(Cq, 64, 5), "layer q_proj decode")
-
-
-# ---------------------------------------------------------------------------------------------
-# Large flat workload (the benchmark's compress launch) and the 24-peer receive workload
-# ---------------------------------------------------------------------------------------------
-def test_large_flat_full_size_sampled():
-    wl = synth.WORKLOADS["large_flat"]
-    n = wl.n
-    C = spl.num_chunks(n)
-    gen = synth.generator(0, DEV)
-    ef = torch.zeros(n, device=DEV)
-    flags = torch.zeros(1, dtype=torch.int32, device=DEV)
-    for r in range(3):
-        delta = synth.delta_round(wl, gen, DEV)
-        check_compress_sampled(lambda: gpu_round(delta, ef, wl.beta, flags), delta, ef, wl.beta,
-                               sample_chunks(C, 256, seed=100 + r), f"large flat round {r}")
-        del delta
-    assert int(flags.item()) == 0
-
-
-def test_receive_24_peers_full_size_sampled():
-    wl = synth.WORKLOADS["receive"]
-    n = wl.n
-    C = spl.num_chunks(n)
-    payloads, scales = [], []
-    e = torch.empty(n, device=DEV)
-    for p in range(wl.peers):
-        d = synth.delta_round(wl, synth.generator(1 + p, DEV), DEV)
-        e.zero_()
-        pl, sc = gpu_round(d, e, wl.beta)
-        payloads.append(pl), scales.append(sc)
-        del d
-    del e
-    theta = synth.theta(n, synth.generator(0, DEV), DEV)
-    ids = sample_chunks(C, 256, seed=7)
-    t_body, t_tail, _ = gather_chunks(theta, ids, n)
-    flags = torch.zeros(1, dtype=torch.int32, device=DEV)
-    mean = spl.decode_aggregate(payloads, scales, n, theta=theta, lr=wl.lr, flags=flags)
-    torch.cuda.synchronize()
-    assert int(flags.item()) == 0
-    check_decode_sampled(payloads, scales, n, mean, (t_body, t_tail), theta, wl.lr, ids,
-                         "receive P=24")
 
 
 # ---------------------------------------------------------------------------------------------
