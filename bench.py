@@ -368,7 +368,7 @@ def run_offload(args, dev):
     return 0
 
 
-def setup_other_workload(name: str, dev):
+def setup_other_workload(name: str, dev, layer_scale: int = 1):
     """Buffers and one-round step of another workload, a fresh pseudo-gradient each round (the
     workload's round count of them, cycled).  heavy_tail_bf16: 2^27 bf16 compress + 8-peer mean;
     decoder_layer: the 72B-class layer's nine tensors compressed in one multi-tensor call;
@@ -382,7 +382,9 @@ def setup_other_workload(name: str, dev):
     wl = synth.WORKLOADS[name]
     R = wl.rounds
     if wl.name == "decoder_layer":
-        rounds = [synth.decoder_layer_round(synth.generator(1 + 1000 * r, dev), dev)
+        shapes = tuple((nm, (max(1, sh[0] // layer_scale),) + tuple(sh[1:]))
+                       for nm, sh in synth.DECODER_LAYER_SHAPES)
+        rounds = [synth.decoder_layer_round(synth.generator(1 + 1000 * r, dev), dev, shapes)
                   for r in range(R)]
         efs = [torch.zeros_like(d) for d in rounds[0]]
         sizes = [d.numel() for d in rounds[0]]
@@ -399,7 +401,8 @@ def setup_other_workload(name: str, dev):
                 ev[1].record()
                 ev[2].record()
             return 1
-        return step, {"name": wl.name, "n": sum(sizes), "chunks": C, "rounds": R, "peers": 0,
+        name = wl.name if layer_scale == 1 else f"{wl.name} (rows / {layer_scale})"
+        return step, {"name": name, "n": sum(sizes), "chunks": C, "rounds": R, "peers": 0,
                       "dtype": "f32", "comp_bytes": comp_bytes, "dec_bytes": 0,
                       "tensors": len(sizes)}
     n = wl.n
@@ -503,7 +506,7 @@ def run_other_workload(args, dev):
     plain calls and as CUDA graphs of each round replayed in turn; reports the faster."""
     import torch
 
-    step, info = setup_other_workload(args.workload, dev)
+    step, info = setup_other_workload(args.workload, dev, args.layer_scale)
     R = info["rounds"]
     step_bytes = info["comp_bytes"] + info["dec_bytes"]
     for k in range(args.warmup):
@@ -625,6 +628,93 @@ def run_codecs(args, dev):
             "config": {"workload": f"codec variants: receive step at {n} values, 24 peers",
                        "n": n, "peak_gbs": peak, "peak_kind": kind, "codecs": rows},
             "gpu_launches": launches}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_sharded(args, dev, rank, world):
+    """One peer's 2^30-value pseudo-gradient spread over the node's GPUs (chunk-sharded): each
+    rank compresses its slice, the ranks all-gather the records (the peer's whole payload on
+    every rank), and each rank decodes the 24 peers' records of its own chunk range into its
+    slice of the mean fused with the outer step.  Total work is fixed as N grows (strong
+    scaling); the value is the whole tensor's algorithmic bytes over the slowest rank's time."""
+    import torch
+    import compressed_pseudo_gradient_gb300 as spl
+    from compressed_pseudo_gradient_gb300 import sharded, synth
+
+    n = args.elements
+    C = (n + CHUNK - 1) // CHUNK
+    lo, hi = sharded.shard_range(n, world, rank)
+    m = hi - lo
+    base = rank_seed_base(0)
+    deltas = [synth.laplace(m, 1e-4, synth.generator(sd + 7 * rank, dev), dev)
+              for sd in round_seeds(base)]
+    ef = torch.zeros(m, dtype=torch.float32, device=dev)
+    pls, scs = [], []
+    tmp = torch.empty(m, dtype=torch.float32, device=dev)
+    for p in range(PEERS):   # the peers' records of this rank's chunk range
+        d = synth.laplace(m, 1e-4, synth.generator(base + 1 + p + 1000 * rank, dev), dev)
+        tmp.zero_()
+        a, b = spl.ef_compress(d, tmp, BETA)
+        pls.append(a)
+        scs.append(b)
+        del d
+    del tmp
+    theta = synth.theta(m, synth.generator(base + 5000 + rank, dev), dev)
+    mean = torch.empty(m, dtype=torch.float32, device=dev)
+    state = {"round": 0}
+
+    def step(ev=None):
+        if ev:
+            ev[0].record()
+        pl, sc = sharded.compress_shard(deltas[state["round"] % ROUNDS], ef, BETA)
+        state["round"] += 1
+        if ev:
+            ev[1].record()
+        full_pl, full_sc = sharded.gather_records(pl, sc, C)
+        if ev:
+            ev[2].record()
+        sharded.decode_shard(pls, scs, n, mean=mean, theta=theta, lr=LR)
+        if ev:
+            ev[3].record()
+        return full_pl
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    barrier(dev)
+    torch.cuda.synchronize(dev)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(smi_id(dev)) as clk:
+        start.record()
+        for k in range(args.steps):
+            step(evs[k])
+        end.record()
+        torch.cuda.synchronize(dev)
+    barrier(dev)
+    t_max = max_over_ranks(start.elapsed_time(end) / 1e3, dev)
+    if rank != 0:
+        return 0
+    step_bytes = compress_bytes(n, C) + decode_bytes(n, C, PEERS)
+    ms = [statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs) for i in range(3)]
+    peak, kind = read_peaks()
+    value = step_bytes / (t_max / args.steps) / 1e9
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * t_max / args.steps, 4), "higher_is_better": True,
+            "scaling": "strong", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"chunk-sharded: one {n}-value pseudo-gradient over {world} "
+                                   f"GPU(s): compress of each slice, all-gather of the records, "
+                                   f"decode of 24 peers' records of each rank's chunk range "
+                                   f"fused with the outer step",
+                       "n": n, "chunks": C, "peers": PEERS, "parallelism": f"chunk-sharded x{world}",
+                       "rank0_slice": [lo, hi],
+                       "rank0_ms": {"compress": round(ms[0], 4), "all_gather": round(ms[1], 4),
+                                    "decode": round(ms[2], 4)},
+                       "frac_of_hbm_per_gpu": round(value / world / peak, 4), "peak_kind": kind},
+            "clocks": clk.summary(), "gpu_launches": 2 * args.steps}
     print(json.dumps(line), flush=True)
     return 0
 
@@ -881,13 +971,16 @@ def main(argv=None):
                     help="skip the heavy-tailed bf16 and decoder-layer sub-records")
     ap.add_argument("--workload", default="receive",
                     choices=["receive", "heavy_tail_bf16", "decoder_layer", "tiny", "offload",
-                             "codecs"],
+                             "codecs", "sharded"],
                     help="receive (default): the headline step; the others time one round of "
                          "another workload on one GPU")
     ap.add_argument("--decode-stats", action="store_true",
                     help="also gather the per-peer statistics in the receive pass")
     ap.add_argument("--elements", type=int, default=N_ELEMS,
                     help="pseudo-gradient size; smaller than 2^30 only for profiling captures")
+    ap.add_argument("--layer-scale", type=int, default=1,
+                    help="decoder_layer only: divide every tensor's rows by this (a profiling "
+                         "case of the same shapes' row width and data)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -901,9 +994,12 @@ def main(argv=None):
     rank, world, local = dist_env()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if args.workload == "sharded":
+        dist_init("nccl")
+        return run_sharded(args, dev, rank, world)
     if args.workload != "receive":
         if world != 1:
-            raise SystemExit("--workload other than receive runs on one GPU")
+            raise SystemExit("--workload other than receive and sharded runs on one GPU")
         if args.workload == "offload":
             return run_offload(args, dev)
         if args.workload == "codecs":
