@@ -632,6 +632,48 @@ def run_codecs(args, dev):
     return 0
 
 
+def run_hbm_mix(args, dev):
+    """Context for the roofline: what plain streaming torch kernels reach on this GPU for the
+    two kernels' read/write mixes, on 2^30 fp32 values each, best of `steps` (CUDA events):
+    a copy (4 B read + 4 B written per value, the measured peak's own kernel), an add (8 + 4,
+    the compress's mix: delta and the error buffer in, the error buffer out) and frexp (4 + 8,
+    the decode's mix: theta in, the mean and theta out).  Not a codec step."""
+    import torch
+    n = args.elements
+    a = torch.rand(n, device=dev)
+    b = torch.rand(n, device=dev)
+    c = torch.empty(n, device=dev)
+    e = torch.empty(n, dtype=torch.int32, device=dev)
+    kernels = {"copy (read 4 B, write 4 B per value)": (lambda: c.copy_(a), 8 * n),
+               "add (read 8 B, write 4 B)": (lambda: torch.add(a, b, out=c), 12 * n),
+               "frexp (read 4 B, write 8 B)": (lambda: torch.frexp(a, out=(c, e)), 12 * n)}
+    peak, kind = read_peaks()
+    rows = {}
+    for name, (fn, nbytes) in kernels.items():
+        for _ in range(args.warmup):
+            fn()
+        best = float("inf")
+        for _ in range(args.steps):
+            s0 = torch.cuda.Event(enable_timing=True)
+            s1 = torch.cuda.Event(enable_timing=True)
+            s0.record()
+            fn()
+            s1.record()
+            torch.cuda.synchronize(dev)
+            best = min(best, s0.elapsed_time(s1) / 1e3)
+        gbs = nbytes / best / 1e9
+        rows[name] = {"ms": round(1e3 * best, 4), "GB/s": round(gbs, 1),
+                      "frac_of_hbm": round(gbs / peak, 4)}
+    line = {"metric": "HBM bandwidth of plain streaming kernels by read/write mix (context)",
+            "value": rows["add (read 8 B, write 4 B)"]["GB/s"], "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"hbm-mix: torch copy_, add and frexp on {n} fp32 values",
+                       "peak_gbs": peak, "peak_kind": kind, "kernels": rows}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_sharded(args, dev, rank, world):
     """One peer's 2^30-value pseudo-gradient spread over the node's GPUs (chunk-sharded): each
     rank compresses its slice, the ranks all-gather the records (the peer's whole payload on
@@ -971,7 +1013,7 @@ def main(argv=None):
                     help="skip the heavy-tailed bf16 and decoder-layer sub-records")
     ap.add_argument("--workload", default="receive",
                     choices=["receive", "heavy_tail_bf16", "decoder_layer", "tiny", "offload",
-                             "codecs", "sharded"],
+                             "codecs", "sharded", "hbm-mix"],
                     help="receive (default): the headline step; the others time one round of "
                          "another workload on one GPU")
     ap.add_argument("--decode-stats", action="store_true",
@@ -994,6 +1036,8 @@ def main(argv=None):
     rank, world, local = dist_env()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if args.workload == "hbm-mix":
+        return run_hbm_mix(args, dev)
     if args.workload == "sharded":
         dist_init("nccl")
         return run_sharded(args, dev, rank, world)

@@ -58,7 +58,9 @@ def _load():
     with _lock:
         if _lib is not None:
             return _lib
-        lib = ctypes.CDLL(build())
+        # SPL_ORACLE_LIB: load another build of this oracle instead (the mutation test runs the
+        # pins against deliberately broken copies of spl_oracle.c this way)
+        lib = ctypes.CDLL(os.environ.get("SPL_ORACLE_LIB") or build())
         vp, i64, f32, u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_uint32
         lib.orc_num_chunks.argtypes, lib.orc_num_chunks.restype = [i64], i64
         lib.orc_topk_select.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp]

@@ -216,6 +216,19 @@ def test_mean_abs_sums_in_index_order_not_rank_order():
     assert scales[0] == F32(0.375)
 
 
+def test_mean_abs_pairs_neighbours_in_index_order():
+    """Chosen |a| in index order 1, 2^-24, 2^-24, 1 + 2^-23.  Pairwise: 1 + 2^-24 rounds to 1
+    (a tie, to even) and 2^-24 + (1 + 2^-23) to 1 + 2^-22 (a tie, to even), so the sum is
+    2 + 2^-22 and s = 1/2 + 2^-24.  Any other order the summation might take (left to right,
+    rank order, the pairs shifted by one place) rounds the small terms away: s = 1/2."""
+    L, k = 16, 4
+    delta = np.zeros(L, np.float32)
+    delta[[0, 1, 2, 3]] = np.array([1.0, 2.0 ** -24, -(2.0 ** -24), 1.0 + 2.0 ** -23], np.float32)
+    ef = np.zeros(L, np.float32)
+    _, scales, _ = oracle.ef_compress(delta, ef, 1.0, codec=(L, k, MEAN))
+    assert scales[0] == F32(0.5 + 2.0 ** -24)
+
+
 def test_variant_tail_chunk_pads_lose_ties_and_are_not_stored():
     L, k = 2048, 32
     n = L + 5

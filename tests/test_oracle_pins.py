@@ -238,6 +238,26 @@ def test_tail_chunk_pads_lose_ties_and_are_not_stored():
     assert np.count_nonzero(mean[4096:]) == 10
 
 
+def test_tail_chunk_real_zeros_win_ties_against_pads():
+    """A tail chunk of 100 real values, only 10 of them nonzero: the 64 chosen are the 10
+    nonzero values and the real zeros at the lowest indices; the pads (zeros past n, with
+    larger indices) lose every tie to them."""
+    n = 4096 + 100
+    delta = np.zeros(n, np.float32)
+    nz = 4096 + np.array([3, 9, 17, 30, 44, 51, 66, 70, 88, 99])
+    delta[nz] = np.arange(1, 11, dtype=np.float32)
+    delta[:4096] = 1.0
+    ef = np.zeros(n, np.float32)
+    payload, scales, _ = oracle.ef_compress(delta, ef, 1.0)
+    idx, codes = oracle.unpack(payload)
+    zeros = [j for j in range(100) if j + 4096 not in set(nz.tolist())][:54]
+    assert idx[1].tolist() == sorted(zeros + (nz - 4096).tolist())
+    assert idx[1].max() < 100
+    s = F32(10.0) / F32(1.5)
+    assert scales[1] == s
+    assert all(ef[4096 + j] == -F32(0.5) * s for j in zeros)
+
+
 @pytest.mark.parametrize("beta", [1.0, 0.5])
 def test_ef_conservation_exact_betas(beta):
     """e_new = a off the chosen set and e_new = RN(a - q) on it, with a = RN(beta*e + delta)."""
