@@ -75,7 +75,8 @@ def test_host_error_buffer_and_streams_touch_nothing_out_of_bounds(checked):
 
 def test_receiver_cases_touch_nothing_out_of_bounds(checked):
     parity.test_pack_unpack_match_oracle()
-    parity.test_malformed_records_rejected_like_oracle()
+    parity.test_malformed_records_rejected_like_oracle(False)
+    parity.test_malformed_records_rejected_like_oracle(True)
     for P in (1, 5, 8, 24):
         parity.test_decode_without_validation_matches_oracle(P)
     parity.test_peer_stats_match_oracle()

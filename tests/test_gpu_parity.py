@@ -311,7 +311,8 @@ def test_pack_unpack_match_oracle():
     assert np.array_equal(host(g_codes), codes)
 
 
-def test_malformed_records_rejected_like_oracle():
+@pytest.mark.parametrize("with_theta", [False, True])
+def test_malformed_records_rejected_like_oracle(with_theta):
     n = 6 * 4096
     gen = synth.generator(31, DEV)
     pls, scs = [], []
@@ -329,12 +330,17 @@ def test_malformed_records_rejected_like_oracle():
     scs[2][4] = -1.0
     scs[0][5] = -0.0                          # -0.0 is a valid (zero) scale
     flags = torch.zeros(1, dtype=torch.int32, device=DEV)
+    theta = synth.theta(n, synth.generator(32, DEV), DEV) if with_theta else None
+    th_h = host(theta) if with_theta else None
     mean = spl.decode_aggregate([torch.from_numpy(p).to(DEV) for p in pls],
-                                [torch.from_numpy(s).to(DEV) for s in scs], n, flags=flags)
+                                [torch.from_numpy(s).to(DEV) for s in scs], n, flags=flags,
+                                theta=theta, lr=0.7)
     torch.cuda.synchronize()
-    o_mean, o_flags = oracle.decode_aggregate(pls, scs, n)
+    o_mean, o_flags = oracle.decode_aggregate(pls, scs, n, theta=th_h, lr=0.7)
     assert int(flags.item()) == o_flags == oracle.FLAG_BAD_RECORD
     assert_bit_equal(host(mean), o_mean, "mean with rejected records")
+    if with_theta:
+        assert_bit_equal(host(theta), th_h, "theta with rejected records")
 
 
 @pytest.mark.parametrize("P", [1, 5, 8, 24])
