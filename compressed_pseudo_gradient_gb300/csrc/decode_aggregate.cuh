@@ -84,7 +84,7 @@ constexpr int kLeanMaxPeers = 16;
 // Dynamic shared memory for P peers (offsets 16-byte aligned), G = min(P, group):
 //   bar[4] | theta stage [S][4096] f32 (with theta only) | record stage [S][P][112] (+16) |
 //   acc [4096] f32 |
-//   entries [G][64] (position, value) | validity [G] u32 |
+//   entries [G][64] (position, value) | validity [G] u32 (read with statistics only) |
 //   with statistics only: (scale, magnitude | sign << 8 bit counts) [G] | per-peer totals of
 //   this CTA: sum of squares and its Kahan compensation [2][P] f32 | rejected, big, negative
 //   [3][P] u32 | max scale [P] f32
@@ -285,15 +285,17 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
                     bits = __reduce_add_sync(0xffffffffu, bits);
                     if (ok && lane == 0) sgrp[g] = make_uint2(__float_as_uint(s), bits);
                 }
-                if (ok) {
-                    uint2* eg = ent + g * kTopK;
+                // a rejected record adds +0.0 at its own (in-chunk) positions: the accumulator
+                // starts at +0.0 and a correctly rounded sum is -0.0 only for (-0) + (-0), so it
+                // never holds -0.0, and x + (+0.0) is x for every value it can hold (a NaN
+                // there is already the canonical one); the adds need no per-peer branch
+                uint2* eg = ent + g * kTopK;
 #pragma unroll
-                    for (int m = 0; m < kPerLane; ++m)
-                        eg[lane + 32 * m] = make_uint2(ix[m], __float_as_uint(level_value(f[m] & 3u, s)));
-                } else {
-                    bad = true;
-                }
-                if (lane == 0) okp[g] = ok ? 1u : 0u;
+                for (int m = 0; m < kPerLane; ++m)
+                    eg[lane + 32 * m] = make_uint2(
+                        ix[m], ok ? __float_as_uint(level_value(f[m] & 3u, s)) : 0u);
+                bad = bad || !ok;
+                if (kStats && lane == 0) okp[g] = ok ? 1u : 0u;
             }
             const bool last = g0 + kGroup >= P;
             if (last) {
@@ -347,23 +349,18 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
                 uint2 en[kPerLane];
 #pragma unroll
                 for (int m = 0; m < kPerLane; ++m) en[m] = ent[lane + 32 * m];
-                uint32_t okn = okp[0];
                 for (int g = 0; g < gn; ++g) {
                     uint2 e[kPerLane];
 #pragma unroll
                     for (int m = 0; m < kPerLane; ++m) e[m] = en[m];
-                    const uint32_t ok = okn;
-                    if (g + 1 < gn) {
+                    // the next peer's entries (after the last peer: its own again, unused)
+                    const int gnext = g + 1 < gn ? g + 1 : g;
 #pragma unroll
-                        for (int m = 0; m < kPerLane; ++m) en[m] = ent[(g + 1) * kTopK + lane + 32 * m];
-                        okn = okp[g + 1];
-                    }
-                    if (ok != 0u) {
+                    for (int m = 0; m < kPerLane; ++m) en[m] = ent[gnext * kTopK + lane + 32 * m];
 #pragma unroll
-                        for (int m = 0; m < kPerLane; ++m)
-                            if (SPL_CHECK(e[m].x < static_cast<uint32_t>(kChunk), kSiteAcc, e[m].x))
-                                acc[e[m].x] = __fadd_rn(acc[e[m].x], __uint_as_float(e[m].y));
-                    }
+                    for (int m = 0; m < kPerLane; ++m)
+                        if (SPL_CHECK(e[m].x < static_cast<uint32_t>(kChunk), kSiteAcc, e[m].x))
+                            acc[e[m].x] = __fadd_rn(acc[e[m].x], __uint_as_float(e[m].y));
                     __syncwarp();
                 }
             }
