@@ -636,8 +636,10 @@ def run_hbm_mix(args, dev):
     """Context for the roofline: what plain streaming torch kernels reach on this GPU for the
     two kernels' read/write mixes, on 2^30 fp32 values each, best of `steps` (CUDA events):
     a copy (4 B read + 4 B written per value, the measured peak's own kernel), an add (8 + 4,
-    the compress's mix: delta and the error buffer in, the error buffer out) and frexp (4 + 8,
-    the decode's mix: theta in, the mean and theta out).  Not a codec step."""
+    the compress's mix: delta and the error buffer in, the error buffer out), frexp (4 + 8,
+    the decode's mix: theta in, the mean and theta out) and a fill (0 + 4, the mix of a
+    mean-only decode, whose few record bytes read are 6 % of what it writes at 8 peers).  Not a
+    codec step."""
     import torch
     n = args.elements
     a = torch.rand(n, device=dev)
@@ -646,7 +648,8 @@ def run_hbm_mix(args, dev):
     e = torch.empty(n, dtype=torch.int32, device=dev)
     kernels = {"copy (read 4 B, write 4 B per value)": (lambda: c.copy_(a), 8 * n),
                "add (read 8 B, write 4 B)": (lambda: torch.add(a, b, out=c), 12 * n),
-               "frexp (read 4 B, write 8 B)": (lambda: torch.frexp(a, out=(c, e)), 12 * n)}
+               "frexp (read 4 B, write 8 B)": (lambda: torch.frexp(a, out=(c, e)), 12 * n),
+               "fill (write 4 B)": (lambda: c.fill_(1.0), 4 * n)}
     peak, kind = read_peaks()
     rows = {}
     for name, (fn, nbytes) in kernels.items():
@@ -668,7 +671,7 @@ def run_hbm_mix(args, dev):
             "value": rows["add (read 8 B, write 4 B)"]["GB/s"], "unit": "GB/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
             "dtype": "f32", "data": "synthetic",
-            "config": {"workload": f"hbm-mix: torch copy_, add and frexp on {n} fp32 values",
+            "config": {"workload": f"hbm-mix: torch copy_, add, frexp and fill_ on {n} fp32 values",
                        "peak_gbs": peak, "peak_kind": kind, "kernels": rows}}
     print(json.dumps(line), flush=True)
     return 0

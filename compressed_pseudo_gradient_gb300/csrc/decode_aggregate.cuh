@@ -59,6 +59,7 @@ struct RecvShape {
     static constexpr int kTopK = Geo::kTopK;
     static_assert(!kLean || (kChunk == 4096 && kTopK <= 64), "lean receiver shape");
     static constexpr int kThreads = kLean ? 128 : (kChunk == 8192 ? 512 : (kChunk == 2048 ? 128 : 256));
+    static constexpr bool kIsLean = kLean;
     static constexpr int kStages = kLean ? 4 : 1;           // prefetch stages (<= 4 mbarriers)
     static constexpr int kWarps = kThreads / 32;
     static constexpr int kSlice = kChunk / kWarps;          // positions per warp
@@ -111,7 +112,10 @@ struct Layout {
 // theta bytes (a full chunk when the outer step is fused) and starts its bulk copy; the
 // record pieces (7 x 16 B per peer; 4-byte pieces for a variant whose records are not 16-byte
 // aligned) are spread over the threads, each of which arrives once its own copies have
-// landed.  Arrivals per phase: min(pieces, 256) + 1.
+// landed.  In the lean shape piece i comes from thread 32 + i (from warp 0 only past
+// kThreads - 32 pieces), so that warp 0 goes straight on to the ordered adds: 8-peer mean of
+// 2^27 values 0.0985 -> 0.0959 ms; the wide shape with theta measured 0.6 % slower that way.
+// Arrivals per phase: min(pieces, threads) + 1.
 template <class Geo, class S>
 __device__ __forceinline__ void prefetch(const DecodeTable& tab, int P, int64_t c, int64_t C,
                                          bool full, const float* theta, uint64_t* bar,
@@ -131,8 +135,9 @@ __device__ __forceinline__ void prefetch(const DecodeTable& tab, int P, int64_t 
         }
     }
     const int pieces = P * kPieces;
-    if (tid < pieces) {
-        for (int i = tid; i < pieces; i += kThreads) {
+    const int t = !S::kIsLean ? tid : (tid >= 32 ? tid - 32 : tid + kThreads - 32);   // first piece
+    if (t < pieces) {
+        for (int i = t; i < pieces; i += kThreads) {
             const int p = i / kPieces;
             const int w = i - p * kPieces;
             if (!SPL_CHECK(c < C && p < P, kSiteRecCopy, c)) continue;
