@@ -11,35 +11,34 @@
 //
 // Design (HBM-bound: 8 B read + 4 B written per fp32 value, 116 B written per chunk):
 //   - one 256-thread CTA per 4096-value chunk (L values for a variant; the figures below are
-//     the default codec's), grid-stride over chunks with a persistent grid
-//     (SMs x resident CTAs); while a chunk is worked on, the next chunk's error buffer and
-//     delta fly into a shared-memory stage as two 1-D bulk copies (TMA, no multicast, no
-//     cluster) completing on an mbarrier, whose wait is bounded in time;
+//     the default codec's), grid-stride over chunks with a persistent grid (SMs x resident
+//     CTAs, four per SM); while a chunk is worked on, the next chunk's error buffer and delta
+//     fly into a shared-memory stage as two 1-D bulk copies (TMA, no multicast, no cluster)
+//     completing on an mbarrier, whose wait is bounded in time;
 //   - each thread takes 16 values from the stage into registers (four 16-byte vectors at
 //     chunk offsets v*1024 + 4*tid), forms a = fma(beta, e, delta) and the 31-bit magnitude
-//     keys, and keeps them there for the whole chunk; the error buffer is written back once,
-//     from registers, with streaming stores;
+//     keys, and stores a to the error buffer at once, unchanged (plain stores: the lines stay
+//     in L2 for the read-back below); only the keys stay in registers;
 //   - the 64th-largest key: a shared-memory histogram of 2048 bins of 1/128 octave over the
-//     16 octaves below the chunk's largest key; warp 0 finds the bin holding the 64th key
-//     among the top 512 bins (a block-wide search over all 2048 runs only when those hold
-//     fewer than 64 keys); keys above that bin are marked chosen, and the bin's own keys are
-//     taken whole or, up to 64 of them, ranked by warp 0 (magnitude, then index); any other
-//     chunk (a non-finite value, the 64th key more than 16 octaves below the largest, more
-//     than 64 keys in its bin) takes an out-of-line radix select over key bits [30:20],
-//     [19:9] and [8:0] with ties to the lowest indices; the chosen positions end up in a
-//     4096-bit shared bitmap;
-//   - one warp turns the bitmap into per-word prefix counts, from which every thread that
-//     owns a chosen value knows its rank in ascending index order; it writes the value and
-//     its position to shared memory by rank, and every thread stores its error-buffer values
-//     unchanged; the last warp, at the top of the next iteration behind the barrier that
-//     already follows the owner step (overlapping the histogram), codes the 64 entries,
-//     writes their residuals over the stored values, assembles the 112-byte record (28
-//     words) and stores it as seven 16-byte vectors; five block barriers per chunk in all;
-//   - mean-abs scale (variant): the same, the last warp first forming the scale (pairwise sum
-//     in ascending index order, divided by k);
-//   - error buffer in host memory, and k = 128 under the max-abs rule: the owners code their
-//     values and form the residuals in registers instead (the host buffer then crosses the
-//     link once, in whole vectors; the packing warp's work stays short).
+//     16 octaves below the chunk's largest key (one unconditional atomic per key); warp 0
+//     finds the bin holding the 64th key among the top 512 bins (a block-wide search over all
+//     2048 runs only when those hold fewer than 64 keys); marking is branch-free: keys above
+//     that bin go into a 4096-bit chosen bitmap with predicated ORs, and the bin's own keys
+//     are taken whole or, up to 64 of them, recorded in a tie bitmap and a key buffer and
+//     ranked by warp 0 (magnitude, then index); any other chunk (a non-finite value, the 64th
+//     key more than 16 octaves below the largest, more than 64 keys in its bin) takes an
+//     out-of-line radix select over key bits [30:20], [19:9] and [8:0] with ties to the
+//     lowest indices;
+//   - the finish of a chunk overlaps the next chunk's select on warp groups: beside warp 0's
+//     bin search the gather group turns the previous chunk's bitmap into positions by rank and
+//     reads the chosen values back from the error buffer (cp.async, from L2); beside warp 0's
+//     ranking the packing group codes them, writes their residuals over the stored values and
+//     packs the record with shuffles (the mean-abs rule first forms the scale as a pairwise
+//     sum in ascending index order); four block barriers per chunk;
+//   - error buffer in host memory: only delta is staged, the buffer crosses the link once in
+//     whole vectors, and the owners of the chosen values code them and form the residuals in
+//     registers before that one store (k scattered writes per chunk over the link would cost
+//     more); five barriers per chunk.
 #pragma once
 
 #include <type_traits>
