@@ -17,16 +17,20 @@
 //     chunk is worked on, the next chunk's theta (one 16 KB bulk copy, TMA) and its P records
 //     (16-byte cp.async copies spread over the threads) fly into a shared-memory stage, all
 //     completing on one mbarrier; the next chunk's P scales travel as plain loads into
-//     registers (lane l of warp w holds peer 8 l + w's);
+//     registers (lane l of warp w holds peer 8 l + w's); a mean of a few peers without theta
+//     or statistics takes a lean shape instead (128 threads, four record stages, no theta
+//     stage, warp 0 free of copies);
 //   - each warp unpacks whole records (one peer at a time): the 64 14-bit fields, a check that
 //     the indices ascend strictly and the scale is finite and non-negative, and the decoded
-//     value of every entry, stored as (position, value) pairs (with statistics, the warp also
-//     counts the record's magnitude and sign bits and keeps them beside its scale);
+//     value of every entry, stored as (position, value) pairs (+0.0 for a rejected record, an
+//     exact identity in the adds; with statistics, the warp also counts the record's magnitude
+//     and sign bits and keeps them beside its scale);
 //   - then one warp adds the peers into a 16 KB shared accumulator in order p = 0..P-1, two
 //     entries per lane (distinct positions within a valid record), so every position is summed
 //     in fp32 in peer order from +0.0, as a plain sequential loop over peers would, with no
-//     atomics; a single warp keeps every lane busy and the instruction count minimal, while
-//     the other resident CTAs keep the SM fed (with statistics, the threads of the other warps
+//     atomics and no branch per peer; a single warp keeps every lane busy and the instruction
+//     count minimal, while
+//     the other resident CTAs keep the SM fed (with statistics, threads of warps 1-2
 //     meanwhile fold one record each into per-CTA per-peer totals, flushed with atomics at
 //     the end);
 //   - the dense pass divides by P (correctly rounded, with a precomputed reciprocal; one
