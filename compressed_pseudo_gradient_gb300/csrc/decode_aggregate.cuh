@@ -29,13 +29,12 @@
 //     entries per lane (distinct positions within a valid record), so every position is summed
 //     in fp32 in peer order from +0.0, as a plain sequential loop over peers would, with no
 //     atomics and no branch per peer; a single warp keeps every lane busy and the instruction
-//     count minimal, while
-//     the other resident CTAs keep the SM fed (with statistics, threads of warps 1-2
-//     meanwhile fold one record each into per-CTA per-peer totals, flushed with atomics at
-//     the end);
+//     count minimal, while the other resident CTAs keep the SM fed (with statistics, threads
+//     of warps 1-2 meanwhile fold one record each into per-CTA per-peer totals, flushed with
+//     atomics at the end);
 //   - the dense pass divides by P (correctly rounded, with a precomputed reciprocal; one
-//     multiply when P is a power of two, whose reciprocal is exact), stores
-//     the mean and the updated theta with streaming stores and clears the accumulator.  Peers
+//     multiply when P is a power of two, whose reciprocal is exact), stores the mean and the
+//     updated theta with streaming stores and clears the accumulator.  Peers
 //     are unpacked in groups of up to 64 (16 or 32 for k = 128), so shared memory stays
 //     bounded for any P.
 #pragma once
