@@ -2,7 +2,9 @@
 (the default and every variant), tensor size (1 value to a few chunks, ragged), delta type,
 beta (including negative and zero), peer count, the outer step on or off, statistics on or
 off, and malformed records.  Every output is compared bit for bit (statistics' sum of squares
-within 1e-6 relative)."""
+within 1e-6 relative).  SPL_SWEEP_CASES sets the number of cases (80 by default)."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -18,7 +20,7 @@ CODECS = [None, (4096, 64, 1), (4096, 32, 0), (4096, 32, 1), (4096, 128, 0), (40
           (2048, 32, 0), (2048, 32, 1), (8192, 128, 0), (8192, 128, 1)]
 
 
-@pytest.mark.parametrize("case", range(80))
+@pytest.mark.parametrize("case", range(int(os.environ.get("SPL_SWEEP_CASES", "80"))))
 def test_random_case_matches_oracle(case):
     rng = np.random.default_rng(1000 + case)
     codec = CODECS[case % len(CODECS)]
