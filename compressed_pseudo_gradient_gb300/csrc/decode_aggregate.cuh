@@ -56,7 +56,7 @@ namespace {
 // kLean (L = 4096, k <= 64, a few peers, no theta, no statistics): 128 threads, so 8 CTAs share
 // an SM, and four prefetch stages (chunks c + G .. c + 4G), cheap without a theta stage: the
 // 8-peer mean of 2^27 values goes from 63 % to 73 % of the measured copy bandwidth.
-template <class Geo, bool kLean = false>
+template <class Geo, bool kLean = false, bool kStats = false>
 struct RecvShape {
     static constexpr int kChunk = Geo::kChunk;
     static constexpr int kTopK = Geo::kTopK;
@@ -73,6 +73,12 @@ struct RecvShape {
     static constexpr int kPerLane = kTopK / 32;             // entries per lane of a record
     static constexpr int kPieceBytes = Geo::kVecRecords ? 16 : 4;
     static constexpr int kPieces = Geo::kRecordBytes / kPieceBytes;   // copies per record
+    // records of a multiple of 16 bytes as one bulk copy each, from the last warp (measured
+    // per shape: the 24-peer decode with theta 2.137 -> 2.086 ms, L = 8192 2.44 -> 2.33 ms;
+    // the lean shape, statistics and k = 128 at 256 threads measured 2-3 % slower that way
+    // and keep 16-byte cp.async pieces spread over the threads)
+    static constexpr bool kBulkRecords =
+        Geo::kVecRecords && !kLean && !kStats && (kTopK <= 64 || kThreads == 512);
     static constexpr int kMinBlocks = kThreads == 256 && kChunk > 4096 ? 2 : 1024 / kThreads;
     // scales a lane carries: peer (32 W) i + W lane + w in slot i, for up to 256 peers
     static constexpr int kScalesPerLane = (kMaxPeers + 32 * kWarps - 1) / (32 * kWarps);
@@ -111,8 +117,10 @@ struct Layout {
     }
 };
 
-// All threads: start chunk c's copies into one stage.  Thread 0 arrives with the expected
-// theta bytes (a full chunk when the outer step is fused) and starts its bulk copy; the
+// All threads: start chunk c's copies into one stage.  Where the shape takes records as bulk
+// copies (kBulkRecords), the last warp starts one per record and theta's, and its first lane
+// arrives with all their bytes (one arrival per phase).  Otherwise thread 0 arrives with the
+// expected theta bytes (a full chunk when the outer step is fused) and starts its bulk copy; the
 // record pieces (7 x 16 B per peer; 4-byte pieces for a variant whose records are not 16-byte
 // aligned) are spread over the threads, each of which arrives once its own copies have
 // landed.  In the lean shape piece i comes from thread 32 + i (from warp 0 only past
@@ -128,6 +136,25 @@ __device__ __forceinline__ void prefetch(const DecodeTable& tab, int P, int64_t 
     constexpr int kRecordBytes = Geo::kRecordBytes;
     constexpr int kPieces = S::kPieces;
     constexpr int kPieceBytes = S::kPieceBytes;
+    if constexpr (S::kBulkRecords) {
+        // one bulk copy per record, from the last warp, with theta's; one arrival with all
+        // the bytes
+        if (tid >= kThreads - 32) {
+            const int lane = tid - (kThreads - 32);
+            fence_async_smem();
+            if (lane == 0) {
+                const bool th = theta != nullptr && full;
+                mbar_expect_tx(bar, static_cast<uint32_t>(P * kRecordBytes) + (th ? kChunk * 4u : 0u));
+                if (th) bulk_load(st_theta, theta + c * kChunk, kChunk * 4, bar);
+            }
+            __syncwarp();
+            for (int p = lane; p < P; p += 32)
+                if (SPL_CHECK(c < C && p < P, kSiteRecCopy, c))
+                    bulk_load(st_rec + p * kRecordBytes, tab.payload[p] + c * kRecordBytes,
+                              kRecordBytes, bar);
+        }
+        return;
+    }
     if (tid == 0) {
         if (theta != nullptr && full) {
             fence_async_smem();
@@ -154,11 +181,11 @@ __device__ __forceinline__ void prefetch(const DecodeTable& tab, int P, int64_t 
 }
 
 template <class Geo, bool kLean, bool kStats, bool kPow2>
-__global__ void __launch_bounds__(RecvShape<Geo, kLean>::kThreads, RecvShape<Geo, kLean>::kMinBlocks)
+__global__ void __launch_bounds__(RecvShape<Geo, kLean, kStats>::kThreads, RecvShape<Geo, kLean, kStats>::kMinBlocks)
 k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __restrict__ mean,
                    float* __restrict__ theta_arg, float neg_lr, bool validate,
                    PeerStats* __restrict__ stats, uint32_t* __restrict__ flags) {
-    using S = RecvShape<Geo, kLean>;
+    using S = RecvShape<Geo, kLean, kStats>;
     constexpr int kStages = S::kStages;
     // the lean shape is launched without theta: knowing so here drops its code and registers
     float* __restrict__ const theta = kLean ? nullptr : theta_arg;
@@ -209,7 +236,8 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
         }
     }
     if (tid == 0) {
-        const uint32_t arrivals = static_cast<uint32_t>(min(P * S::kPieces, kThreads) + 1);
+        const uint32_t arrivals =
+            S::kBulkRecords ? 1u : static_cast<uint32_t>(min(P * S::kPieces, kThreads) + 1);
         for (int st = 0; st < kStages; ++st) mbar_init(&bars[st], arrivals);
     }
     __syncthreads();
@@ -455,7 +483,7 @@ template <class Geo, bool kLean, bool kStats, bool kPow2>
 cudaError_t launch_kernel(const DecodeTable& tab, int P, int64_t n, int64_t C, float* mean,
                           float* theta, float lr, bool validate, PeerStats* stats, uint32_t* flags,
                           cudaStream_t stream) {
-    using S = RecvShape<Geo, kLean>;
+    using S = RecvShape<Geo, kLean, kStats>;
     const size_t smem = Layout<Geo, S>(P, kStats, theta != nullptr).total;
     const void* kern = reinterpret_cast<const void*>(&k_decode_aggregate<Geo, kLean, kStats, kPow2>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
