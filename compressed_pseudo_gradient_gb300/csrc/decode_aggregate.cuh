@@ -75,8 +75,8 @@ struct RecvShape {
     static constexpr int kPieces = Geo::kRecordBytes / kPieceBytes;   // copies per record
     // records of a multiple of 16 bytes as one bulk copy each, from the last warp (measured
     // per shape: the 24-peer decode with theta 2.137 -> 2.086 ms, L = 8192 2.44 -> 2.33 ms;
-    // the lean shape, statistics and k = 128 at 256 threads measured 2-3 % slower that way
-    // and keep 16-byte cp.async pieces spread over the threads)
+    // the lean shape (3 %), k = 128 at 256 threads (3 %) and statistics (0.4 %) measured
+    // slower that way and keep 16-byte cp.async pieces spread over the threads)
     static constexpr bool kBulkRecords =
         Geo::kVecRecords && !kLean && !kStats && (kTopK <= 64 || kThreads == 512);
     static constexpr int kMinBlocks = kThreads == 256 && kChunk > 4096 ? 2 : 1024 / kThreads;
