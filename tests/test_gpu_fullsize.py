@@ -167,7 +167,8 @@ def test_decoder_layer_every_chunk():
 
 
 def test_receive_24_peers_every_value():
-    """24 peers' records of 2^30 values into the mean, fused with the outer step."""
+    """24 peers' records of 2^30 values into the mean, fused with the outer step; the same
+    decode through the checked build gives the same bytes with no failed memory check."""
     wl = synth.WORKLOADS["receive"]
     n = wl.n
     pls, scs = [], []
@@ -181,9 +182,15 @@ def test_receive_24_peers_every_value():
     del e
     theta = synth.theta(n, synth.generator(0, DEV), DEV)
     th_h = host(theta)
+    theta_chk = theta.clone()
     flags = torch.zeros(1, dtype=torch.int32, device=DEV)
     mean = spl.decode_aggregate(pls, scs, n, theta=theta, lr=wl.lr, flags=flags)
     torch.cuda.synchronize()
+    mean_chk, d = checked_paths(lambda: spl.decode_aggregate(pls, scs, n, theta=theta_chk,
+                                                             lr=wl.lr))
+    assert torch.equal(mean_chk.view(torch.int32), mean.view(torch.int32))
+    assert torch.equal(theta_chk.view(torch.int32), theta.view(torch.int32))
+    del mean_chk, theta_chk
     o_mean, o_flags = oracle_decode([host(p) for p in pls], [host(s) for s in scs], n,
                                     theta_h=th_h, lr=wl.lr)
     assert int(flags.item()) == o_flags == 0
