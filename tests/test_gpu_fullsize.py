@@ -133,7 +133,8 @@ def test_large_flat_every_chunk():
 
 
 def test_heavy_tail_bf16_every_chunk():
-    """2^27 bf16 heavy-tailed, beta 0.95, all five rounds, then the 8-peer mean."""
+    """2^27 bf16 heavy-tailed, beta 0.95, all five rounds, then the 8-peer mean (also through
+    the checked build)."""
     wl = synth.WORKLOADS["heavy_tail_bf16"]
     gen = synth.generator(0, DEV)
     ef = torch.zeros(wl.n, device=DEV)
@@ -148,6 +149,8 @@ def test_heavy_tail_bf16_every_chunk():
     flags = torch.zeros(1, dtype=torch.int32, device=DEV)
     mean = spl.decode_aggregate(pls, scs, wl.n, flags=flags)
     torch.cuda.synchronize()
+    mean_chk, _ = checked_paths(lambda: spl.decode_aggregate(pls, scs, wl.n))
+    assert torch.equal(mean_chk.view(torch.int32), mean.view(torch.int32))
     o_mean, o_flags = oracle_decode([host(p) for p in pls], [host(s) for s in scs], wl.n)
     assert int(flags.item()) == o_flags == 0
     assert_close(host(mean), o_mean, "heavy tail mean of 8")
