@@ -224,16 +224,24 @@ def test_variant_many_peers_span_several_groups(codec, P):
         scs.append((rng.random(C) * 1e-3).astype(np.float32))
     theta = synth.theta(n, synth.generator(P, DEV), DEV)
     th_h = host(theta).copy()
+    theta2 = theta.clone()
     flags = torch.zeros(1, dtype=torch.int32, device=DEV)
     stats = spl.new_peer_stats(P, DEV)
-    mean = spl.decode_aggregate([torch.from_numpy(p).to(DEV) for p in pls],
-                                [torch.from_numpy(s).to(DEV) for s in scs], n, theta=theta,
-                                lr=0.7, flags=flags, stats=stats, codec=codec)
+    d_pls = [torch.from_numpy(p).to(DEV) for p in pls]
+    d_scs = [torch.from_numpy(s).to(DEV) for s in scs]
+    mean = spl.decode_aggregate(d_pls, d_scs, n, theta=theta, lr=0.7, flags=flags, stats=stats,
+                                codec=codec)
+    # and without statistics (another receiver shape: bulk-copied records where they are
+    # 16-byte multiples)
+    flags2 = torch.zeros(1, dtype=torch.int32, device=DEV)
+    mean2 = spl.decode_aggregate(d_pls, d_scs, n, theta=theta2, lr=0.7, flags=flags2, codec=codec)
     torch.cuda.synchronize()
     o_mean, o_flags = oracle.decode_aggregate(pls, scs, n, theta=th_h, lr=0.7, codec=codec)
-    assert int(flags.item()) == o_flags == oracle.FLAG_BAD_RECORD
+    assert int(flags.item()) == int(flags2.item()) == o_flags == oracle.FLAG_BAD_RECORD
     assert_bit_equal(host(mean), o_mean, f"{codec} P={P}: mean")
     assert_bit_equal(host(theta), th_h, f"{codec} P={P}: theta")
+    assert_bit_equal(host(mean2), o_mean, f"{codec} P={P}: mean without statistics")
+    assert_bit_equal(host(theta2), th_h, f"{codec} P={P}: theta without statistics")
     got = spl.read_peer_stats(stats)
     ref = oracle.peer_stats(pls, scs, n, codec=codec)
     for key in ("rejected", "big", "negative"):
