@@ -67,9 +67,15 @@ struct RecvShape {
     static constexpr int kWarps = kThreads / 32;
     static constexpr int kSlice = kChunk / kWarps;          // positions per warp
     static constexpr int kVec = kSlice / 128;               // vectors of 4 per thread
-    // peers unpacked per pass: with k = 128, 16 at 256 threads keeps the entries at 16 KB, so
-    // four CTAs fit an SM; a multiple of the warp count (peer p is unpacked by warp p mod W)
-    static constexpr int kGroup = kTopK <= 64 ? 64 : (kThreads == 256 ? 16 : 32);
+    // entries: (position, value) pairs of 8 bytes; for k = 128 at 256 threads the raw 2-byte
+    // fields, decoded by the adding warp with the peer's scale, so that 64 peers' entries fit
+    // 16 KB and one pass takes them all (2.85 -> 2.71 ms for the 24-peer decode; the k <= 64
+    // decode measured 1.3 % slower that way, L = 8192 at 512 threads 3.5 %)
+    static constexpr bool kFieldEntries = kTopK > 64 && kThreads == 256;
+    static constexpr int kEntryBytes = kFieldEntries ? 2 : 8;
+    // peers unpacked per pass, a multiple of the warp count (peer p is unpacked by warp p mod
+    // W): 32 for 8-byte entries of k = 128, so the entries stay at 32 KB
+    static constexpr int kGroup = kTopK <= 64 || kFieldEntries ? 64 : 32;
     static constexpr int kPerLane = kTopK / 32;             // entries per lane of a record
     static constexpr int kPieceBytes = Geo::kVecRecords ? 16 : 4;
     static constexpr int kPieces = Geo::kRecordBytes / kPieceBytes;   // copies per record
@@ -93,14 +99,14 @@ constexpr int kLeanMaxPeers = 16;
 
 // Dynamic shared memory for P peers (offsets 16-byte aligned), G = min(P, group):
 //   bar[4] | theta stage [S][4096] f32 (with theta only) | record stage [S][P][112] (+16) |
-//   acc [4096] f32 |
-//   entries [G][64] (position, value) | validity [G] u32 (read with statistics only) |
+//   acc [4096] f32 | entries [G][k] (position, value), or for k > 64 raw fields [G][k] u16
+//   and the peers' scales [G] f32 | validity [G] u32 (read with statistics only) |
 //   with statistics only: (scale, magnitude | sign << 8 bit counts) [G] | per-peer totals of
 //   this CTA: sum of squares and its Kahan compensation [2][P] f32 | rejected, big, negative
 //   [3][P] u32 | max scale [P] f32
 template <class Geo, class S>
 struct Layout {
-    size_t bar, theta, rec, acc, ent, ok, sgrp, st_sq, st_cnt, st_max, total;
+    size_t bar, theta, rec, acc, ent, scl, ok, sgrp, st_sq, st_cnt, st_max, total;
     __host__ __device__ Layout(int P, bool stats, bool with_theta) {
         const size_t G = static_cast<size_t>(P < S::kGroup ? P : S::kGroup);
         bar = 0;
@@ -108,7 +114,8 @@ struct Layout {
         rec = theta + (with_theta ? S::kStages * S::kChunk * 4 : 0);
         acc = rec + align16(S::kStages * static_cast<size_t>(P) * Geo::kRecordBytes) + 16;
         ent = acc + S::kChunk * 4;
-        ok = ent + G * S::kTopK * 8;
+        scl = ent + align16(G * S::kTopK * S::kEntryBytes);
+        ok = scl + (S::kFieldEntries ? align16(G * 4) : 0);
         sgrp = ok + align16(G * 4);
         st_sq = sgrp + align16(G * 8);
         st_cnt = st_sq + align16(static_cast<size_t>(P) * 8);
@@ -205,6 +212,8 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
     uint8_t* st_rec = smem_raw + L.rec;
     float* acc = reinterpret_cast<float*>(smem_raw + L.acc);
     uint2* ent = reinterpret_cast<uint2*>(smem_raw + L.ent);
+    uint16_t* ent16 = reinterpret_cast<uint16_t*>(smem_raw + L.ent);   // k > 64: raw fields
+    float* scl = reinterpret_cast<float*>(smem_raw + L.scl);         // k > 64: 0 if rejected
     uint32_t* okp = reinterpret_cast<uint32_t*>(smem_raw + L.ok);
     uint2* sgrp = reinterpret_cast<uint2*>(smem_raw + L.sgrp);
     float* st_sum = reinterpret_cast<float*>(smem_raw + L.st_sq);        // [P]
@@ -325,11 +334,18 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
                 // starts at +0.0 and a correctly rounded sum is -0.0 only for (-0) + (-0), so it
                 // never holds -0.0, and x + (+0.0) is x for every value it can hold (a NaN
                 // there is already the canonical one); the adds need no per-peer branch
-                uint2* eg = ent + g * kTopK;
+                if constexpr (S::kFieldEntries) {   // the fields, and the scale they decode with
+                    uint16_t* eg = ent16 + g * kTopK;
 #pragma unroll
-                for (int m = 0; m < kPerLane; ++m)
-                    eg[lane + 32 * m] = make_uint2(
-                        ix[m], ok ? __float_as_uint(level_value(f[m] & 3u, s)) : 0u);
+                    for (int m = 0; m < kPerLane; ++m) eg[lane + 32 * m] = static_cast<uint16_t>(f[m]);
+                    if (lane == 0) scl[g] = ok ? s : 0.0f;   // +-0.0 values: as above
+                } else {
+                    uint2* eg = ent + g * kTopK;
+#pragma unroll
+                    for (int m = 0; m < kPerLane; ++m)
+                        eg[lane + 32 * m] = make_uint2(
+                            ix[m], ok ? __float_as_uint(level_value(f[m] & 3u, s)) : 0u);
+                }
                 bad = bad || !ok;
                 if (kStats && lane == 0) okp[g] = ok ? 1u : 0u;
             }
@@ -381,7 +397,33 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
                 }
             }
             // ---- one warp: add the peers in order, k/32 entries per lane ------------------
-            if (warp == 0) {
+            if (S::kFieldEntries && warp == 0) {
+                uint32_t fn[kPerLane];
+#pragma unroll
+                for (int m = 0; m < kPerLane; ++m) fn[m] = ent16[lane + 32 * m];
+                float sn = scl[0];
+                for (int g = 0; g < gn; ++g) {
+                    uint32_t fe[kPerLane];
+#pragma unroll
+                    for (int m = 0; m < kPerLane; ++m) fe[m] = fn[m];
+                    const float s = sn;
+                    const int gnext = g + 1 < gn ? g + 1 : g;
+#pragma unroll
+                    for (int m = 0; m < kPerLane; ++m) fn[m] = ent16[gnext * kTopK + lane + 32 * m];
+                    sn = scl[gnext];
+                    // level_value, with the peer's two magnitudes formed once
+                    const uint32_t lo = __float_as_uint(__fmul_rn(0.5f, s));
+                    const uint32_t hi = __float_as_uint(__fmul_rn(1.5f, s));
+#pragma unroll
+                    for (int m = 0; m < kPerLane; ++m) {
+                        const uint32_t pos = fe[m] >> 2;
+                        const float v = __uint_as_float(((fe[m] & 1u) ? hi : lo) ^ ((fe[m] & 2u) << 30));
+                        if (SPL_CHECK(pos < static_cast<uint32_t>(kChunk), kSiteAcc, pos))
+                            acc[pos] = __fadd_rn(acc[pos], v);
+                    }
+                    __syncwarp();
+                }
+            } else if (warp == 0) {
                 uint2 en[kPerLane];
 #pragma unroll
                 for (int m = 0; m < kPerLane; ++m) en[m] = ent[lane + 32 * m];
