@@ -15,28 +15,30 @@
 // written when the outer step is fused):
 //   - one 256-thread CTA per chunk, grid-stride over chunks with a persistent grid; while a
 //     chunk is worked on, the next chunk's theta (one 16 KB bulk copy, TMA) and its P records
-//     (16-byte cp.async copies spread over the threads) fly into a shared-memory stage, all
-//     completing on one mbarrier; the next chunk's P scales travel as plain loads into
-//     registers (lane l of warp w holds peer 8 l + w's); a mean of a few peers without theta
-//     or statistics takes a lean shape instead (128 threads, four record stages, no theta
-//     stage, warp 0 free of copies);
+//     (one bulk copy each where the shape allows, else 16-byte cp.async pieces spread over the
+//     threads) fly into a shared-memory stage, all completing on one mbarrier; the next
+//     chunk's P scales travel as plain loads into registers (lane l of warp w holds peer
+//     8 l + w's); a mean of a few peers without theta or statistics takes a lean shape
+//     instead (128 threads, four record stages, no theta stage, warp 0 free of copies);
 //   - each warp unpacks whole records (one peer at a time): the 64 14-bit fields, a check that
 //     the indices ascend strictly and the scale is finite and non-negative, and the decoded
 //     value of every entry, stored as (position, value) pairs (+0.0 for a rejected record, an
 //     exact identity in the adds; with statistics, the warp also counts the record's magnitude
 //     and sign bits and keeps them beside its scale);
 //   - then one warp adds the peers into a 16 KB shared accumulator in order p = 0..P-1, two
-//     entries per lane (distinct positions within a valid record), so every position is summed
-//     in fp32 in peer order from +0.0, as a plain sequential loop over peers would, with no
-//     atomics and no branch per peer; a single warp keeps every lane busy and the instruction
+//     entries per lane (distinct positions within a valid record, so a lane reads both sums
+//     before writing either back: one shared-memory round trip per peer), so every position
+//     is summed in fp32 in peer order from +0.0, as a plain sequential loop over peers would,
+//     with no atomics and no branch per peer; a single warp keeps every lane busy and the instruction
 //     count minimal, while the other resident CTAs keep the SM fed (with statistics, threads
 //     of warps 1-2 meanwhile fold one record each into per-CTA per-peer totals, flushed with
 //     atomics at the end);
 //   - the dense pass divides by P (correctly rounded, with a precomputed reciprocal; one
 //     multiply when P is a power of two, whose reciprocal is exact), stores the mean and the
 //     updated theta with streaming stores and clears the accumulator.  Peers
-//     are unpacked in groups of up to 64 (16 or 32 for k = 128), so shared memory stays
-//     bounded for any P.
+//     are unpacked in groups of up to 64 (32 for k = 128 at L = 8192; at L = 4096 the k = 128
+//     entries are the raw 2-byte fields and a per-peer scale), so shared memory stays bounded
+//     for any P.
 #pragma once
 
 #include <cfloat>
@@ -414,12 +416,21 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
                     // level_value, with the peer's two magnitudes formed once
                     const uint32_t lo = __float_as_uint(__fmul_rn(0.5f, s));
                     const uint32_t hi = __float_as_uint(__fmul_rn(1.5f, s));
+                    // an accepted record's positions are distinct and a rejected one adds
+                    // +0.0, so a lane's k/32 sums may be read before any of them is written
+                    // back: one shared-memory round trip per peer instead of k/32
+                    float a[kPerLane];
+#pragma unroll
+                    for (int m = 0; m < kPerLane; ++m) {
+                        const uint32_t pos = fe[m] >> 2;
+                        a[m] = SPL_CHECK(pos < static_cast<uint32_t>(kChunk), kSiteAcc, pos) ? acc[pos] : 0.0f;
+                    }
 #pragma unroll
                     for (int m = 0; m < kPerLane; ++m) {
                         const uint32_t pos = fe[m] >> 2;
                         const float v = __uint_as_float(((fe[m] & 1u) ? hi : lo) ^ ((fe[m] & 2u) << 30));
                         if (SPL_CHECK(pos < static_cast<uint32_t>(kChunk), kSiteAcc, pos))
-                            acc[pos] = __fadd_rn(acc[pos], v);
+                            acc[pos] = __fadd_rn(a[m], v);
                     }
                     __syncwarp();
                 }
@@ -435,10 +446,16 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
                     const int gnext = g + 1 < gn ? g + 1 : g;
 #pragma unroll
                     for (int m = 0; m < kPerLane; ++m) en[m] = ent[gnext * kTopK + lane + 32 * m];
+                    // the lane's sums are all read before any is written back (see above)
+                    float a[kPerLane];
+#pragma unroll
+                    for (int m = 0; m < kPerLane; ++m)
+                        a[m] = SPL_CHECK(e[m].x < static_cast<uint32_t>(kChunk), kSiteAcc, e[m].x)
+                                   ? acc[e[m].x] : 0.0f;
 #pragma unroll
                     for (int m = 0; m < kPerLane; ++m)
                         if (SPL_CHECK(e[m].x < static_cast<uint32_t>(kChunk), kSiteAcc, e[m].x))
-                            acc[e[m].x] = __fadd_rn(acc[e[m].x], __uint_as_float(e[m].y));
+                            acc[e[m].x] = __fadd_rn(a[m], __uint_as_float(e[m].y));
                     __syncwarp();
                 }
             }
