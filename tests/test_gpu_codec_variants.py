@@ -206,8 +206,8 @@ def test_variant_host_error_buffer_rejected():
 @pytest.mark.parametrize("codec", [(L, k, MAX) for (L, k) in GEOMETRIES])
 @pytest.mark.parametrize("P", [24, 70, 200])
 def test_variant_many_peers_span_several_groups(codec, P):
-    """Peers are unpacked in groups (16 or 32 for k = 128, 64 otherwise); 24, 70 and 200 peers
-    span one to thirteen groups, and 200 peers need the second scale slot of a lane where a
+    """Peers are unpacked in groups (32 for k = 128 at L = 8192, 64 otherwise); 24, 70 and 200
+    peers span one to seven groups, and 200 peers need the second scale slot of a lane where a
     CTA has four warps (L = 2048)."""
     L, k, _ = codec
     n = 5 * L + 9
