@@ -157,6 +157,8 @@ def test_variant_malformed_records_rejected_like_oracle(codec):
     idx, codes = oracle.unpack(pls[1], codec)
     idx[0, [k - 3, k - 2]] = idx[0, [k - 2, k - 3]]   # chunk 0: not ascending near the end
     idx[2, 20] = idx[2, 19]                            # chunk 2: duplicate
+    # chunk 3: duplicate; for k > 32 the two entries one lane of the adding warp holds
+    idx[3, k - 1] = idx[3, k - 33 if k > 32 else k - 2]
     pls[1] = oracle.pack(idx, codes, codec)
     scs[2][1] = np.nan
     scs[2][4] = -1.0
@@ -171,7 +173,7 @@ def test_variant_malformed_records_rejected_like_oracle(codec):
     assert_bit_equal(host(mean), o_mean, f"{codec}: mean with rejected records")
     got = spl.read_peer_stats(stats)
     assert list(got["rejected"]) == list(oracle.peer_stats(pls, scs, n, codec=codec)["rejected"])
-    assert list(got["rejected"]) == [0, 2, 2]
+    assert list(got["rejected"]) == [0, 3, 2]
 
 
 def test_variant_multi_tensor_matches_single_calls():

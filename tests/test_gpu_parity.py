@@ -324,6 +324,7 @@ def test_malformed_records_rejected_like_oracle(with_theta):
     idx[0, [3, 4]] = idx[0, [4, 3]]           # chunk 0: not ascending
     idx[2, 40] = idx[2, 39]                   # chunk 2: duplicate
     idx[5, 63] = idx[5, 0]                    # chunk 5: wraps
+    idx[3, 33] = idx[3, 1]                    # chunk 3: entries one adding lane holds both
     pls[1] = oracle.pack(idx, codes)
     scs[2][1] = np.nan                        # chunk 1 of peer 2
     scs[2][3] = np.inf
