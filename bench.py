@@ -140,11 +140,12 @@ def read_peaks():
 
 
 def kernel_source_hash(name: str) -> str:
-    """Hash of a kernel's code: its launch unit, its template header and the device helpers,
-    with // comments and blank lines left out (a comment edit does not change the kernel)."""
+    """Hash of a kernel's code: its launch unit, its template header, the device helpers and
+    the launch constants, with // comments and blank lines left out (a comment edit does not
+    change the kernel)."""
     src = os.path.join(ROOT, "compressed_pseudo_gradient_gb300", "csrc")
     h = hashlib.sha256()
-    for f in (f"{name}.cu", f"{name}.cuh", "spl_device.cuh"):
+    for f in (f"{name}.cu", f"{name}.cuh", "spl_device.cuh", "spl_kernels.h"):
         with open(os.path.join(src, f)) as fh:
             for line in fh:
                 code = line.split("//", 1)[0].rstrip()
@@ -638,24 +639,36 @@ def run_hbm_mix(args, dev):
     a copy (4 B read + 4 B written per value, the measured peak's own kernel), an add (8 + 4,
     the compress's mix: delta and the error buffer in, the error buffer out), frexp (4 + 8,
     the decode's mix: theta in, the mean and theta out) and a fill (0 + 4, the mix of a
-    mean-only decode, whose few record bytes read are 6 % of what it writes at 8 peers).  Not a
-    codec step."""
+    mean-only decode, whose few record bytes read are 6 % of what it writes at 8 peers); and the
+    library's data-movement reference kernels (spl_calib.h), which move each codec kernel's
+    bytes the way that kernel does (bulk copies into a stage, its stores, its CTA shape) with
+    none of its arithmetic.  Not a codec step."""
     import torch
+    import compressed_pseudo_gradient_gb300 as spl
     n = args.elements
     a = torch.rand(n, device=dev)
     b = torch.rand(n, device=dev)
     c = torch.empty(n, device=dev)
+    d = torch.empty(n, device=dev)
     e = torch.empty(n, dtype=torch.int32, device=dev)
     kernels = {"copy (read 4 B, write 4 B per value)": (lambda: c.copy_(a), 8 * n),
                "add (read 8 B, write 4 B)": (lambda: torch.add(a, b, out=c), 12 * n),
                "frexp (read 4 B, write 8 B)": (lambda: torch.frexp(a, out=(c, e)), 12 * n),
                "fill (write 4 B)": (lambda: c.fill_(1.0), 4 * n)}
+    if n % CHUNK == 0:
+        for order, pers in (("codec order", False), ("one persistent wave", True)):
+            kernels[f"the sender's movement (e and delta staged by bulk copies, plain stores), "
+                    f"{order}"] = (lambda pers=pers: spl.calib_moves(
+                        spl.CALIB_SENDER_MOVES, a, b, out0=c, persistent=pers), 12 * n)
+            kernels[f"the receiver's movement (theta staged, mean and theta streamed), "
+                    f"{order}"] = (lambda pers=pers: spl.calib_moves(
+                        spl.CALIB_RECEIVER_MOVES, a, out0=c, out1=d, persistent=pers), 12 * n)
     peak, kind = read_peaks()
     rows = {}
     for name, (fn, nbytes) in kernels.items():
         for _ in range(args.warmup):
             fn()
-        best = float("inf")
+        times = []
         for _ in range(args.steps):
             s0 = torch.cuda.Event(enable_timing=True)
             s1 = torch.cuda.Event(enable_timing=True)
@@ -663,15 +676,18 @@ def run_hbm_mix(args, dev):
             fn()
             s1.record()
             torch.cuda.synchronize(dev)
-            best = min(best, s0.elapsed_time(s1) / 1e3)
+            times.append(s0.elapsed_time(s1) / 1e3)
+        best = min(times)
         gbs = nbytes / best / 1e9
         rows[name] = {"ms": round(1e3 * best, 4), "GB/s": round(gbs, 1),
-                      "frac_of_hbm": round(gbs / peak, 4)}
+                      "frac_of_hbm": round(gbs / peak, 4),
+                      "mean_ms": round(1e3 * sum(times) / len(times), 4)}
     line = {"metric": "HBM bandwidth of plain streaming kernels by read/write mix (context)",
             "value": rows["add (read 8 B, write 4 B)"]["GB/s"], "unit": "GB/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
             "dtype": "f32", "data": "synthetic",
-            "config": {"workload": f"hbm-mix: torch copy_, add, frexp and fill_ on {n} fp32 values",
+            "config": {"workload": f"hbm-mix: torch copy_, add, frexp and fill_, and the codec "
+                                   f"kernels' data movement alone, on {n} fp32 values",
                        "peak_gbs": peak, "peak_kind": kind, "kernels": rows}}
     print(json.dumps(line), flush=True)
     return 0

@@ -13,6 +13,8 @@ Doesn't Break Convergence".
 from __future__ import annotations
 
 from ._binding import (  # noqa: F401
+    CALIB_RECEIVER_MOVES,
+    CALIB_SENDER_MOVES,
     CHUNK,
     FLAG_BAD_RECORD,
     FLAG_COPY_PENDING,
@@ -24,6 +26,7 @@ from ._binding import (  # noqa: F401
     SCALE_MEAN_ABS,
     TOPK,
     SplError,
+    calib_moves,
     checked_library_path,
     debug_words,
     decode_aggregate,

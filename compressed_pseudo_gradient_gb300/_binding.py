@@ -118,6 +118,8 @@ def library():
         lib.spl_decode_aggregate_codec.restype = ci
         lib.spl_pack.argtypes, lib.spl_pack.restype = [vp, vp, sz, vp, vp], ci
         lib.spl_unpack.argtypes, lib.spl_unpack.restype = [vp, sz, vp, vp, vp], ci
+        lib.spl_calib_moves.argtypes = [ci, ci, vp, vp, vp, vp, sz, vp, vp]
+        lib.spl_calib_moves.restype = ci
         if hasattr(lib, "spl_debug_read"):   # the checked build
             lib.spl_debug_read.argtypes, lib.spl_debug_read.restype = [vp, ci], ci
         _lib = lib
@@ -415,3 +417,45 @@ def unpack(payload: torch.Tensor, *, idx=None, codes=None):
         st = lib.spl_unpack(payload.data_ptr(), C, idx.data_ptr(), codes.data_ptr(), _stream(dev))
     _check("spl_unpack", st)
     return idx, codes
+
+
+CALIB_SENDER_MOVES = 0
+CALIB_RECEIVER_MOVES = 1
+
+
+def calib_moves(pattern: int, in0: torch.Tensor, in1=None, *, out0=None, out1=None, flags=None,
+                persistent: bool = False):
+    """Data-movement reference kernels (include/spl_calib.h), for roofline calibration, not the
+    codec: CALIB_SENDER_MOVES moves the sender's bytes (out0 = in0 + in1, in0 and in1 staged
+    by bulk copies, plain stores); CALIB_RECEIVER_MOVES the receiver's (out0 = -in0,
+    out1 = in0, in0 staged, streaming stores).  Chunks in the codec kernels' order, or with
+    persistent=True in one persistent wave.  fp32 CUDA tensors, numel a multiple of 4096.
+    Returns out0 (sender) or (out0, out1) (receiver)."""
+    lib = library()
+    sender = pattern == CALIB_SENDER_MOVES
+    if not sender and pattern != CALIB_RECEIVER_MOVES:
+        raise ValueError(f"unknown calibration pattern {pattern}")
+    _cuda(in0, "in0", (torch.float32,))
+    dev, n = in0.device, in0.numel()
+    if sender:
+        if in1 is None:
+            raise ValueError("the sender pattern takes in1")
+        _cuda(in1, "in1", (torch.float32,))
+        if in1.numel() != n or in1.device != dev:
+            raise ValueError("in1 must match in0")
+    if out0 is None:
+        out0 = torch.empty_like(in0)
+    if not sender and out1 is None:
+        out1 = torch.empty_like(in0)
+    for t, name in ((out0, "out0"), (out1, "out1")):
+        if t is not None:
+            _cuda(t, name, (torch.float32,))
+            if t.numel() != n or t.device != dev:
+                raise ValueError(f"{name} must match in0")
+    with torch.cuda.device(dev):
+        st = lib.spl_calib_moves(pattern, int(bool(persistent)), in0.data_ptr(),
+                                 in1.data_ptr() if sender else None,
+                                 out0.data_ptr(), None if sender else out1.data_ptr(), n,
+                                 _flags_ptr(flags, dev), _stream(dev))
+    _check("spl_calib_moves", st)
+    return out0 if sender else (out0, out1)

@@ -13,13 +13,15 @@
 //
 // Design (HBM-bound: P x 116 B read per chunk, 16 KB of mean written, 32 KB of theta read and
 // written when the outer step is fused):
-//   - one 256-thread CTA per chunk, grid-stride over chunks with a persistent grid; while a
-//     chunk is worked on, the next chunk's theta (one 16 KB bulk copy, TMA) and its P records
-//     (one bulk copy each where the shape allows, else 16-byte cp.async pieces spread over the
-//     threads) fly into a shared-memory stage, all completing on one mbarrier; the next
-//     chunk's P scales travel as plain loads into registers (lane l of warp w holds peer
-//     8 l + w's); a mean of a few peers without theta or statistics takes a lean shape
-//     instead (128 threads, four record stages, no theta stage, warp 0 free of copies);
+//   - one 256-thread CTA per chunk at a time; the grid runs in waves of the resident CTAs,
+//     each CTA taking 32 chunks spaced a wave apart, so the chunks in flight stay close
+//     together in memory; while a chunk is worked on, the next chunk's theta (one 16 KB bulk
+//     copy, TMA) and its P records (one bulk copy each where the shape allows, else 16-byte
+//     cp.async pieces spread over the threads) fly into a shared-memory stage, all completing
+//     on one mbarrier; the next chunk's P scales travel as plain loads into registers (lane l
+//     of warp w holds peer 8 l + w's); a mean of a few peers without theta or statistics
+//     takes a lean shape instead (128 threads, four record stages, no theta stage, warp 0
+//     free of copies);
 //   - each warp unpacks whole records (one peer at a time): the 64 14-bit fields, a check that
 //     the indices ascend strictly and the scale is finite and non-negative, and the decoded
 //     value of every entry, stored as (position, value) pairs (+0.0 for a rejected record, an
@@ -35,7 +37,7 @@
 //     atomics at the end);
 //   - the dense pass divides by P (correctly rounded, with a precomputed reciprocal; one
 //     multiply when P is a power of two, whose reciprocal is exact), stores the mean and the
-//     updated theta with streaming stores and clears the accumulator.  Peers
+//     updated theta with plain 16-byte stores and clears the accumulator.  Peers
 //     are unpacked in groups of up to 64 (32 for k = 128 at L = 8192; at L = 4096 the k = 128
 //     entries are the raw 2-byte fields and a per-peer scale), so shared memory stays bounded
 //     for any P.
@@ -193,7 +195,8 @@ template <class Geo, bool kLean, bool kStats, bool kPow2>
 __global__ void __launch_bounds__(RecvShape<Geo, kLean, kStats>::kThreads, RecvShape<Geo, kLean, kStats>::kMinBlocks)
 k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __restrict__ mean,
                    float* __restrict__ theta_arg, float neg_lr, bool validate,
-                   PeerStats* __restrict__ stats, uint32_t* __restrict__ flags) {
+                   PeerStats* __restrict__ stats, uint32_t* __restrict__ flags, int ctas,
+                   int per_cta) {
     using S = RecvShape<Geo, kLean, kStats>;
     constexpr int kStages = S::kStages;
     // the lean shape is launched without theta: knowing so here drops its code and registers
@@ -227,8 +230,10 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
     const int lane = tid & 31;
     const int warp = tid >> 5;
     const int64_t C = (n + kChunk - 1) / kChunk;
-    const int64_t G = gridDim.x;
-    if (static_cast<int64_t>(blockIdx.x) >= C) return;
+    const int64_t G = ctas;   // between one CTA's chunks
+    const ChunkSpan span = cta_chunks(C, ctas, per_cta);
+    const int64_t end = span.end;
+    if (span.first >= end) return;
     const float pf = static_cast<float>(P);
     const int slice0 = kSlice * warp;    // this warp's positions: slice0 + 128 v + 4 lane + u
     constexpr int kSpl = S::kScalesPerLane;
@@ -253,21 +258,21 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
     }
     __syncthreads();
     for (int st = 0; st < kStages; ++st) {
-        const int64_t c = blockIdx.x + st * G;
-        if (c < C)
+        const int64_t c = span.first + st * G;
+        if (c < end)
             prefetch<Geo, S>(tab, P, c, C, (c + 1) * kChunk <= n, theta, &bars[st],
                      st_rec + st * P * kRecordBytes, st_theta + st * kChunk, tid);
     }
     float sc_cur[kSpl];
 #pragma unroll
     for (int i = 0; i < kSpl; ++i)
-        sc_cur[i] = my_peer[i] < P ? __ldcs(tab.scale[my_peer[i]] + blockIdx.x) : 0.0f;
+        sc_cur[i] = my_peer[i] < P ? __ldcs(tab.scale[my_peer[i]] + span.first) : 0.0f;
 
     bool bad = false;
     bool aborted = false;
     int it = 0;
-    int64_t c = blockIdx.x;
-    for (; c < C; c += G, ++it) {
+    int64_t c = span.first;
+    for (; c < end; c += G, ++it) {
         const int st = it % kStages;
         const uint32_t parity = static_cast<uint32_t>(it / kStages) & 1u;
         const uint8_t* rec = st_rec + st * P * kRecordBytes;
@@ -359,12 +364,12 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
                 }
                 // the stage has been read: start chunk c + S G's copies, and c + G's scales
                 const int64_t c2 = c + kStages * G;
-                if (c2 < C)
+                if (c2 < end)
                     prefetch<Geo, S>(tab, P, c2, C, (c2 + 1) * kChunk <= n, theta, &bars[st],
                              st_rec + st * P * kRecordBytes, st_theta + st * kChunk, tid);
 #pragma unroll
                 for (int i = 0; i < kSpl; ++i)
-                    if (my_peer[i] < P && c + G < C) sc_next[i] = __ldcs(tab.scale[my_peer[i]] + c + G);
+                    if (my_peer[i] < P && c + G < end) sc_next[i] = __ldcs(tab.scale[my_peer[i]] + c + G);
             } else {
                 __syncthreads();
             }
@@ -484,19 +489,17 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
             }
             if (!SPL_CHECK(j0 + 3 < kChunk, kSiteMean, j0)) continue;
             if (full) {
-                // the lean shape writes its mean with plain stores (0.0962 -> 0.0956 ms for the
-                // 8-peer mean of 2^27 values); the wide shape streams it (plain: 2.13 -> 2.17 ms)
-                if constexpr (kLean)
-                    *reinterpret_cast<float4*>(mean + base + j0) = m4;
-                else
-                    st_stream_f4(mean + base + j0, m4);
+                // plain stores: with the chunks in wave order they beat streaming (evict-first)
+                // ones, 2.031 against 2.050 ms for the 24-peer receive step at 2^30 values, and
+                // 0.0956 against 0.0962 ms for the 8-peer mean of 2^27 values
+                *reinterpret_cast<float4*>(mean + base + j0) = m4;
                 if (theta != nullptr) {
                     float4 t4 = th[v];
                     t4.x = __fmaf_rn(neg_lr, m4.x, t4.x);
                     t4.y = __fmaf_rn(neg_lr, m4.y, t4.y);
                     t4.z = __fmaf_rn(neg_lr, m4.z, t4.z);
                     t4.w = __fmaf_rn(neg_lr, m4.w, t4.w);
-                    st_stream_f4(theta + base + j0, t4);
+                    *reinterpret_cast<float4*>(theta + base + j0) = t4;
                 }
             } else {
                 const float m[4] = {m4.x, m4.y, m4.z, m4.w};
@@ -519,7 +522,7 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
         // wait runs out again, the block exits with a copy possibly in flight: reported)
         for (int k = 0; k < kStages; ++k) {
             const int it2 = it + k;
-            if (c + k * G < C &&
+            if (c + k * G < end &&
                 !mbar_wait(&bars[it2 % kStages], static_cast<uint32_t>(it2 / kStages) & 1u))
                 copy_pending = true;
         }
@@ -556,10 +559,11 @@ cudaError_t launch_kernel(const DecodeTable& tab, int P, int64_t n, int64_t C, f
     constexpr int kThreads = S::kThreads;
     const int resident = persistent_grid(kern, kThreads, smem);
     if (resident <= 0) return cudaErrorInvalidConfiguration;
-    const int grid = static_cast<int>(C < resident ? C : resident);
+    const int grid = wave_grid(C, resident, kRecvChunksPerCta);
     const float rp = 1.0f / static_cast<float>(P);   // correctly rounded on the host
     k_decode_aggregate<Geo, kLean, kStats, kPow2><<<grid, kThreads, smem, stream>>>(
-        tab, P, rp, n, mean, theta, -lr, validate || kStats, stats, flags);
+        tab, P, rp, n, mean, theta, -lr, validate || kStats, stats, flags, resident,
+        kRecvChunksPerCta);
     return cudaGetLastError();
 }
 

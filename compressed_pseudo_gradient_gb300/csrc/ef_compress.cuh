@@ -11,8 +11,10 @@
 //
 // Design (HBM-bound: 8 B read + 4 B written per fp32 value, 116 B written per chunk):
 //   - one 256-thread CTA per 4096-value chunk (L values for a variant; the figures below are
-//     the default codec's), grid-stride over chunks with a persistent grid (SMs x resident
-//     CTAs, four per SM); while a chunk is worked on, the next chunk's error buffer and delta
+//     the default codec's) at a time, four resident per SM; the grid runs in waves of the
+//     resident CTAs, each CTA taking 16 chunks spaced a wave apart, so the chunks in flight
+//     stay close together in memory (1.86 ms per 2^30 values against 2.00 ms with one
+//     persistent wave); while a chunk is worked on, the next chunk's error buffer and delta
 //     fly into a shared-memory stage as two 1-D bulk copies (TMA, no multicast, no cluster)
 //     completing on an mbarrier, whose wait is bounded in time;
 //   - each thread takes 16 values from the stage into registers (four 16-byte vectors at
@@ -627,7 +629,7 @@ __device__ __forceinline__ void code_and_pack(Sm& sm, uint8_t* __restrict__ payl
 template <class Geo, int kRule, bool kBf16, bool kEfHost>
 __global__ void __launch_bounds__(SendShape<Geo>::kThreads, SendShape<Geo>::kMinBlocks)
 k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload,
-              float* __restrict__ scales, uint32_t* __restrict__ flags) {
+              float* __restrict__ scales, uint32_t* __restrict__ flags, int ctas, int per_cta) {
     using S = SendShape<Geo>;
     constexpr int kChunk = S::kChunk;
     constexpr int kTopK = S::kTopK;
@@ -666,7 +668,8 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
     const int lane = tid & 31;
     const int warp = tid >> 5;
     const int64_t total = tab.chunk_begin[tab.num];
-    if (static_cast<int64_t>(blockIdx.x) >= total) return;
+    const ChunkSpan span = cta_chunks(total, ctas, per_cta);
+    if (span.first >= span.end) return;
 
     // thread 0 locates each chunk once, when it starts the chunk's copies, and leaves it in
     // shared memory for the CTA
@@ -677,7 +680,7 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
     if (tid == 0) {
         mbar_init(&sm.bar, 1);
         sm.next_tensor = 0;
-        const ChunkRef r0 = locate<kChunk, kBf16>(tab, blockIdx.x, sm.next_tensor);
+        const ChunkRef r0 = locate<kChunk, kBf16>(tab, span.first, sm.next_tensor);
         sm.next_delta = r0.delta;
         sm.next_ef = r0.ef;
         sm.next_valid = r0.valid;
@@ -695,9 +698,9 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
     int pend_valid = 0;
 
     // chunk indices stay below 2^31 (the host checks), so they are 32-bit here
-    const int total32 = static_cast<int>(total);
+    const int end32 = static_cast<int>(span.end);
     int it = 0;   // this CTA's iteration: kFast alternates the bitmaps by its parity
-    for (int c = blockIdx.x; c < total32; c += gridDim.x, ++it) {
+    for (int c = static_cast<int>(span.first); c < end32; c += ctas, ++it) {
         const int cur = kFast ? (it & 1) : 0;   // this chunk's bitmap: sm.sel_bm[cur]
         ChunkRef r;
         r.delta = sm.next_delta;
@@ -750,8 +753,8 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
         }
         // the stage has been read by every thread: start the next chunk's copies (and every
         // thread has read this chunk's location: replace it with the next one's)
-        if (tid == 0 && c + static_cast<int>(gridDim.x) < total32) {
-            const ChunkRef rn = locate<kChunk, kBf16>(tab, c + gridDim.x, sm.next_tensor);
+        if (tid == 0 && c + ctas < end32) {
+            const ChunkRef rn = locate<kChunk, kBf16>(tab, c + ctas, sm.next_tensor);
             sm.next_delta = rn.delta;
             sm.next_ef = rn.ef;
             sm.next_valid = rn.valid;
@@ -1101,9 +1104,9 @@ cudaError_t launch_compress(const CompressTable& tab, int64_t total, float beta,
     constexpr int kThreads = SendShape<Geo>::kThreads;
     const int resident = persistent_grid(kern, kThreads, smem);
     if (resident <= 0) return cudaErrorInvalidConfiguration;
-    const int grid = static_cast<int>(total < resident ? total : resident);
-    k_ef_compress<Geo, kRule, kBf16, kEfHost><<<grid, kThreads, smem, stream>>>(tab, beta, payload,
-                                                                                scales, flags);
+    const int grid = wave_grid(total, resident, kSendChunksPerCta);
+    k_ef_compress<Geo, kRule, kBf16, kEfHost><<<grid, kThreads, smem, stream>>>(
+        tab, beta, payload, scales, flags, resident, kSendChunksPerCta);
     return cudaGetLastError();
 }
 

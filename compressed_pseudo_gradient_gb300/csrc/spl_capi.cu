@@ -5,6 +5,7 @@
 #include <mutex>
 
 #include "spl.h"
+#include "spl_calib.h"
 #include "spl_device.cuh"
 #include "spl_kernels.h"
 #if SPL_CHECKED
@@ -394,6 +395,31 @@ spl_status spl_unpack(const uint8_t* payload, size_t num_chunks, uint16_t* idx, 
         return SPL_ERR_INVALID_ARG;
     return cuda_status(spl::launch_unpack(payload, static_cast<int64_t>(num_chunks), idx, codes,
                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+spl_status spl_calib_moves(spl_calib_pattern pattern, int persistent, const float* in0,
+                           const float* in1, float* out0, float* out1, size_t n,
+                           uint32_t* d_flags, spl_stream_t stream) {
+    const bool sender = pattern == SPL_CALIB_SENDER_MOVES;
+    if (!sender && pattern != SPL_CALIB_RECEIVER_MOVES) return SPL_ERR_INVALID_ARG;
+    if (n % SPL_CHUNK != 0 || n / SPL_CHUNK > kMaxChunks) return SPL_ERR_INVALID_ARG;
+    if (n == 0) return SPL_OK;
+    const float* other = sender ? in1 : out1;   // the pattern's second array
+    if (in0 == nullptr || out0 == nullptr || other == nullptr) return SPL_ERR_INVALID_ARG;
+    if (!aligned(in0, 16) || !aligned(out0, 16) || !aligned(other, 16)) return SPL_ERR_ALIGNMENT;
+    const size_t b = n * 4;
+    if (overlap(out0, b, in0, b) || overlap(out0, b, other, b) ||
+        (!sender && overlap(out1, b, in0, b)) || overlap(d_flags, 4, in0, b) ||
+        overlap(d_flags, 4, out0, b) || overlap(d_flags, 4, other, b))
+        return SPL_ERR_INVALID_ARG;
+    if (memory_type(in0) != cudaMemoryTypeDevice || memory_type(out0) != cudaMemoryTypeDevice ||
+        memory_type(other) != cudaMemoryTypeDevice)
+        return SPL_ERR_INVALID_ARG;
+    return cuda_status(spl::launch_calib_moves(sender, in0, sender ? in1 : nullptr, out0,
+                                               sender ? nullptr : out1,
+                                               static_cast<int64_t>(n / SPL_CHUNK),
+                                               persistent != 0, d_flags,
+                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

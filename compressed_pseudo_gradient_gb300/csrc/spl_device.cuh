@@ -161,6 +161,28 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t h16) {
     return __uint_as_float(h16 << 16);
 }
 
+// ---- which chunks a CTA works on ------------------------------------------------------------
+// A launch is a sequence of waves of `ctas` CTAs (as many as are resident on the GPU at once);
+// CTA b of wave w takes chunks w ctas K + b + j ctas for j = 0 .. K - 1 (K = per_cta), below
+// `total`, in that order.  The CTAs on the GPU at any moment thus work on one compact range of
+// chunks that advances through memory, and a CTA that runs ahead or behind can drift by at
+// most K chunks.  (With one persistent wave, CTAs drift apart over hundreds of chunks, the
+// addresses in flight spread over a wide range, and DRAM delivers less for the same bytes:
+// spl_calib_moves measures both schedules.)
+struct ChunkSpan {
+    int64_t first;   // this CTA's first chunk (none if >= end)
+    int64_t end;     // one past the last chunk of its wave; its chunks are first + j ctas < end
+};
+
+__device__ __forceinline__ ChunkSpan cta_chunks(int64_t total, int ctas, int per_cta) {
+    const int64_t w = blockIdx.x / ctas;
+    const int64_t base = w * ctas * per_cta;
+    ChunkSpan s;
+    s.first = base + blockIdx.x % ctas;
+    s.end = min(base + static_cast<int64_t>(ctas) * per_cta, total);
+    return s;
+}
+
 // ---- 1-D bulk copies (TMA, no multicast, no cluster launch) completed on an mbarrier ------
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

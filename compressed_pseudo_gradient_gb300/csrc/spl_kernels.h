@@ -91,6 +91,29 @@ cudaError_t launch_pack(const uint16_t* idx, const uint8_t* codes, int64_t C,
 cudaError_t launch_unpack(const uint8_t* payload, int64_t C, uint16_t* idx, uint8_t* codes,
                           cudaStream_t stream);
 
+// Chunks per CTA in the codec kernels' wave schedule (spl_device.cuh, cta_chunks): fewer keep
+// the chunks in flight closer together, more spread each CTA's start-up and final work (the
+// sender's last record, the receiver's first copies and accumulator clear) over more chunks.
+// Measured at 2^30 values: the sender 1.860 ms at 16 (1.860 at 8, 1.867 at 32), the 24-peer
+// receiver 2.050 ms at 32 (2.078 at 8, 2.057 at 16).  And the grid that covers `total` chunks
+// in waves of `resident` CTAs: one partial wave when everything fits in one, else whole waves
+// (the last one's surplus CTAs exit at once).
+constexpr int kSendChunksPerCta = 16;
+constexpr int kRecvChunksPerCta = 32;
+
+inline int wave_grid(int64_t total, int resident, int per_cta) {
+    const int64_t per_wave = static_cast<int64_t>(resident) * per_cta;
+    const int64_t waves = (total + per_wave - 1) / per_wave;
+    return static_cast<int>(waves <= 1 ? (total < resident ? total : resident) : waves * resident);
+}
+
+// Data-movement reference kernels (spl_calib.h), C chunks of 4,096 values: sender = the
+// sender's movement (out0 = in0 + in1), otherwise the receiver's (out0 = -in0, out1 = in0);
+// the codec kernels' wave schedule, or one persistent wave.
+cudaError_t launch_calib_moves(bool sender, const float* in0, const float* in1, float* out0,
+                               float* out1, int64_t C, bool persistent, uint32_t* flags,
+                               cudaStream_t stream);
+
 #if SPL_CHECKED
 // Checked build only: each translation unit's debug array (see spl_device.cuh), copied to out
 // (kDebugWords words) and cleared when reset is set.

@@ -20,8 +20,8 @@ def lib():
     return spl.library()
 
 
-def declared_functions():
-    text = open(HEADER).read()
+def declared_functions(header=HEADER):
+    text = open(header).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(spl_[a-z_]+)\s*\(", text)))
 
@@ -40,6 +40,15 @@ def test_library_exports_every_declared_symbol(lib):
     for fn in declared_functions():
         assert hasattr(lib, fn), f"{fn} declared in spl.h but not exported"
     assert os.path.exists(lib_build.LIB_PATH)
+
+
+def test_library_exports_the_calibration_call(lib):
+    """spl_calib.h declares the data-movement reference kernels' one call; both builds export
+    it."""
+    names = declared_functions(os.path.join(ROOT, "include", "spl_calib.h"))
+    assert names == ["spl_calib_moves"]
+    for path in (lib_build.LIB_PATH, lib_build.CHECKED_LIB_PATH):
+        assert hasattr(ctypes.CDLL(path), "spl_calib_moves")
 
 
 def test_checked_library_exports_the_same_calls_and_its_reader():
@@ -253,3 +262,22 @@ def test_header_is_plain_c_and_links(tmp_path, lib):
                     f"-Wl,-rpath,{libdir}"], check=True)
     out = subprocess.run([str(exe)], capture_output=True, text=True)
     assert out.returncode == 0 and out.stdout.strip() == "ok", out.stdout
+
+
+def test_calib_argument_errors(lib):
+    f = lib.spl_calib_moves
+    f.argtypes = [ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 4 + [ctypes.c_size_t] + \
+        [ctypes.c_void_p] * 2
+    n = 8192
+    for persistent in (0, 1):
+        g = lambda *a: f(a[0], persistent, *a[1:])   # noqa: E731
+        assert g(0, None, None, None, None, 0, None, None) == OK             # empty: no-op
+        assert g(2, A, B, Cp, None, n, None, None) == INVALID                # unknown pattern
+        assert g(0, A, B, Cp, None, n + 1, None, None) == INVALID            # not whole chunks
+        assert g(0, A, None, Cp, None, n, None, None) == INVALID             # sender without in1
+        assert g(1, A, B, Cp, None, n, None, None) == INVALID                # receiver, no out1
+        assert g(0, A + 4, B, Cp, None, n, None, None) == ALIGN
+        assert g(1, A, None, Cp, D + 8, n, None, None) == ALIGN
+        assert g(0, A, B, A + 1024, None, n, None, None) == INVALID          # out0 overlaps in0
+        assert g(1, A, None, Cp, A + 64, n, None, None) == INVALID           # out1 overlaps in0
+        assert g(0, A, B, Cp, None, n, Cp + 16, None) == INVALID             # flags in out0
