@@ -660,7 +660,7 @@ def run_hbm_mix(args, dev):
             kernels[f"the sender's movement (e and delta staged by bulk copies, plain stores), "
                     f"{order}"] = (lambda pers=pers: spl.calib_moves(
                         spl.CALIB_SENDER_MOVES, a, b, out0=c, persistent=pers), 12 * n)
-            kernels[f"the receiver's movement (theta staged, mean and theta streamed), "
+            kernels[f"the receiver's movement (theta staged, mean and theta stored), "
                     f"{order}"] = (lambda pers=pers: spl.calib_moves(
                         spl.CALIB_RECEIVER_MOVES, a, out0=c, out1=d, persistent=pers), 12 * n)
     peak, kind = read_peaks()

@@ -428,7 +428,7 @@ def calib_moves(pattern: int, in0: torch.Tensor, in1=None, *, out0=None, out1=No
     """Data-movement reference kernels (include/spl_calib.h), for roofline calibration, not the
     codec: CALIB_SENDER_MOVES moves the sender's bytes (out0 = in0 + in1, in0 and in1 staged
     by bulk copies, plain stores); CALIB_RECEIVER_MOVES the receiver's (out0 = -in0,
-    out1 = in0, in0 staged, streaming stores).  Chunks in the codec kernels' order, or with
+    out1 = in0, in0 staged, plain stores).  Chunks in the codec kernels' order, or with
     persistent=True in one persistent wave.  fp32 CUDA tensors, numel a multiple of 4096.
     Returns out0 (sender) or (out0, out1) (receiver)."""
     lib = library()

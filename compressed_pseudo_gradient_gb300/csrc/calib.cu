@@ -12,7 +12,7 @@ constexpr int kCalibThreads = 256;
 constexpr int kCalibCtasPerSm = 4;   // as the codec kernels run: 4 resident CTAs per SM
 
 // kSender: stage = [in0 chunk | in1 chunk], out0 = in0 + in1 with plain stores.
-// receiver: stage = [in0 chunk], out0 = -in0 and out1 = in0 with streaming stores.
+// receiver: stage = [in0 chunk], out0 = -in0 and out1 = in0 with plain stores.
 // Each thread handles 16 values, 4 vectors of 4 at j = v * 1024 + 4 * tid, as the codec
 // kernels do.
 template <bool kSender>
@@ -80,8 +80,8 @@ k_calib_moves(const float* __restrict__ in0, const float* __restrict__ in1,
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
                 const int64_t i = c * kCalibChunk + v * 1024 + 4 * tid;
-                st_stream_f4(out0 + i, r0[v]);
-                st_stream_f4(out1 + i, r1[v]);
+                *reinterpret_cast<float4*>(out0 + i) = r0[v];
+                *reinterpret_cast<float4*>(out1 + i) = r1[v];
             }
         }
     }

@@ -14,7 +14,7 @@
  *   SPL_CALIB_RECEIVER_MOVES out0[i] = -in0[i], out1[i] = in0[i]
  *       the receiver's dense movement with the outer step fused: per chunk, in0 (theta's place)
  *       arrives by one 16 KB bulk copy into one stage, and out0 (the mean's place) and out1
- *       (theta's) are written with streaming 16-byte stores; 12 bytes per value.  in1 is unused.
+ *       (theta's) are written with plain 16-byte stores; 12 bytes per value.  in1 is unused.
  *
  * persistent: 0: chunks in the codec kernel's order (waves of resident CTAs, 16 chunks each
  *           for the sender, 32 for the receiver);
