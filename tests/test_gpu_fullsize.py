@@ -201,3 +201,34 @@ def test_receive_24_peers_every_value():
     assert_close(host(theta), th_h, "theta")
     assert_bit_equal(host(mean), o_mean, "mean of 24 (fixed peer order)")
     assert_bit_equal(host(theta), th_h, "theta (one fma)")
+
+
+def test_several_waves_with_a_ragged_tail():
+    """A tensor of 40,000 chunks whose last chunk is partial: the sender and both receiver
+    shapes take several waves of CTAs (16 or 32 chunks per CTA, the last wave partial), and
+    every chunk, the tail included, matches the oracle; also through the checked build."""
+    n = 40000 * CHUNK - 1234
+    P = 3
+    gen = synth.generator(77, DEV)
+    pls, scs = [], []
+    for p in range(P):
+        d = synth.laplace(n, 1e-4, synth.generator(80 + p, DEV), DEV)
+        e = synth.normal(n, 1e-4, synth.generator(90 + p, DEV), DEV)
+        compress_round_every_chunk([d], [e], 0.95, f"ragged waves, peer {p}")
+        a, b = spl.ef_compress(d, e, 0.95)     # a second round, kept for the decode
+        pls.append(a), scs.append(b)
+        del d, e
+    pls_h, scs_h = [host(p) for p in pls], [host(s) for s in scs]
+    theta = synth.theta(n, gen, DEV)
+    th_h = host(theta)
+    flags = torch.zeros(1, dtype=torch.int32, device=DEV)
+    mean = spl.decode_aggregate(pls, scs, n, theta=theta, lr=0.7, flags=flags)   # wide shape
+    lean = spl.decode_aggregate(pls, scs, n, flags=flags)                         # lean shape
+    torch.cuda.synchronize()
+    (lean_chk, _) = checked_paths(lambda: spl.decode_aggregate(pls, scs, n))
+    assert torch.equal(lean_chk.view(torch.int32), lean.view(torch.int32))
+    o_mean, o_flags = oracle_decode(pls_h, scs_h, n, theta_h=th_h, lr=0.7)
+    assert int(flags.item()) == o_flags == 0
+    assert_bit_equal(host(mean), o_mean, "ragged waves: mean with theta")
+    assert_bit_equal(host(theta), th_h, "ragged waves: theta")
+    assert_bit_equal(host(lean), o_mean, "ragged waves: mean, lean shape")
