@@ -27,7 +27,7 @@ k_calib_moves(const float* __restrict__ in0, const float* __restrict__ in1,
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem_raw + kArrays * kBytes);
     const int tid = threadIdx.x;
     const int64_t G = ctas;
-    const ChunkSpan span = cta_chunks(C, ctas, per_cta);
+    const ChunkSpan span = cta_chunks(C, ctas, per_cta, blockIdx.x);
     if (span.first >= span.end) return;
     if (tid == 0) {
         mbar_init(bar, 1);

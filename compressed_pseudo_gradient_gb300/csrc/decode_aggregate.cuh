@@ -231,7 +231,7 @@ k_decode_aggregate(const DecodeTable tab, int P, float rp, int64_t n, float* __r
     const int warp = tid >> 5;
     const int64_t C = (n + kChunk - 1) / kChunk;
     const int64_t G = ctas;   // between one CTA's chunks
-    const ChunkSpan span = cta_chunks(C, ctas, per_cta);
+    const ChunkSpan span = cta_chunks(C, ctas, per_cta, blockIdx.x);
     const int64_t end = span.end;
     if (span.first >= end) return;
     const float pf = static_cast<float>(P);

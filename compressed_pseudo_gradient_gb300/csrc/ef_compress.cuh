@@ -668,7 +668,7 @@ k_ef_compress(const CompressTable tab, float beta, uint8_t* __restrict__ payload
     const int lane = tid & 31;
     const int warp = tid >> 5;
     const int64_t total = tab.chunk_begin[tab.num];
-    const ChunkSpan span = cta_chunks(total, ctas, per_cta);
+    const ChunkSpan span = cta_chunks(total, ctas, per_cta, blockIdx.x);
     if (span.first >= span.end) return;
 
     // thread 0 locates each chunk once, when it starts the chunk's copies, and leaves it in

@@ -174,12 +174,14 @@ struct ChunkSpan {
     int64_t end;     // one past the last chunk of its wave; its chunks are first + j ctas < end
 };
 
-__device__ __forceinline__ ChunkSpan cta_chunks(int64_t total, int ctas, int per_cta) {
-    const int64_t w = blockIdx.x / ctas;
+__host__ __device__ __forceinline__ ChunkSpan cta_chunks(int64_t total, int ctas, int per_cta,
+                                                         int64_t block) {
+    const int64_t w = block / ctas;
     const int64_t base = w * ctas * per_cta;
+    const int64_t wave_end = base + static_cast<int64_t>(ctas) * per_cta;
     ChunkSpan s;
-    s.first = base + blockIdx.x % ctas;
-    s.end = min(base + static_cast<int64_t>(ctas) * per_cta, total);
+    s.first = base + block % ctas;
+    s.end = wave_end < total ? wave_end : total;
     return s;
 }
 
