@@ -94,9 +94,11 @@ cudaError_t launch_unpack(const uint8_t* payload, int64_t C, uint16_t* idx, uint
 // Chunks per CTA in the codec kernels' wave schedule (spl_device.cuh, cta_chunks): fewer keep
 // the chunks in flight closer together, more spread each CTA's start-up and final work (the
 // sender's last record, the receiver's first copies and accumulator clear) over more chunks.
-// Measured at 2^30 values: the sender 1.860 ms at 16 (1.860 at 8, 1.867 at 32), the 24-peer
-// receiver 2.050 ms at 32 (2.078 at 8, 2.057 at 16; its lean 8-peer mean of 2^27 values
-// 0.0961 ms at 32 and 16, 0.0967 at 8).  And the grid that covers `total` chunks
+// Measured at 2^30 values: the sender 1.860 ms at 16 (1.860 at 8 and 12, 1.867-1.869 at 24
+// and 32; at 24 the decoder layer's multi-tensor round gains 0.8 % and the flat one loses
+// 0.5 %), the 24-peer receiver 2.032-2.050 ms at 32 (2.078 at 8, 2.057 at 16, 2.052 at 24,
+// 2.094 at 48, 2.077 at 64; its lean 8-peer mean of 2^27 values 0.0961 ms at 32 and 16,
+// 0.0967 at 8).  And the grid that covers `total` chunks
 // in waves of `resident` CTAs: one partial wave when everything fits in one, else whole waves
 // (the last one's surplus CTAs exit at once).
 constexpr int kSendChunksPerCta = 16;
