@@ -476,6 +476,48 @@ def kernel_split(info, evs, peak):
     return out
 
 
+def movement_record(dev, n: int, C: int, steps: int, warmup: int, comp_ms: float,
+                    dec_ms: float):
+    """Each kernel against its own data movement: the library's reference kernels
+    (spl_calib_moves) move the sender's and the receiver's dense bytes (12 B per value) the
+    way the kernels do, in their order of chunks, with none of the codec's arithmetic; scaled
+    to each kernel's algorithmic bytes (records and scales included) at the same rate, that
+    time is the floor the kernel's own access pattern sets.  Mean of `steps` after `warmup`."""
+    import torch
+    import compressed_pseudo_gradient_gb300 as spl
+    a = torch.rand(n, device=dev)
+    b = torch.rand(n, device=dev)
+    c = torch.empty(n, device=dev)
+    d = torch.empty(n, device=dev)
+    runs = {"sender": lambda: spl.calib_moves(spl.CALIB_SENDER_MOVES, a, b, out0=c),
+            "receiver": lambda: spl.calib_moves(spl.CALIB_RECEIVER_MOVES, a, out0=c, out1=d)}
+    out = {}
+    for name, fn in runs.items():
+        for _ in range(warmup):
+            fn()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        s0.record()
+        for _ in range(steps):
+            fn()
+        s1.record()
+        torch.cuda.synchronize(dev)
+        out[name] = s0.elapsed_time(s1) / steps
+    del a, b, c, d
+    torch.cuda.empty_cache()
+    comp_floor = out["sender"] * compress_bytes(n, C) / (12 * n)
+    dec_floor = out["receiver"] * decode_bytes(n, C, PEERS) / (12 * n)
+    return {"sender_moves_ms": round(out["sender"], 4),
+            "receiver_moves_ms": round(out["receiver"], 4),
+            "ef_compress": {"floor_ms": round(comp_floor, 4),
+                            "frac_of_own_movement": round(comp_floor / comp_ms, 4)},
+            "decode_aggregate": {"floor_ms": round(dec_floor, 4),
+                                 "frac_of_own_movement": round(dec_floor / dec_ms, 4)},
+            "note": "spl_calib_moves in the kernels' order of chunks; floor = its time scaled "
+                    "to the kernel's algorithmic bytes"}
+
+
 def other_workload_record(name: str, dev, steps: int, warmup: int):
     """A sub-record of the default line: `steps` rounds of another workload as plain calls,
     timed as a whole and per kernel, with the clocks sampled meanwhile."""
@@ -1073,18 +1115,21 @@ def main(argv=None):
     if rank != 0:
         return 0
     others = None
+    movement = None
+    n = args.elements
+    C = (n + CHUNK - 1) // CHUNK
     if world == 1 and not args.no_other_workloads and args.elements == N_ELEMS:
-        # the other two single-GPU workloads, timed per kernel after the headline step (their
-        # own buffers; the headline's are released first)
+        # the other two single-GPU workloads and the kernels' own data movement, timed after
+        # the headline step (their own buffers; the headline's are released first)
         import gc
         gc.collect()
         torch.cuda.empty_cache()
         steps = max(args.steps, 20)
+        movement = movement_record(dev, n, C, steps, args.warmup,
+                                   statistics.mean(r["comp_ms"]), statistics.mean(r["dec_ms"]))
         others = [other_workload_record(name, dev, steps, args.warmup)
                   for name in ("heavy_tail_bf16", "decoder_layer")]
 
-    n = args.elements
-    C = (n + CHUNK - 1) // CHUNK
     step_bytes = compress_bytes(n, C) + decode_bytes(n, C, PEERS)
     comp_avg = statistics.mean(r["comp_ms"]) / 1e3
     dec_avg = statistics.mean(r["dec_ms"]) / 1e3
@@ -1128,6 +1173,8 @@ def main(argv=None):
                        "d2h_bytes_per_step": e["d2h"], "steps": e["steps"]}
     if r["cpu"] is not None:
         line["cpu_baseline"] = r["cpu"]
+    if movement is not None:
+        line["config"]["data_movement"] = movement
     if others is not None:
         line["config"]["other_workloads"] = others
     print(json.dumps(line), flush=True)
