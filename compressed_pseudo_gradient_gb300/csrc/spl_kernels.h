@@ -98,12 +98,13 @@ cudaError_t launch_unpack(const uint8_t* payload, int64_t C, uint16_t* idx, uint
 // and 32; at 24 the decoder layer's multi-tensor round gains 0.8 % and the flat one loses
 // 0.5 %), the 24-peer receiver 2.032-2.050 ms at 32 (2.078 at 8, 2.057 at 16, 2.052 at 24,
 // 2.094 at 48, 2.077 at 64; its lean 8-peer mean of 2^27 values 0.0961 ms at 32 and 16,
-// 0.0967 at 8).  And the grid that covers `total` chunks
-// in waves of `resident` CTAs: one partial wave when everything fits in one, else whole waves
-// (the last one's surplus CTAs exit at once).
+// 0.0967 at 8).
 constexpr int kSendChunksPerCta = 16;
 constexpr int kRecvChunksPerCta = 32;
 
+// The grid that covers `total` chunks in waves of `resident` CTAs taking `per_cta` chunks
+// each: one partial wave when everything fits in one, else whole waves (the last one's
+// surplus CTAs exit at once).
 inline int wave_grid(int64_t total, int resident, int per_cta) {
     const int64_t per_wave = static_cast<int64_t>(resident) * per_cta;
     const int64_t waves = (total + per_wave - 1) / per_wave;
