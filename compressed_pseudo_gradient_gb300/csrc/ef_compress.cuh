@@ -1104,9 +1104,10 @@ cudaError_t launch_compress(const CompressTable& tab, int64_t total, float beta,
     constexpr int kThreads = SendShape<Geo>::kThreads;
     const int resident = persistent_grid(kern, kThreads, smem);
     if (resident <= 0) return cudaErrorInvalidConfiguration;
-    const int grid = wave_grid(total, resident, kSendChunksPerCta);
+    constexpr int kPerCta = kBf16 ? kSendChunksPerCtaBf16 : kSendChunksPerCta;
+    const int grid = wave_grid(total, resident, kPerCta);
     k_ef_compress<Geo, kRule, kBf16, kEfHost><<<grid, kThreads, smem, stream>>>(
-        tab, beta, payload, scales, flags, resident, kSendChunksPerCta);
+        tab, beta, payload, scales, flags, resident, kPerCta);
     return cudaGetLastError();
 }
 

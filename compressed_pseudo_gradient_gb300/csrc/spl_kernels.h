@@ -100,6 +100,8 @@ cudaError_t launch_unpack(const uint8_t* payload, int64_t C, uint16_t* idx, uint
 // 2.094 at 48, 2.077 at 64; its lean 8-peer mean of 2^27 values 0.0961 ms at 32 and 16,
 // 0.0967 at 8).
 constexpr int kSendChunksPerCta = 16;
+constexpr int kSendChunksPerCtaBf16 = 24;   // a bf16 delta: 2^27 heavy-tailed values 0.2260
+                                            // ms at 24, 0.2290 at 16, 0.2301 at 32
 constexpr int kRecvChunksPerCta = 32;
 
 // The grid that covers `total` chunks in waves of `resident` CTAs taking `per_cta` chunks
